@@ -1,0 +1,400 @@
+"""Pins for the fp64 oracle: checks against what the pages and the mathematics
+fix, never against the oracle itself.  Each pin takes an oracle library handle
+so that tests/test_oracle_mutants.py can run the same pins against builds of
+the oracle with planted mistakes.
+
+Sources (page title, section):
+  Speculative Decoding overview page (猜想解码 (Speculative Decoding) 全景):
+    考点2 acceptance probability, residual distribution, losslessness;
+    考点4 expected tokens per step; 第二章 acceptance formula;
+    第三章 NumPy operator and its self-test vectors.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+from scipy.special import softmax
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+F32, BF16 = 0, 1
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _ln(p):
+    with np.errstate(divide="ignore"):
+        return np.log(np.asarray(p, dtype=np.float64))
+
+
+def _batch(B, target_rows, draft_rows, x, u_acc, u_res, temp):
+    """Broadcast per-request row sets to a B-request fp32 batch."""
+    tr = np.asarray(target_rows, dtype=np.float32)
+    R, V = tr.shape
+    g = R - 1
+    dr = np.asarray(draft_rows, dtype=np.float32).reshape(g, V)
+    Lt = np.ascontiguousarray(np.broadcast_to(tr, (B, R, V)))
+    Ld = np.ascontiguousarray(np.broadcast_to(dr, (B, g, V)))
+    x = np.ascontiguousarray(np.broadcast_to(np.asarray(x, np.int32), (B, g)))
+    u_acc = np.ascontiguousarray(np.broadcast_to(np.asarray(u_acc, np.float32), (B, g)))
+    u_res = np.ascontiguousarray(np.broadcast_to(np.asarray(u_res, np.float32), (B, R)))
+    temp = np.ascontiguousarray(np.broadcast_to(np.asarray(temp, np.float32), (B,)))
+    return Lt, Ld, x, u_acc, u_res, temp
+
+
+def _midgrid(n):
+    return ((np.arange(n) + 0.5) / n).astype(np.float32)
+
+
+def _emitted(out):
+    return (out["tokens"] >= 0).sum(axis=1)
+
+
+# ---------------------------------------------------------------- page values
+
+def pin_worked_example(lib):
+    """考点2 / 第二章 worked example: P_draft = 0.5, P_target = 0.3 -> 0.6."""
+    g = _golden("worked_example.json")
+    pt, pd, pacc = g["p_target"], g["p_draft"], g["p_accept"]
+    n = 20000
+    u = _midgrid(n)
+    Lt, Ld, x, ua, ur, T = _batch(n, [_ln([pt, 0.5, 0.2]), _ln([1 / 3] * 3)],
+                                  [_ln([pd, 0.3, 0.2])], [0], 0.0, [0.5, 0.5], 1.0)
+    ua = u.reshape(n, 1).copy()
+    out = oracle.verify(Lt, Ld, x, ua, ur, T, F32, lib=lib)
+    assert np.allclose(out["pt"][:, 0], pt, rtol=1e-6)
+    assert np.allclose(out["pd"][:, 0], pd, rtol=1e-6)
+    acc = out["n"] == 1
+    assert abs(acc.mean() - pacc) <= 1.0 / n
+    far = np.abs(u.astype(np.float64) - pacc) > 1e-6
+    assert np.array_equal(acc[far], (u <= pacc)[far])
+    assert np.all(out["tokens"][acc, 0] == 0)
+
+
+def pin_numpy_operator_vectors(lib):
+    """第三章 self-test vectors: token 1 (ratio 1.5) and token 0 (ratio 1) are
+    always accepted; token 2 (ratio 1/3) is rejected for u > 1/3 and then the
+    residual [0, .2, 0, 0, 0] makes the resampled token always 1."""
+    g = _golden("numpy_operator_vectors.json")
+    pt, pd = g["p_target"], g["p_draft"]
+    d = g["derived_by_exact_arithmetic_from_the_vectors"]
+    n = 4000
+    u = _midgrid(n)
+    for tok, ratio in ((1, d["ratio_token_1"]), (0, d["ratio_token_0"]),
+                       (2, d["ratio_token_2"])):
+        Lt, Ld, x, ua, ur, T = _batch(n, [_ln(pt), _ln([0.2] * 5)], [_ln(pd)], [tok], 0.0,
+                                      [0.0, 0.5], 1.0)
+        ua = u.reshape(n, 1).copy()
+        ur = np.stack([u[::-1], np.full(n, 0.5, np.float32)], axis=1).copy()
+        out = oracle.verify(Lt, Ld, x, ua, ur, T, F32, lib=lib)
+        assert np.allclose(out["pt"][:, 0] / out["pd"][:, 0], ratio, rtol=1e-6)
+        if ratio >= 1.0:
+            assert np.all(out["n"] == 1) and np.all(out["tokens"][:, 0] == tok)
+        else:
+            far = np.abs(u.astype(np.float64) - ratio) > 1e-6
+            rej = out["n"] == 0
+            assert np.array_equal(rej[far], (u > ratio)[far])
+            assert np.all(out["tokens"][rej, 0] == d["resample_token_after_any_rejection"])
+            assert np.all(out["tokens"][rej, 1] == -1)
+            assert np.allclose(out["Z"][rej], sum(d["residual_unnormalised"]), rtol=1e-6)
+
+
+def pin_expected_tokens(lib):
+    """考点4: with a per-position acceptance probability alpha, the mean number
+    of emitted tokens is sum_{i=0..gamma} alpha^i; alpha -> 0 gives exactly 1.
+    Construction: V=8, T=1, logits ln p with p_t = (a, 1-a-6e, e..e),
+    p_d = (1-a-6e, a, e..e), a = (alpha-6e)/2, so sum_v min(p_t, p_d) = alpha,
+    rows independent of one another."""
+    g = _golden("expected_tokens.json")
+    gamma = g["gamma"]
+    rng = np.random.default_rng(7)
+    eps = 1e-3
+    for alpha_s, closed in g["closed_form_with_bonus"].items():
+        alpha = float(alpha_s)
+        a = (alpha - 6 * eps) / 2
+        p_t = np.array([a, 1 - a - 6 * eps] + [eps] * 6)
+        p_d = np.array([1 - a - 6 * eps, a] + [eps] * 6)
+        N = 200000
+        x = rng.choice(8, size=(N, gamma), p=p_d).astype(np.int32)
+        Lt, Ld, _, _, _, T = _batch(N, [_ln(p_t)] * (gamma + 1), [_ln(p_d)] * gamma,
+                                    [0] * gamma, 0.0, [0.0] * (gamma + 1), 1.0)
+        ua = rng.random((N, gamma), dtype=np.float32)
+        ur = rng.random((N, gamma + 1), dtype=np.float32)
+        out = oracle.verify(Lt, Ld, x, ua, ur, T, F32, lib=lib)
+        tokens = _emitted(out)
+        assert np.all(tokens == out["n"] + 1)
+        sd = tokens.std() / np.sqrt(N)
+        assert abs(tokens.mean() - closed) < 4 * sd + 1e-9, (alpha, tokens.mean(), closed)
+        nobonus = np.minimum(tokens, gamma)
+        want_nb = (1 - alpha ** gamma) / (1 - alpha)
+        assert abs(nobonus.mean() - want_nb) < 4 * nobonus.std() / np.sqrt(N) + 1e-9
+        assert abs(want_nb - g["page_printed"][alpha_s]) < 0.01
+    # alpha -> 0: disjoint supports, every step still emits exactly one token
+    p_t = np.array([0.25] * 4 + [0.0] * 4)
+    p_d = np.array([0.0] * 4 + [0.25] * 4)
+    N = 5000
+    x = rng.integers(4, 8, size=(N, gamma)).astype(np.int32)
+    Lt, Ld, _, _, _, T = _batch(N, [_ln(p_t)] * (gamma + 1), [_ln(p_d)] * gamma,
+                                [0] * gamma, 0.0, [0.0] * (gamma + 1), 1.0)
+    ua = np.maximum(rng.random((N, gamma), dtype=np.float32), np.float32(1e-7))
+    ur = rng.random((N, gamma + 1), dtype=np.float32)
+    out = oracle.verify(Lt, Ld, x, ua, ur, T, F32, lib=lib)
+    assert np.all(_emitted(out) == 1) and np.all(out["n"] == 0)
+    assert np.all(out["tokens"][:, 0] < 4)
+
+
+# ------------------------------------------------------------- mathematics
+
+def pin_losslessness_chisq(lib, trials=1_000_000):
+    """考点2 identity P_final == P_target: draft tokens drawn from P_draft, the
+    token emitted at position 0 (always emitted) follows P_target[0]; the token
+    at position 1, given that position 1 is reached, follows P_target[1].
+    Chi-square with 7 degrees of freedom, rejected above 24.32 (p = 0.001)."""
+    rng = np.random.default_rng(2026)
+    V, gamma, T = 8, 2, float(np.float32(0.7))
+    lt = rng.normal(0, 1.5, size=(gamma + 1, V)).astype(np.float32)
+    ld = rng.normal(0, 1.5, size=(gamma, V)).astype(np.float32)
+    Pt = softmax(lt.astype(np.float64) / T, axis=1)
+    Pd = softmax(ld.astype(np.float64) / T, axis=1)
+    x = np.stack([rng.choice(V, size=trials, p=Pd[i]) for i in range(gamma)], axis=1)
+    Lt, Ld, _, _, _, Tb = _batch(trials, lt, ld, [0] * gamma, 0.0, [0.0] * (gamma + 1), T)
+    ua = rng.random((trials, gamma), dtype=np.float32)
+    ur = rng.random((trials, gamma + 1), dtype=np.float32)
+    out = oracle.verify(Lt, Ld, x.astype(np.int32), ua, ur, Tb, F32, lib=lib)
+    for pos in range(2):
+        reached = out["n"] >= pos
+        toks = out["tokens"][reached, pos]
+        assert np.all(toks >= 0)
+        obs = np.bincount(toks, minlength=V)
+        exp_ = Pt[pos] * reached.sum()
+        chi2 = float(((obs - exp_) ** 2 / exp_).sum())
+        assert chi2 < 24.32, (pos, chi2)
+
+
+def pin_brute_force_tiny(lib):
+    """Brute force at V=4, gamma=3: every point of a u_acc grid gives the
+    first-rejection index of the plain rule (u_i > r_i, r from the textbook
+    softmax), the frequencies of k match prod r_i (1 - r_k) within grid
+    resolution, and for each k the token over a u_res grid equals the
+    index-order inverse CDF of max(0, P_t - P_d) (np.searchsorted on the
+    cumulative sum, side='right'), with frequencies w/Z within 1/n."""
+    rng = np.random.default_rng(11)
+    V, gamma, T = 4, 3, float(np.float32(0.9))
+    lt = rng.normal(0, 1.2, size=(gamma + 1, V)).astype(np.float32)
+    ld = rng.normal(0, 1.2, size=(gamma, V)).astype(np.float32)
+    Pt = softmax(lt.astype(np.float64) / T, axis=1)
+    Pd = softmax(ld.astype(np.float64) / T, axis=1)
+    xs = np.array([int(np.argmax(Pd[i])) for i in range(gamma)], np.int32)
+    r = np.minimum(1.0, Pt[np.arange(gamma), xs] / Pd[np.arange(gamma), xs])
+    n = 24
+    grid = _midgrid(n)
+    mesh = np.stack(np.meshgrid(*([grid] * gamma), indexing="ij"), -1).reshape(-1, gamma)
+    N = mesh.shape[0]
+    Lt, Ld, x, _, ur, Tb = _batch(N, lt, ld, xs, 0.0, [0.5] * (gamma + 1), T)
+    out = oracle.verify(Lt, Ld, x, mesh.copy(), ur, Tb, F32, lib=lib)
+    rej = mesh.astype(np.float64) > r[None, :]
+    k_rule = np.where(rej.any(1), rej.argmax(1), gamma)
+    far = np.all(np.abs(mesh.astype(np.float64) - r[None, :]) > 1e-6, axis=1)
+    assert np.array_equal(out["n"][far], k_rule[far])
+    for k in range(gamma + 1):
+        want = np.prod(r[:k]) * ((1 - r[k]) if k < gamma else 1.0)
+        assert abs((out["n"] == k).mean() - want) <= gamma * 0.5 / n + 1e-12
+    m = 10000
+    ug = _midgrid(m)
+    for k in range(gamma + 1):
+        ua = np.zeros((m, gamma), np.float32)
+        if k < gamma:
+            if r[k] >= 1.0:
+                continue
+            ua[:, k] = np.float32(0.9999999)
+            w = np.maximum(0.0, Pt[k] - Pd[k])
+        else:
+            w = Pt[gamma].copy()
+        ur = np.zeros((m, gamma + 1), np.float32)
+        ur[:, k] = ug
+        Lt, Ld, x, _, _, Tb = _batch(m, lt, ld, xs, 0.0, [0.0] * (gamma + 1), T)
+        out = oracle.verify(Lt, Ld, x, ua, ur, Tb, F32, lib=lib)
+        assert np.all(out["n"] == k)
+        cum = np.cumsum(w)
+        want = np.searchsorted(cum, ug.astype(np.float64) * cum[-1], side="right")
+        nearb = np.min(np.abs(cum[None, :] / cum[-1] - ug.astype(np.float64)[:, None]), 1) < 1e-6
+        got = out["tokens"][:, k]
+        assert np.array_equal(got[~nearb], want[~nearb])
+        freq = np.bincount(got, minlength=V) / m
+        assert np.all(np.abs(freq - w / w.sum()) <= 1.0 / m + 1e-12)
+
+
+def pin_accept_boundary(lib):
+    """Reading R1 (accept iff u <= r) and R2 (P_draft(x) = 0 -> accept),
+    on rows whose probabilities are exact in binary: p_t = 1/4 each,
+    p_d = (1/2, 1/2, 0, 0), so r = 1/2 for token 0 exactly."""
+    z = 0.0
+    ninf = -np.inf
+    lt = [[z, z, z, z], [z, z, z, z]]
+    ld = [[z, z, ninf, ninf]]
+    half = np.float32(0.5)
+    above = np.nextafter(half, np.float32(1))
+    ua = np.array([[half], [above], [0.0], [0.999]], np.float32)
+    Lt, Ld, x, _, ur, T = _batch(4, lt, ld, [0], 0.0, [0.3, 0.3], 1.0)
+    x = np.array([[0], [0], [2], [2]], np.int32)  # token 2: P_draft = 0 -> r = 1
+    out = oracle.verify(Lt, Ld, x, ua, ur, T, F32, lib=lib)
+    assert list(out["n"]) == [1, 0, 1, 1]
+    # P_target(x) = 0 gives r = 0: only u = 0 is accepted
+    lt2 = [[ninf, z, z, z], [z, z, z, z]]
+    Lt, Ld, x, _, ur, T = _batch(2, lt2, [[z, z, z, z]], [0], 0.0, [0.3, 0.3], 1.0)
+    out = oracle.verify(Lt, Ld, x, np.array([[0.0], [1e-7]], np.float32), ur, T, F32, lib=lib)
+    assert list(out["n"]) == [1, 0]
+
+
+def pin_inverse_cdf_strict(lib):
+    """Reading R5: the token is the smallest v whose running residual mass
+    exceeds u * Z (strict), so a zero-mass token is never emitted, even at
+    u = 0.  p_t = (.2, .5, .3), p_d = (.4, .1, .5): residual (0, .4, 0)."""
+    lt = [_ln([0.2, 0.5, 0.3]), _ln([1 / 3] * 3)]
+    ld = [_ln([0.4, 0.1, 0.5])]
+    us = np.array([0.0, 0.25, 0.5, 0.9999999], np.float32)
+    Lt, Ld, x, _, _, T = _batch(len(us), lt, ld, [0], 0.0, [0.0, 0.0], 1.0)
+    ur = np.stack([us, us], 1).copy()
+    out = oracle.verify(Lt, Ld, x, np.full((len(us), 1), 0.9999, np.float32), ur, T, F32,
+                        lib=lib)
+    assert np.all(out["n"] == 0) and np.all(out["tokens"][:, 0] == 1)
+    # residual (0.1, 0, 0.3): u = 0 -> token 0; u = 0.2 -> 0; u = 0.3 -> 2
+    lt = [_ln([0.3, 0.2, 0.5]), _ln([1 / 3] * 3)]
+    ld = [_ln([0.2, 0.6, 0.2])]
+    us = np.array([0.0, 0.2, 0.3, 0.9], np.float32)
+    Lt, Ld, x, _, _, T = _batch(len(us), lt, ld, [1], 0.0, [0.0, 0.0], 1.0)
+    ur = np.stack([us, us], 1).copy()
+    out = oracle.verify(Lt, Ld, x, np.full((len(us), 1), 0.9999, np.float32), ur, T, F32,
+                        lib=lib)
+    assert list(out["tokens"][:, 0]) == [0, 0, 2, 2]
+
+
+def pin_softmax_textbook(lib):
+    """Softmax against the textbook definition: ln p logits at T = 1 give p
+    back; tempered rows match softmax(l / T); logits near 1000 (which overflow
+    exp without the max shift) and -inf entries stay exact."""
+    rng = np.random.default_rng(5)
+    V = 7
+    p = rng.dirichlet(np.ones(V))
+    lt = np.stack([_ln(p), _ln(p)])
+    ld = rng.normal(0, 2, size=(1, V))
+    xs = np.arange(V, dtype=np.int32).reshape(V, 1)
+    Lt, Ld, _, _, ur, T = _batch(V, lt, ld, [0], 0.0, [0.5, 0.5], 1.0)
+    out = oracle.verify(Lt, Ld, xs, np.zeros((V, 1), np.float32), ur, T, F32, lib=lib)
+    assert np.allclose(out["pt"][:, 0], p, rtol=2e-6)
+    for T, shift in ((0.37, 0.0), (2.5, 0.0), (1.0, 1000.0), (0.8, -1000.0)):
+        lt = (rng.normal(0, 3, size=(2, V)) + shift).astype(np.float32)
+        lt[0, 3] = -np.inf
+        ld = (rng.normal(0, 3, size=(1, V)) + shift).astype(np.float32)
+        Lt, Ld, _, _, ur, Tb = _batch(V, lt, ld, [0], 0.0, [0.5, 0.5], T)
+        out = oracle.verify(Lt, Ld, xs, np.zeros((V, 1), np.float32), ur, Tb, F32, lib=lib)
+        assert np.all(out["flags"] & oracle.INVALID_ANY == 0)
+        T32 = float(np.float32(T))  # the oracle sees the stored fp32 temperature
+        wt = softmax(lt[0].astype(np.float64) / T32)
+        wd = softmax(ld[0].astype(np.float64) / T32)
+        assert np.allclose(out["pt"][:, 0], wt, rtol=1e-12, atol=0)
+        assert np.allclose(out["pd"][:, 0], wd, rtol=1e-12, atol=0)
+
+
+def pin_degenerate_shapes(lib):
+    """gamma = 0 (plain sampling from target row 0: over a u grid the token
+    frequencies are P_t[0] within 1/n) and V = 1 (every draft accepted)."""
+    rng = np.random.default_rng(3)
+    V, n = 6, 6000
+    lt = rng.normal(0, 1, size=(1, V)).astype(np.float32)
+    Lt = np.ascontiguousarray(np.broadcast_to(lt, (n, 1, V)))
+    Ld = np.zeros((n, 0, V), np.float32)
+    ur = _midgrid(n).reshape(n, 1)
+    out = oracle.verify(Lt, Ld, np.zeros((n, 0), np.int32), np.zeros((n, 0), np.float32), ur,
+                        np.ones(n, np.float32), F32, lib=lib)
+    assert np.all(out["n"] == 0)
+    freq = np.bincount(out["tokens"][:, 0], minlength=V) / n
+    assert np.all(np.abs(freq - softmax(lt[0].astype(np.float64))) <= 1.0 / n + 1e-12)
+    g = 3
+    Lt = rng.normal(0, 1, size=(5, g + 1, 1)).astype(np.float32)
+    Ld = rng.normal(0, 1, size=(5, g, 1)).astype(np.float32)
+    out = oracle.verify(Lt, Ld, np.zeros((5, g), np.int32), rng.random((5, g), np.float32),
+                        rng.random((5, g + 1), np.float32), np.ones(5, np.float32), F32, lib=lib)
+    assert np.all(out["n"] == g) and np.all(out["tokens"] == 0)
+
+
+def pin_invalid_inputs(lib):
+    """Reading R7/R8: bad temperature, NaN / +inf / all -inf rows and
+    out-of-range draft tokens invalidate only their own request."""
+    rng = np.random.default_rng(9)
+    B, g, V = 12, 2, 16
+    Lt = rng.normal(0, 1, size=(B, g + 1, V)).astype(np.float32)
+    Ld = rng.normal(0, 1, size=(B, g, V)).astype(np.float32)
+    x = rng.integers(0, V, size=(B, g)).astype(np.int32)
+    T = np.ones(B, np.float32)
+    Lt[1, 0, 5] = np.nan
+    Ld[2, 1, 0] = np.inf
+    Lt[3, 2, :] = -np.inf
+    x[4, 1] = V
+    x[5, 0] = -1
+    T[6], T[7], T[8], T[9] = 0.0, -1.0, np.nan, np.float32(1e-39)
+    T[10] = np.inf
+    Lt[11, 1, :] = -np.inf
+    Lt[11, 1, 3] = 0.0  # -inf entries are legal while one entry is finite
+    out = oracle.verify(Lt, Ld, x, rng.random((B, g), np.float32),
+                        rng.random((B, g + 1), np.float32), T, F32, lib=lib)
+    fl = out["flags"]
+    assert fl[0] & oracle.INVALID_ANY == 0 and fl[11] & oracle.INVALID_ANY == 0
+    for b in (1, 2, 3):
+        assert fl[b] & oracle.INVALID_NONFINITE
+    for b in (4, 5):
+        assert fl[b] & oracle.INVALID_TOKEN
+    for b in (6, 7, 8, 9, 10):
+        assert fl[b] & oracle.INVALID_TEMP
+    for b in range(1, 11):
+        assert out["n"][b] == 0 and np.all(out["tokens"][b] == -1)
+
+
+def pin_greedy(lib):
+    """Reading R9 against the textbook argmax (np.argmax returns the first
+    maximal index), with planted ties, on bf16 logits."""
+    rng = np.random.default_rng(13)
+    B, g, V = 40, 5, 300
+    lt = rng.normal(0, 3, size=(B, g + 1, V)).astype(np.float32)
+    bits = (lt.view(np.uint32) >> 16).astype(np.uint16)  # truncate to bf16
+    wide = (bits.astype(np.uint32) << 16).view(np.float32)
+    for b in range(0, B, 3):  # plant a tie: copy the max to a later and an earlier index
+        for i in range(g + 1):
+            a = int(np.argmax(wide[b, i]))
+            bits[b, i, (a + 7) % V] = bits[b, i, a]
+            if b % 2 == 0 and a > 0:
+                bits[b, i, a - 1] = bits[b, i, a]
+    wide = (bits.astype(np.uint32) << 16).view(np.float32)
+    amax = np.argmax(wide, axis=2)
+    x = amax[:, :g].copy().astype(np.int32)
+    kk = rng.integers(0, g + 1, size=B)
+    for b in range(B):
+        if kk[b] < g:
+            x[b, kk[b]] = (amax[b, kk[b]] + 1) % V
+    out = oracle.greedy(bits, x, BF16, lib=lib)
+    assert np.array_equal(out["argmax"], amax)
+    assert np.array_equal(out["n"], kk)
+    for b in range(B):
+        k = kk[b]
+        assert np.array_equal(out["tokens"][b, :k], amax[b, :k])
+        assert out["tokens"][b, k] == amax[b, k]
+        assert np.all(out["tokens"][b, k + 1:] == -1)
+    bits[0, 2, 9] = 0x7FC0  # NaN
+    bits[1, 0, :] = 0xFF80  # all -inf
+    x[2, 0] = V
+    out = oracle.greedy(bits, x, BF16, lib=lib)
+    for b in range(3):
+        assert out["flags"][b] & oracle.INVALID_ANY and out["n"][b] == 0
+        assert np.all(out["tokens"][b] == -1)
+
+
+ALL_PINS = [pin_worked_example, pin_numpy_operator_vectors, pin_expected_tokens,
+            pin_losslessness_chisq, pin_brute_force_tiny, pin_accept_boundary,
+            pin_inverse_cdf_strict, pin_softmax_textbook, pin_degenerate_shapes,
+            pin_invalid_inputs, pin_greedy]
