@@ -1,0 +1,351 @@
+"""Benchmark of the speculative-decoding verification step on GB300.
+
+One step = one spec_verify call over one batch of the headline workload
+(default c4: B=256 requests, gamma=4, V=151936, bf16 logits, T=1; the
+largest-vocabulary workload, 700 MB of logits per step).  The metric is
+verified draft positions per second (B * gamma per step) with the achieved
+HBM bandwidth reported in `roofline`.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c4]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Inputs are synthetic (seeded Philox, see speculative_decoding_verification_09_gb300/synth.py),
+generated on the host and copied to the device once; three input sets rotate
+so every step reads its 700 MB from HBM (3 x 700 MB >> 129 MB L2).
+Multi-GPU (torchrun): every rank verifies its own batch (independent
+requests, no collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verification_09_gb300 import synth  # noqa: E402
+
+METRIC = "verified draft positions/sec and achieved HBM GB/s (fraction of GB300 peak)"
+UNIT = "positions/s"
+KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_09_gb300", "csrc",
+                          "specverify.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_c4.txt")
+WORKLOADS = {f"c{i}": i for i in synth.CONFIGS}
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def read_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def read_traffic() -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernel source as it is now (else None)."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") != kernel_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def oracle_positions_per_s(inp: synth.Inputs, n_req: int, threads: int) -> tuple[float, float]:
+    import oracle
+    sl = slice(0, n_req)
+    t0 = time.perf_counter()
+    oracle.verify(inp.Lt[sl], inp.Ld[sl], inp.x[sl], inp.u_acc[sl], inp.u_res[sl],
+                  inp.temp[sl], inp.dtype, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return n_req * inp.gamma / dt, dt
+
+
+def run_reference(args) -> None:
+    """The reference arm: the fp64 CPU oracle as it stands, on the host cores,
+    timed on bounded samples of the same workload."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cid = WORKLOADS[args.workload]
+    n_req = args.ref_requests
+    inp = synth.make_inputs(cid, B=n_req)
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle_positions_per_s(inp, n_req, cores)
+    times = []
+    for _ in range(args.steps):
+        times.append(oracle_positions_per_s(inp, n_req, cores)[1])
+    t = float(np.mean(times))
+    value = n_req * inp.gamma / t
+    cfg = synth.CONFIGS[cid]
+    sample = f"first {n_req} of {cfg['B']} requests of {cfg['name']} per step, fp64, {cores} threads"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": cfg["name"], "B": n_req,
+                                        "gamma": cfg["gamma"], "V": cfg["V"]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_ours(args) -> None:
+    import torch
+
+    from speculative_decoding_verification_09_gb300 import binding
+
+    ws_n, rank, local = dist_env()
+    pg = None
+    if ws_n > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        pg = dist
+    dev = torch.device("cuda", local if ws_n > 1 else 0)
+    torch.cuda.set_device(dev)
+    cid = WORKLOADS[args.workload]
+    cfg = synth.CONFIGS[cid]
+    B, g, V = cfg["B"], cfg["gamma"], cfg["V"]
+    greedy = cfg["kind"] == "greedy"
+    stream = torch.cuda.current_stream(dev)
+
+    # input sets: host copies (pinned, for the end-to-end leg) and device copies
+    host_sets = [synth.make_inputs(cid, set_index=1000 * rank + s) for s in range(args.sets)]
+    logit_bytes = host_sets[0].Lt.nbytes if greedy else host_sets[0].logit_bytes
+
+    def dev_tensors(inp):
+        t = {k: torch.from_numpy(np.ascontiguousarray(getattr(inp, k))).to(dev)
+             for k in ("Lt", "Ld", "x", "u_acc", "u_res", "temp")}
+        if inp.dtype == synth.BF16:
+            t["Lt"], t["Ld"] = t["Lt"].view(torch.bfloat16), t["Ld"].view(torch.bfloat16)
+        return t
+
+    sets = [dev_tensors(h) for h in host_sets]
+    out_tok = torch.empty(B, g + 1, dtype=torch.int32, device=dev)
+    out_n = torch.empty(B, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = binding.make_workspace(B, g, V, dev)
+
+    def step(t):
+        if greedy:
+            binding.spec_verify_greedy(t["Lt"], t["x"], out_tok, out_n, ws, status, stream)
+        else:
+            binding.spec_verify(t["Lt"], t["Ld"], t["x"], t["u_acc"], t["u_res"], t["temp"],
+                                out_tok, out_n, ws, status, stream)
+
+    for i in range(args.warmup):
+        step(sets[i % len(sets)])
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    if not args.no_clocks:
+        clocks.start()
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(sets[i % len(sets)])
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    if pg:
+        pg.barrier()
+    clk = clocks.stop() if not args.no_clocks else None
+    total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    if pg:
+        tt = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    st = int(status.item())
+    ms_step = total_ms / args.steps
+    positions = B * g * ws_n * args.steps
+    value = positions / (total_ms / 1e3)
+    launch_ms = float(np.mean(per_launch))
+    peak, peak_kind = read_peaks()
+    achieved = logit_bytes / (launch_ms / 1e3) / 1e9
+
+    # end to end: pinned host inputs -> device, verify, results -> host, every step
+    e2e = None
+    if not args.no_e2e:
+        h = host_sets[0]
+        pinned = {k: torch.from_numpy(np.ascontiguousarray(getattr(h, k))).pin_memory()
+                  for k in ("Lt", "Ld", "x", "u_acc", "u_res", "temp")}
+        d = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pinned.items()}
+        tok_h = torch.empty(B, g + 1, dtype=torch.int32).pin_memory()
+        n_h = torch.empty(B, dtype=torch.int32).pin_memory()
+        keys = ("Lt", "x") if greedy else ("Lt", "Ld", "x", "u_acc", "u_res", "temp")
+        h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in keys)
+        d2h = tok_h.numel() * 4 + n_h.numel() * 4
+
+        def e2e_step():
+            for k in keys:
+                d[k].copy_(pinned[k], non_blocking=True)
+            t = dict(d)
+            if h.dtype == synth.BF16:
+                t["Lt"], t["Ld"] = d["Lt"].view(torch.bfloat16), d["Ld"].view(torch.bfloat16)
+            step(t)
+            tok_h.copy_(out_tok, non_blocking=True)
+            n_h.copy_(out_n, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        k_e2e = max(3, min(args.steps, 10))
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(b_) / k_e2e
+        e2e = {"value": B * g / (e_ms / 1e3), "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        n_req = min(B, args.cpu_requests)
+        v, dt = oracle_positions_per_s(host_sets[0], n_req, cores)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {n_req} of {B} requests of {cfg['name']} (set 0), fp64, "
+                         f"{cores} threads, {dt:.2f} s wall"}
+
+    if rank != 0:
+        return
+    traffic = read_traffic() if cid == 4 else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": cfg["name"], "B": B, "gamma": g, "V": V, "greedy": greedy,
+                   "logit_bytes_per_step": int(logit_bytes),
+                   "l2": f"{args.sets} rotating input sets of {logit_bytes / 1e6:.0f} MB "
+                         f"(each larger than the 129 MB L2)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                     "kernel_ms": launch_ms},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
+        "status": st, "wall_s_timed": t_wall,
+    }
+    print(json.dumps(line))
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c4")
+    ap.add_argument("--sets", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-requests", type=int, default=256)
+    ap.add_argument("--ref-requests", type=int, default=32)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,146 @@
+/*
+ * specverify.h -- C ABI of the GB300 (sm_103a) speculative-decoding
+ * verification library (libspecverify.so).
+ *
+ * The operation (Speculative Decoding overview page, "猜想解码 (Speculative
+ * Decoding) 全景", sections 考点2, 第二章 and 第三章; the deferred-speculation
+ * page's scheduler section "动态推迟投机验证调度器设计"):
+ *
+ *   for every request b, with temperature T_b, target rows i = 0..gamma and
+ *   draft rows i = 0..gamma-1 over a vocabulary of V entries:
+ *     P_t[i] = softmax(Lt[b][i] / T_b),  P_d[i] = softmax(Ld[b][i] / T_b)
+ *     r_i    = min(1, P_t[i][x_i] / P_d[i][x_i])      (r_i = 1 when P_d[i][x_i] = 0)
+ *     accept x_i iff u_accept[b][i] <= r_i; k = first i that is not accepted,
+ *     or gamma when all are
+ *     k < gamma: w = max(0, P_t[k] - P_d[k])  (residual distribution)
+ *     k = gamma: w = P_t[gamma]              (bonus token)
+ *     token k = smallest v with sum_{j<=v} w_j > u_resample[b][k] * sum_j w_j
+ *   outputs: out_tokens[b] = (x_0 .. x_{k-1}, token k, -1 ...), out_num_accepted[b] = k.
+ *
+ * Layouts (all row-major, contiguous):
+ *   target_logits  [B][gamma+1][V]   dtype (SV_F32: float, SV_BF16: bfloat16 bits)
+ *   draft_logits   [B][gamma][V]     dtype
+ *   draft_tokens   [B][gamma]        int32, expected in [0, V)
+ *   u_accept       [B][gamma]        float, in [0, 1)
+ *   u_resample     [B][gamma+1]      float, in [0, 1); only entry k is used
+ *   temperature    [B]               float, finite and >= 2^-126
+ *   out_tokens     [B][gamma+1]      int32, -1 padded
+ *   out_num_accepted [B]             int32, in [0, gamma]
+ *
+ * Conventions:
+ *   - Every pointer is a DEVICE pointer owned by the caller (logit pointers
+ *     aligned to their element size, all others to 4 bytes); the library
+ *     allocates nothing.  Calls are enqueued on `stream` (a cudaStream_t;
+ *     NULL = legacy default stream) and return before the work finishes.
+ *   - The return value reports only what the host can see: a bad argument, a
+ *     too small workspace, or a failed launch.  Data errors are reported per
+ *     request on the device: that request gets out_num_accepted = 0 and
+ *     out_tokens all -1, and the matching SV_ST_* bit is OR-ed into
+ *     *dev_status (when dev_status is not NULL).  Nothing traps.
+ *   - -inf logits are legal (probability 0).  NaN or +inf anywhere in a
+ *     request's rows, an all -inf row, a draft token outside [0, V) or a bad
+ *     temperature invalidate that request only.
+ *   - workspace: sv_workspace_bytes() bytes of device memory, 256-byte
+ *     aligned, zeroed ONCE before its first use (sv_workspace_init); every
+ *     call leaves it ready for the next one.  Calls that may overlap on the
+ *     GPU (different streams) need separate workspaces.
+ *   - The library is thread-safe apart from sv_set_tuning().
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* logit storage types */
+enum { SV_F32 = 0, SV_BF16 = 1 };
+
+/* host return codes */
+enum {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1, /* NULL pointer, B < 0, gamma outside [0, SV_MAX_GAMMA], V < 1, misalignment */
+  SV_ERR_DTYPE = 2,       /* dtype is neither SV_F32 nor SV_BF16 */
+  SV_ERR_CUDA = 3,        /* a CUDA runtime call or the launch failed */
+  SV_ERR_WORKSPACE = 4    /* workspace NULL, unaligned or smaller than sv_workspace_bytes() */
+};
+
+/* device status bits, OR-ed into *dev_status */
+#define SV_ST_NONFINITE 0x1   /* NaN / +inf logit, or an all -inf row, in a request */
+#define SV_ST_BAD_TOKEN 0x2   /* a draft token outside [0, V) */
+#define SV_ST_BAD_TEMP 0x4    /* temperature not finite or below 2^-126 */
+#define SV_ST_TIMEOUT 0x8     /* an internal wait gave up (results of the call are void) */
+#define SV_ST_WORKSPACE 0x10  /* workspace was not in its ready state (results void; it is
+                                 repaired by the call that reports this) */
+#define SV_ST_DEGENERATE 0x20 /* informational: a residual summed to 0 and the target row
+                                 was sampled instead */
+
+#define SV_MAX_GAMMA 32
+
+/* Bytes of workspace needed for any call with these sizes (any dtype). */
+size_t sv_workspace_bytes(int B, int gamma, int V);
+
+/* Zero a workspace on `stream` (a cudaMemsetAsync).  Call once after
+ * allocating it, or after a call reported SV_ST_TIMEOUT. */
+int sv_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Sampling verification (T > 0) for B requests -- the operation above.
+ * dev_status may be NULL.  For gamma == 0, draft_logits, draft_tokens and
+ * u_accept may be NULL: token 0 is then sampled from target row 0.
+ */
+int spec_verify(const void* target_logits, const void* draft_logits,
+                const int32_t* draft_tokens, const float* u_accept,
+                const float* u_resample, const float* temperature, int B, int gamma,
+                int V, int dtype, int32_t* out_tokens, int32_t* out_num_accepted,
+                void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                void* stream);
+
+/*
+ * spec_verify plus diagnostics (either may be NULL):
+ *   out_p [B][gamma][2] float: (P_t[i][x_i], P_d[i][x_i]) for every i < gamma
+ *   out_Z [B] float: the mass the final token was drawn from (sum of the
+ *         residual after a rejection, sum of P_t[gamma] for the bonus)
+ */
+int spec_verify_diag(const void* target_logits, const void* draft_logits,
+                     const int32_t* draft_tokens, const float* u_accept,
+                     const float* u_resample, const float* temperature, int B,
+                     int gamma, int V, int dtype, int32_t* out_tokens,
+                     int32_t* out_num_accepted, float* out_p, float* out_Z,
+                     void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                     void* stream);
+
+/*
+ * Greedy verification (temperature 0): a_i = argmax_v target_logits[b][i][v]
+ * over the stored values, lowest index on ties; k = first i < gamma with
+ * draft_tokens[b][i] != a_i, else gamma; out_tokens[b] = (a_0 .. a_k, -1 ...),
+ * out_num_accepted[b] = k.  This is the temperature -> 0 limit of the
+ * sampling rule (the pages give no greedy rule of their own).
+ */
+int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B,
+                       int gamma, int V, int dtype, int32_t* out_tokens,
+                       int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                       int32_t* dev_status, void* stream);
+
+/*
+ * Process-wide tuning overrides for benchmarking sweeps (0 = automatic):
+ * elements per phase-1 chunk (rounded up to a multiple of 64), resident CTAs
+ * per SM, and the phase-2 lag in requests.  Not thread-safe; set it before
+ * issuing calls.  Returns SV_OK.
+ */
+int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests);
+
+/* Human-readable name of a host return code. */
+const char* sv_error_string(int code);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int sv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -61,7 +61,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib = ctypes.CDLL(path)
         P = ctypes.c_void_p
         I = ctypes.c_int
-        lib.svo_verify.argtypes = [I, P, P, P, P, P, P, I, I, I, P, P, P, P, P, P,
+        lib.svo_verify.argtypes = [I, P, P, P, P, P, P, I, I, I, P, P, P, P, P, P, P,
                                    ctypes.c_double, I]
         lib.svo_verify.restype = I
         lib.svo_greedy.argtypes = [I, P, P, I, I, I, P, P, P, P, I]
@@ -82,7 +82,9 @@ def _threads(nthreads):
 def verify(Lt, Ld, x, u_acc, u_res, temp, dtype: int, near_eps: float = NEAR_EPS,
            nthreads: int | None = None, lib: ctypes.CDLL | None = None) -> dict:
     """Sampling-path oracle.  Arrays as in synth.Inputs (C-contiguous).
-    Returns tokens [B][gamma+1], n [B], pt/pd [B][gamma], Z [B], flags [B]."""
+    Returns tokens [B][gamma+1], n [B], pt/pd [B][gamma], Z [B], flags [B] and
+    dist [B][2] (distance of u_acc to the nearest decided ratio, and of
+    u_resample to the emitted token's nearer CDF edge)."""
     lib = lib or load()
     Lt = np.ascontiguousarray(Lt)
     B, R, V = Lt.shape
@@ -94,10 +96,12 @@ def verify(Lt, Ld, x, u_acc, u_res, temp, dtype: int, near_eps: float = NEAR_EPS
     temp = np.ascontiguousarray(temp, dtype=np.float32).reshape(B)
     out = dict(tokens=np.empty((B, R), np.int32), n=np.empty(B, np.int32),
                pt=np.empty((B, g), np.float64), pd=np.empty((B, g), np.float64),
-               Z=np.empty(B, np.float64), flags=np.zeros(B, np.int32))
+               Z=np.empty(B, np.float64), dist=np.empty((B, 2), np.float64),
+               flags=np.zeros(B, np.int32))
     rc = lib.svo_verify(int(dtype), _ptr(Lt), _ptr(Ld), _ptr(x), _ptr(u_acc), _ptr(u_res),
                         _ptr(temp), B, g, V, _ptr(out["tokens"]), _ptr(out["n"]),
-                        _ptr(out["pt"]), _ptr(out["pd"]), _ptr(out["Z"]), _ptr(out["flags"]),
+                        _ptr(out["pt"]), _ptr(out["pd"]), _ptr(out["Z"]), _ptr(out["dist"]),
+                        _ptr(out["flags"]),
                         float(near_eps), _threads(nthreads))
     if rc != 0:
         raise RuntimeError(f"svo_verify failed with {rc}")

@@ -114,7 +114,7 @@ static int softmax_row(const void* base, int dtype, size_t row_off, int V, doubl
  * smallest v whose index-order running sum exceeds tau = u * Z.  Sets *near
  * when the chosen token's CDF edges sit within near_eps of u. */
 static int inverse_cdf(const double* w, int V, double Z, double u, double near_eps,
-                       int* near) {
+                       int* near, double* dist) {
   double tau = u * Z;
   double C = 0.0;
   int chosen = -1;
@@ -141,7 +141,8 @@ static int inverse_cdf(const double* w, int V, double Z, double u, double near_e
     c_hi = C;
     *near = 1;
   }
-  if (fabs(c_lo / Z - u) < near_eps || fabs(c_hi / Z - u) < near_eps) *near = 1;
+  *dist = fmin(fabs(c_lo / Z - u), fabs(c_hi / Z - u));
+  if (*dist < near_eps) *near = 1;
   return chosen;
 }
 
@@ -152,7 +153,7 @@ typedef struct {
   const float *u_acc, *u_res, *temp;
   int B, gamma, V;
   int32_t *out_tokens, *out_n;
-  double *out_pt, *out_pd, *out_Z;
+  double *out_pt, *out_pd, *out_Z, *out_dist;
   int32_t* out_flags;
   double near_eps;
   int b0, b1;
@@ -166,6 +167,8 @@ static void verify_request(const verify_job* J, int b, double* Pt, double* Pd, d
   for (int i = 0; i < R; ++i) tok[i] = -1;
   J->out_n[b] = 0;
   if (J->out_Z) J->out_Z[b] = NAN;
+  double dist_acc = INFINITY, dist_smp = INFINITY;
+  if (J->out_dist) J->out_dist[(size_t)b * 2] = J->out_dist[(size_t)b * 2 + 1] = INFINITY;
   for (int i = 0; i < g; ++i) {
     if (J->out_pt) J->out_pt[(size_t)b * g + i] = NAN;
     if (J->out_pd) J->out_pd[(size_t)b * g + i] = NAN;
@@ -210,6 +213,7 @@ static void verify_request(const verify_job* J, int b, double* Pt, double* Pd, d
     double pd = Pd[(size_t)i * V + xi];
     double r = (pd > 0.0) ? fmin(1.0, pt / pd) : 1.0; /* reading R2 */
     double u = (double)J->u_acc[(size_t)b * g + i];
+    if (fabs(u - r) < dist_acc) dist_acc = fabs(u - r);
     if (fabs(u - r) < J->near_eps) flags |= SVO_NEAR_ACCEPT;
 #if SVO_MUTANT == 2
     int accept = (u < r); /* planted: strict test */
@@ -252,7 +256,7 @@ static void verify_request(const verify_job* J, int b, double* Pt, double* Pd, d
       Z = 0.0;
       for (int v = 0; v < V; ++v) { w[v] = pt[v]; Z += w[v]; }
     }
-    chosen = inverse_cdf(w, V, Z, u, J->near_eps, &near);
+    chosen = inverse_cdf(w, V, Z, u, J->near_eps, &near, &dist_smp);
   } else {
 #if SVO_MUTANT == 3
     J->out_n[b] = k; /* planted: no bonus token */
@@ -262,12 +266,16 @@ static void verify_request(const verify_job* J, int b, double* Pt, double* Pd, d
 #endif
     const double* pt = Pt + (size_t)g * V;
     for (int v = 0; v < V; ++v) { w[v] = pt[v]; Z += w[v]; }
-    chosen = inverse_cdf(w, V, Z, u, J->near_eps, &near);
+    chosen = inverse_cdf(w, V, Z, u, J->near_eps, &near, &dist_smp);
   }
   if (near) flags |= SVO_NEAR_SAMPLE;
   tok[k] = chosen;
   J->out_n[b] = k;
   if (J->out_Z) J->out_Z[b] = Z;
+  if (J->out_dist) {
+    J->out_dist[(size_t)b * 2] = dist_acc;
+    J->out_dist[(size_t)b * 2 + 1] = dist_smp;
+  }
   J->out_flags[b] = flags;
 }
 
@@ -293,12 +301,15 @@ static void* verify_worker(void* arg) {
  * u_acc [B][gamma], u_res [B][gamma+1], temp [B].  Outputs: out_tokens
  * [B][gamma+1] (-1 padded), out_n [B]; optional out_pt/out_pd [B][gamma]
  * (the softmax probabilities of x_i), out_Z [B] (residual or bonus mass);
- * out_flags [B] (SVO_* bits).  Returns 0, or -1 on a bad argument. */
+ * out_dist [B][2] optional: the smallest |u_acc - r_i| over the decided
+ * positions, and the distance of u_resample to the nearer CDF edge of the
+ * emitted token (INFINITY where there is none); out_flags [B] (SVO_* bits).
+ * Returns 0, or -1 on a bad argument. */
 int svo_verify(int dtype, const void* Lt, const void* Ld, const int32_t* x,
                const float* u_acc, const float* u_res, const float* temp, int B,
                int gamma, int V, int32_t* out_tokens, int32_t* out_n, double* out_pt,
-               double* out_pd, double* out_Z, int32_t* out_flags, double near_eps,
-               int nthreads) {
+               double* out_pd, double* out_Z, double* out_dist, int32_t* out_flags,
+               double near_eps, int nthreads) {
   if (B < 0 || gamma < 0 || V < 1 || (dtype != SVO_F32 && dtype != SVO_BF16)) return -1;
   if (B == 0) return 0;
   if (nthreads < 1) nthreads = 1;
@@ -311,7 +322,8 @@ int svo_verify(int dtype, const void* Lt, const void* Ld, const int32_t* x,
     J->u_acc = u_acc; J->u_res = u_res; J->temp = temp;
     J->B = B; J->gamma = gamma; J->V = V;
     J->out_tokens = out_tokens; J->out_n = out_n;
-    J->out_pt = out_pt; J->out_pd = out_pd; J->out_Z = out_Z; J->out_flags = out_flags;
+    J->out_pt = out_pt; J->out_pd = out_pd; J->out_Z = out_Z; J->out_dist = out_dist;
+    J->out_flags = out_flags;
     J->near_eps = near_eps;
     J->b0 = (int)((long long)B * t / nthreads);
     J->b1 = (int)((long long)B * (t + 1) / nthreads);

@@ -1,0 +1,160 @@
+"""Thin Python binding of libspecverify.so (argument marshalling only).
+
+The functions carry the C ABI's names (include/specverify.h) and take torch
+tensors for the device buffers; every step of the verification runs in the
+library's CUDA kernels.  There is no CPU fallback: if the library is missing,
+loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build_lib import LIB_PATH
+
+SV_F32, SV_BF16 = 0, 1
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_DTYPE, SV_ERR_CUDA, SV_ERR_WORKSPACE = range(5)
+SV_ST_NONFINITE, SV_ST_BAD_TOKEN, SV_ST_BAD_TEMP = 0x1, 0x2, 0x4
+SV_ST_TIMEOUT, SV_ST_WORKSPACE, SV_ST_DEGENERATE = 0x8, 0x10, 0x20
+SV_MAX_GAMMA = 32
+
+EXPORTED = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_diag",
+            "spec_verify_greedy", "sv_set_tuning", "sv_error_string", "sv_version")
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    pass
+
+
+def lib() -> ctypes.CDLL:
+    """Load libspecverify.so (built by __graft_entry__.build()); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise SpecVerifyError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.sv_workspace_bytes.argtypes = [I, I, I]
+        L.sv_workspace_bytes.restype = Z
+        L.sv_workspace_init.argtypes = [P, Z, P]
+        L.spec_verify.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, P, Z, P, P]
+        L.spec_verify_diag.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, Z, P, P]
+        L.spec_verify_greedy.argtypes = [P, P, I, I, I, I, P, P, P, Z, P, P]
+        L.sv_set_tuning.argtypes = [I, I, I]
+        L.sv_error_string.argtypes = [I]
+        L.sv_error_string.restype = ctypes.c_char_p
+        for name in ("sv_workspace_init", "spec_verify", "spec_verify_diag",
+                     "spec_verify_greedy", "sv_set_tuning", "sv_version"):
+            getattr(L, name).restype = I
+        _lib = L
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != SV_OK:
+        raise SpecVerifyError(lib().sv_error_string(rc).decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SV_F32
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    raise SpecVerifyError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _dev(t: torch.Tensor | None, dtype: torch.dtype | None = None, name: str = "") -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise SpecVerifyError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise SpecVerifyError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise SpecVerifyError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def sv_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    return int(lib().sv_workspace_bytes(B, gamma, V))
+
+
+def sv_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    _check(lib().sv_workspace_init(_dev(workspace, None, "workspace"), workspace.numel() *
+                                   workspace.element_size(), _stream(stream, workspace.device)))
+
+
+def make_workspace(B: int, gamma: int, V: int, device) -> torch.Tensor:
+    """Allocate (torch caching allocator, 256-byte aligned) and zero a workspace."""
+    ws = torch.empty(max(256, sv_workspace_bytes(B, gamma, V)), dtype=torch.uint8, device=device)
+    sv_workspace_init(ws)
+    return ws
+
+
+def sv_set_tuning(chunk_elems: int = 0, ctas_per_sm: int = 0, lag_requests: int = 0) -> None:
+    _check(lib().sv_set_tuning(chunk_elems, ctas_per_sm, lag_requests))
+
+
+def _shapes(target_logits: torch.Tensor):
+    if target_logits.dim() != 3:
+        raise SpecVerifyError("target_logits must be [B][gamma+1][V]")
+    B, R, V = target_logits.shape
+    return B, R - 1, V
+
+
+def spec_verify_diag(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                     temperature, out_tokens, out_num_accepted, out_p, out_Z, workspace,
+                     dev_status=None, stream=None) -> None:
+    B, g, V = _shapes(target_logits)
+    dt = _dtype_code(target_logits)
+    if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
+        raise SpecVerifyError("draft_logits must have the dtype of target_logits")
+    _check(lib().spec_verify_diag(
+        _dev(target_logits, None, "target_logits"), _dev(draft_logits, None, "draft_logits"),
+        _dev(draft_tokens, torch.int32, "draft_tokens"), _dev(u_accept, torch.float32, "u_accept"),
+        _dev(u_resample, torch.float32, "u_resample"),
+        _dev(temperature, torch.float32, "temperature"), B, g, V, dt,
+        _dev(out_tokens, torch.int32, "out_tokens"),
+        _dev(out_num_accepted, torch.int32, "out_num_accepted"),
+        _dev(out_p, torch.float32, "out_p"), _dev(out_Z, torch.float32, "out_Z"),
+        _dev(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(dev_status, torch.int32, "dev_status"), _stream(stream, target_logits.device)))
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_resample, temperature,
+                out_tokens, out_num_accepted, workspace, dev_status=None, stream=None) -> None:
+    B, g, V = _shapes(target_logits)
+    dt = _dtype_code(target_logits)
+    if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
+        raise SpecVerifyError("draft_logits must have the dtype of target_logits")
+    _check(lib().spec_verify(
+        _dev(target_logits, None, "target_logits"), _dev(draft_logits, None, "draft_logits"),
+        _dev(draft_tokens, torch.int32, "draft_tokens"), _dev(u_accept, torch.float32, "u_accept"),
+        _dev(u_resample, torch.float32, "u_resample"),
+        _dev(temperature, torch.float32, "temperature"), B, g, V, dt,
+        _dev(out_tokens, torch.int32, "out_tokens"),
+        _dev(out_num_accepted, torch.int32, "out_num_accepted"),
+        _dev(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(dev_status, torch.int32, "dev_status"), _stream(stream, target_logits.device)))
+
+
+def spec_verify_greedy(target_logits, draft_tokens, out_tokens, out_num_accepted, workspace,
+                       dev_status=None, stream=None) -> None:
+    B, g, V = _shapes(target_logits)
+    dt = _dtype_code(target_logits)
+    _check(lib().spec_verify_greedy(
+        _dev(target_logits, None, "target_logits"), _dev(draft_tokens, torch.int32, "draft_tokens"),
+        B, g, V, dt, _dev(out_tokens, torch.int32, "out_tokens"),
+        _dev(out_num_accepted, torch.int32, "out_num_accepted"),
+        _dev(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(dev_status, torch.int32, "dev_status"), _stream(stream, target_logits.device)))

@@ -1,0 +1,123 @@
+"""Helpers shared by the GPU parity tests: move synthetic inputs to the
+device, call the library through its C ABI (binding), and compare with the
+oracle under the parity rules:
+
+  * tokens and accepted counts bit-exact, except at requests the oracle flags
+    as near-ties (|u_acc - r| < 1e-6 at a decided position, the u_resample
+    CDF boundary within 1e-6, or a vanished residual);
+  * P_t(x_i), P_d(x_i) within relative 1e-5;
+  * the final draw's mass Z within relative 1e-5 plus absolute 1e-6 (the
+    residual max(0, P_t - P_d) loses relative precision by cancellation where
+    the two rows agree; each fp32 term carries ~1e-7 relative error);
+  * invalid requests: accepted count 0, tokens all -1, matching status bits;
+  * greedy: bit-exact everywhere.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from speculative_decoding_verification_09_gb300 import binding, synth
+
+DEV = torch.device("cuda:0")
+P_RTOL = 1e-5
+Z_RTOL, Z_ATOL = 1e-5, 1e-6
+
+
+def to_dev(inp: synth.Inputs, device=DEV) -> dict:
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    Lt, Ld = t(inp.Lt), t(inp.Ld)
+    if inp.dtype == synth.BF16:
+        Lt, Ld = Lt.view(torch.bfloat16), Ld.view(torch.bfloat16)
+    return dict(Lt=Lt, Ld=Ld, x=t(inp.x), u_acc=t(inp.u_acc), u_res=t(inp.u_res), temp=t(inp.temp))
+
+
+def run_sampling(inp: synth.Inputs, d: dict | None = None, ws=None, stream=None) -> dict:
+    d = d or to_dev(inp)
+    B, g = inp.B, inp.gamma
+    tok = torch.full((B, g + 1), -7, dtype=torch.int32, device=DEV)
+    n = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+    p = torch.full((B, g, 2), -7.0, dtype=torch.float32, device=DEV)
+    Z = torch.full((B,), -7.0, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    if ws is None:
+        ws = binding.make_workspace(B, g, inp.V, DEV)
+    binding.spec_verify_diag(d["Lt"], d["Ld"] if g > 0 else None, d["x"] if g > 0 else None,
+                             d["u_acc"] if g > 0 else None, d["u_res"], d["temp"], tok, n, p, Z,
+                             ws, st, stream)
+    torch.cuda.synchronize()
+    return dict(tokens=tok.cpu().numpy(), n=n.cpu().numpy(), p=p.cpu().numpy(),
+                Z=Z.cpu().numpy(), status=int(st.item()))
+
+
+def run_greedy(inp: synth.Inputs, x=None, d: dict | None = None, ws=None) -> dict:
+    d = d or to_dev(inp)
+    B, g = inp.B, inp.gamma
+    xd = d["x"] if x is None else torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+    tok = torch.full((B, g + 1), -7, dtype=torch.int32, device=DEV)
+    n = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    if ws is None:
+        ws = binding.make_workspace(B, g, inp.V, DEV)
+    binding.spec_verify_greedy(d["Lt"], xd if g > 0 else None, tok, n, ws, st)
+    torch.cuda.synchronize()
+    return dict(tokens=tok.cpu().numpy(), n=n.cpu().numpy(), status=int(st.item()))
+
+
+def oracle_sampling(inp: synth.Inputs) -> dict:
+    return oracle.verify(inp.Lt, inp.Ld, inp.x, inp.u_acc, inp.u_res, inp.temp, inp.dtype)
+
+
+def expected_status(flags: np.ndarray) -> int:
+    s = 0
+    if np.any(flags & oracle.INVALID_NONFINITE):
+        s |= binding.SV_ST_NONFINITE
+    if np.any(flags & oracle.INVALID_TOKEN):
+        s |= binding.SV_ST_BAD_TOKEN
+    if np.any(flags & oracle.INVALID_TEMP):
+        s |= binding.SV_ST_BAD_TEMP
+    return s
+
+
+def compare_sampling(inp: synth.Inputs, got: dict, ref: dict) -> dict:
+    flags = ref["flags"]
+    inv = (flags & oracle.INVALID_ANY) != 0
+    near = (flags & oracle.NEAR_ANY) != 0
+    assert np.all(got["n"][inv] == 0) and np.all(got["tokens"][inv] == -1)
+    same = np.all(got["tokens"] == ref["tokens"], axis=1) & (got["n"] == ref["n"])
+    bad = ~inv & ~near & ~same
+    assert not bad.any(), (f"{int(bad.sum())} mismatching requests, e.g. b={int(np.argmax(bad))}: "
+                           f"gpu {got['tokens'][bad][0]} n={got['n'][bad][0]} vs oracle "
+                           f"{ref['tokens'][bad][0]} n={ref['n'][bad][0]}")
+    ok = ~inv
+    if inp.gamma > 0 and ok.any():
+        for j, key in ((0, "pt"), (1, "pd")):
+            g_, r_ = got["p"][ok, :, j].astype(np.float64), ref[key][ok]
+            err = np.abs(g_ - r_) - P_RTOL * np.abs(r_) - 1e-30
+            assert np.all(err <= 0), f"{key}: max rel err {np.max(np.abs(g_ - r_) / np.abs(r_))}"
+    samek = ok & (got["n"] == ref["n"])
+    if samek.any():
+        gz, rz = got["Z"][samek].astype(np.float64), ref["Z"][samek]
+        assert np.all(np.abs(gz - rz) <= Z_RTOL * np.abs(rz) + Z_ATOL), \
+            f"Z: max abs err {np.max(np.abs(gz - rz))}"
+    want = expected_status(flags)
+    st = got["status"] & ~binding.SV_ST_DEGENERATE
+    assert st == want, f"status {st:#x} != expected {want:#x}"
+    near_bits = (((flags & oracle.NEAR_ACCEPT) != 0).astype(int)
+                 + ((flags & oracle.NEAR_SAMPLE) != 0).astype(int)
+                 + ((flags & oracle.DEGENERATE) != 0).astype(int))
+    mism = ~inv & ~same
+    dist = np.min(ref["dist"], axis=1)
+    return dict(requests=inp.B, positions=inp.B * inp.gamma, near=int(near_bits.sum()),
+                near_requests=int(near.sum()), mismatches=int(mism.sum()),
+                max_mismatch_dist=float(dist[mism].max()) if mism.any() else 0.0,
+                accepted=int(ref["n"][~inv].sum()))
+
+
+def compare_greedy(got: dict, ref: dict) -> None:
+    assert np.array_equal(got["tokens"], ref["tokens"]), "greedy tokens differ"
+    assert np.array_equal(got["n"], ref["n"]), "greedy counts differ"
+    want = expected_status(ref["flags"])
+    assert got["status"] == want, f"status {got['status']:#x} != {want:#x}"

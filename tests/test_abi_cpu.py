@@ -1,0 +1,92 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports every
+function include/specverify.h declares, sizes workspaces, and rejects bad
+arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from speculative_decoding_verification_09_gb300 import binding
+from speculative_decoding_verification_09_gb300._build_lib import LIB_PATH, ROOT
+
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(LIB_PATH):
+        __graft_entry__.build()
+    return binding.lib()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|void)\s*\**\s*"
+                                 r"([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)))
+
+
+def test_header_symbols_exported(L):
+    names = header_functions()
+    assert set(names) == set(binding.EXPORTED), names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_workspace_bytes(L):
+    a = binding.sv_workspace_bytes(1, 4, 32000)
+    b = binding.sv_workspace_bytes(256, 4, 151936)
+    assert 0 < a < b and b % 256 == 0
+    assert binding.sv_workspace_bytes(-1, 4, 10) == 0
+    assert binding.sv_workspace_bytes(1, 33, 10) == 0
+    assert binding.sv_workspace_bytes(1, 4, 0) == 0
+    assert L.sv_version() >= 100
+    assert L.sv_error_string(binding.SV_ERR_WORKSPACE) == b"SV_ERR_WORKSPACE"
+
+
+FAKE = 0x10000000  # never dereferenced: every call below fails validation first
+
+
+def _call(L, **kw):
+    a = dict(Lt=FAKE, Ld=FAKE, x=FAKE, ua=FAKE, ur=FAKE, T=FAKE, B=2, g=3, V=100, dt=0,
+             tok=FAKE, n=FAKE, p=None, Z=None, ws=FAKE, wsb=1 << 30, st=None, s=None)
+    a.update(kw)
+    return L.spec_verify_diag(a["Lt"], a["Ld"], a["x"], a["ua"], a["ur"], a["T"], a["B"], a["g"],
+                              a["V"], a["dt"], a["tok"], a["n"], a["p"], a["Z"], a["ws"],
+                              a["wsb"], a["st"], a["s"])
+
+
+def test_argument_validation(L):
+    assert _call(L, dt=7) == binding.SV_ERR_DTYPE
+    assert _call(L, g=33) == binding.SV_ERR_INVALID_ARG
+    assert _call(L, g=-1) == binding.SV_ERR_INVALID_ARG
+    assert _call(L, B=-1) == binding.SV_ERR_INVALID_ARG
+    assert _call(L, V=0) == binding.SV_ERR_INVALID_ARG
+    assert _call(L, Lt=None) == binding.SV_ERR_INVALID_ARG
+    assert _call(L, Ld=None) == binding.SV_ERR_INVALID_ARG
+    assert _call(L, ur=None) == binding.SV_ERR_INVALID_ARG
+    assert _call(L, tok=None) == binding.SV_ERR_INVALID_ARG
+    assert _call(L, Lt=FAKE + 2) == binding.SV_ERR_INVALID_ARG   # fp32 logits need 4-byte alignment
+    assert _call(L, x=FAKE + 1) == binding.SV_ERR_INVALID_ARG
+    assert _call(L, ws=FAKE + 16) == binding.SV_ERR_WORKSPACE    # workspace needs 256-byte alignment
+    assert _call(L, ws=None) == binding.SV_ERR_WORKSPACE
+    assert _call(L, wsb=64) == binding.SV_ERR_WORKSPACE
+    assert _call(L, B=0) == binding.SV_OK                        # empty batch: nothing launched
+    # gamma = 0 needs no draft pointers; it still validates the rest
+    assert _call(L, g=0, Ld=None, x=None, ua=None, wsb=64) == binding.SV_ERR_WORKSPACE
+    assert L.spec_verify_greedy(FAKE, FAKE, 2, 3, 100, 5, FAKE, FAKE, FAKE, 1 << 30, None,
+                                None) == binding.SV_ERR_DTYPE
+    assert L.spec_verify_greedy(FAKE, None, 2, 3, 100, 1, FAKE, FAKE, FAKE, 1 << 30, None,
+                                None) == binding.SV_ERR_INVALID_ARG
+    assert L.spec_verify_greedy(FAKE + 1, FAKE, 2, 3, 100, 1, FAKE, FAKE, FAKE, 1 << 30, None,
+                                None) == binding.SV_ERR_INVALID_ARG
+
+
+def test_no_gpu_fails_loudly(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid-looking arguments reach the device query, which must fail, not fall back
+    assert _call(L) == binding.SV_ERR_CUDA
