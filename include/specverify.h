@@ -125,6 +125,39 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
                        int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
                        int32_t* dev_status, void* stream);
 
+/* Size of the built-in scratch of spec_verify_noalloc: 16 MiB.  Every GPU that
+ * loads this library holds this much device memory until the process exits. */
+#define SV_NOALLOC_MAX_WORKSPACE (16u << 20)
+
+/*
+ * spec_verify for callers that cannot allocate device memory.  (The pages
+ * have no counterpart: this is a service of the library, not part of the
+ * method.)  Some callers run where allocating is not allowed or not
+ * possible: a plugin inside a host framework that owns all device memory
+ * and hands out no allocator, or a latency-critical loop that must not pay
+ * for cudaMalloc's implicit device synchronisation.  This entry point takes
+ * the same inputs and outputs as spec_verify but no workspace: it uses a
+ * scratch array built into the library (SV_NOALLOC_MAX_WORKSPACE bytes per
+ * device) and calls no allocating routine.
+ *   - Sizes whose sv_workspace_bytes(B, gamma, V) exceeds
+ *     SV_NOALLOC_MAX_WORKSPACE return SV_ERR_WORKSPACE; nothing is launched.
+ *   - The first call on a device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that
+ *     first call before any stream capture.
+ *   - Each call clears the scratch's task and exit counters on `stream`
+ *     before its launch; the rest of the scratch keeps the previous call's
+ *     contents, which is safe because every record in it is tagged with the
+ *     launch that wrote it.
+ *   - All calls on a device share the one array: calls that may overlap on
+ *     the GPU (different streams, or different host threads) race and must
+ *     be serialised by the caller.
+ */
+int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
+                        const int32_t* draft_tokens, const float* u_accept,
+                        const float* u_resample, const float* temperature, int B,
+                        int gamma, int V, int dtype, int32_t* out_tokens,
+                        int32_t* out_num_accepted, int32_t* dev_status, void* stream);
+
 /*
  * Process-wide tuning overrides for benchmarking sweeps (0 = automatic):
  * elements per phase-1 chunk (rounded up to a multiple of 64), resident CTAs

@@ -21,7 +21,9 @@ SV_ST_TIMEOUT, SV_ST_WORKSPACE, SV_ST_DEGENERATE = 0x8, 0x10, 0x20
 SV_MAX_GAMMA = 32
 
 EXPORTED = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_diag",
-            "spec_verify_greedy", "sv_set_tuning", "sv_error_string", "sv_version")
+            "spec_verify_greedy", "spec_verify_noalloc", "sv_set_tuning", "sv_error_string",
+            "sv_version")
+SV_NOALLOC_MAX_WORKSPACE = 16 << 20
 
 _lib = None
 
@@ -44,11 +46,12 @@ def lib() -> ctypes.CDLL:
         L.spec_verify.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, P, Z, P, P]
         L.spec_verify_diag.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, Z, P, P]
         L.spec_verify_greedy.argtypes = [P, P, I, I, I, I, P, P, P, Z, P, P]
+        L.spec_verify_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, P, P]
         L.sv_set_tuning.argtypes = [I, I, I]
         L.sv_error_string.argtypes = [I]
         L.sv_error_string.restype = ctypes.c_char_p
         for name in ("sv_workspace_init", "spec_verify", "spec_verify_diag",
-                     "spec_verify_greedy", "sv_set_tuning", "sv_version"):
+                     "spec_verify_greedy", "spec_verify_noalloc", "sv_set_tuning", "sv_version"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -157,4 +160,25 @@ def spec_verify_greedy(target_logits, draft_tokens, out_tokens, out_num_accepted
         B, g, V, dt, _dev(out_tokens, torch.int32, "out_tokens"),
         _dev(out_num_accepted, torch.int32, "out_num_accepted"),
         _dev(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(dev_status, torch.int32, "dev_status"), _stream(stream, target_logits.device)))
+
+
+def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                        temperature, out_tokens, out_num_accepted, dev_status=None,
+                        stream=None) -> None:
+    """spec_verify without a workspace, for callers that may not allocate
+    device memory: the library's built-in scratch (SV_NOALLOC_MAX_WORKSPACE
+    bytes per device) is used instead.  Calls that may overlap on the GPU
+    share that scratch and race; serialise them."""
+    B, g, V = _shapes(target_logits)
+    dt = _dtype_code(target_logits)
+    if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
+        raise SpecVerifyError("draft_logits must have the dtype of target_logits")
+    _check(lib().spec_verify_noalloc(
+        _dev(target_logits, None, "target_logits"), _dev(draft_logits, None, "draft_logits"),
+        _dev(draft_tokens, torch.int32, "draft_tokens"), _dev(u_accept, torch.float32, "u_accept"),
+        _dev(u_resample, torch.float32, "u_resample"),
+        _dev(temperature, torch.float32, "temperature"), B, g, V, dt,
+        _dev(out_tokens, torch.int32, "out_tokens"),
+        _dev(out_num_accepted, torch.int32, "out_num_accepted"),
         _dev(dev_status, torch.int32, "dev_status"), _stream(stream, target_logits.device)))

@@ -32,6 +32,7 @@
 // The greedy kernel runs P1 tasks (chunk argmax) and a decider only.
 #include <cuda_runtime.h>
 #include <limits.h>
+#include <stddef.h>
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -1194,6 +1195,64 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
   return launch(true, target_logits, nullptr, draft_tokens, nullptr, nullptr, nullptr, B, gamma,
                 V, dtype, out_tokens, out_num_accepted, nullptr, nullptr, workspace,
                 workspace_bytes, dev_status, stream);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------- no-allocation entry point
+// Scratch for spec_verify_noalloc, in the library's own device memory.  Host
+// code may not use this name as a device address (on the host it names a
+// stand-in object): the address is looked up per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_MAX_WORKSPACE];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};  // device address of g_noalloc_scratch, per device
+
+// Device address of the scratch on the current device; the lookup runs once
+// per device, with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SV_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SV_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SV_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
+                        const int32_t* draft_tokens, const float* u_accept,
+                        const float* u_resample, const float* temperature, int B, int gamma,
+                        int V, int dtype, int32_t* out_tokens, int32_t* out_num_accepted,
+                        int32_t* dev_status, void* stream) {
+  if (B > 0 && gamma >= 0 && gamma <= SV_MAX_GAMMA && V >= 1 &&
+      sv_workspace_bytes(B, gamma, V) > size_t(SV_NOALLOC_MAX_WORKSPACE))
+    return SV_ERR_WORKSPACE;  // too large for the built-in scratch
+  if (B <= 0 || (dtype != SV_F32 && dtype != SV_BF16) || gamma < 0 || gamma > SV_MAX_GAMMA ||
+      V < 1)  // argument errors and the empty batch: no scratch needed
+    return launch(false, target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                  temperature, B, gamma, V, dtype, out_tokens, out_num_accepted, nullptr,
+                  nullptr, nullptr, 0, dev_status, stream);
+  void* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc != SV_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the task counter and the exit counter must start at zero; the launch
+  // epoch after them must survive from call to call
+  if (cudaMemsetAsync(scratch, 0, offsetof(Ctrl, epoch_counter), st) != cudaSuccess ||
+      cudaMemsetAsync(static_cast<unsigned char*>(scratch) + offsetof(Ctrl, abort), 0,
+                      sizeof(int), st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return launch(false, target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                temperature, B, gamma, V, dtype, out_tokens, out_num_accepted, nullptr, nullptr,
+                scratch, SV_NOALLOC_MAX_WORKSPACE, dev_status, stream);
 }
 
 int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests) {
