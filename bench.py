@@ -210,6 +210,8 @@ def run_ours(args) -> None:
     out_n = torch.empty(B, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = binding.make_workspace(B, g, V, dev)
+    if args.chunk or args.lag:
+        binding.sv_set_tuning(args.chunk, 0, args.lag)
 
     def step(t):
         if greedy:
@@ -319,6 +321,7 @@ def run_ours(args) -> None:
                      "kernel_ms": launch_ms},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
         "status": st, "wall_s_timed": t_wall,
+        "tuning": {"chunk": args.chunk, "lag": args.lag},
     }
     print(json.dumps(line))
     if pg:
@@ -338,6 +341,8 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-requests", type=int, default=256)
     ap.add_argument("--ref-requests", type=int, default=32)
+    ap.add_argument("--chunk", type=int, default=0, help="phase-1 chunk elements (0 = auto)")
+    ap.add_argument("--lag", type=int, default=0, help="task-order lag in requests (0 = auto)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

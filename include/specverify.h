@@ -160,9 +160,10 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
 
 /*
  * Process-wide tuning overrides for benchmarking sweeps (0 = automatic):
- * elements per phase-1 chunk (rounded up to a multiple of 64), resident CTAs
- * per SM, and the phase-2 lag in requests.  Not thread-safe; set it before
- * issuing calls.  Returns SV_OK.
+ * elements per phase-1 chunk (rounded up to a multiple of 64, capped at 16 KB
+ * of logits), and the phase-2 lag in requests; ctas_per_sm is accepted for
+ * compatibility and ignored (the kernel runs one CTA per SM).  Not
+ * thread-safe; set it before issuing calls.  Returns SV_OK.
  */
 int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests);
 

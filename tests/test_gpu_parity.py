@@ -201,12 +201,12 @@ def test_repeated_calls_reuse_workspace_and_streams():
 
 
 # Workspace layout facts used to poison it: the control block starts at byte 0
-# (task counter, u64); per-request words start at byte 256, 32 bytes each
-# (u64 phase-1 counter, u64 phase-2 counter, u32 decision flag, padding).
+# (task counter, u64); per-request words start at byte 256, 16 bytes each
+# (u32 decision flag, padding), followed by records and epoch-tagged partials.
 def test_garbage_request_words_are_harmless():
-    """Arrival counters and flags are tagged with the launch epoch, so leftover
-    or garbage per-request words (another shape's records, a poisoned counter)
-    cannot change the result."""
+    """Decision flags and published values are tagged with the launch epoch, so
+    leftover or garbage per-request words (another shape's records, a stale
+    flag) cannot change the result."""
     cfg = synth.custom_config(8, 3, 6000, "bf16", "normal")
     inp = synth.make_inputs(cfg, seed=12)
     d = to_dev(inp)
@@ -215,7 +215,7 @@ def test_garbage_request_words_are_harmless():
     ws[256:256 + 8 * 32].view(torch.int32).copy_(
         torch.randint(-2**31, 2**31 - 1, (8 * 8,), dtype=torch.int32, device=DEV))
     compare_sampling(inp, run_sampling(inp, d, ws), ref)
-    ws[256:264].view(torch.int64).fill_(3)  # request 0: three phantom arrivals, epoch 0
+    ws[256:264].view(torch.int64).fill_(3)  # request 0: a stale decision flag
     compare_sampling(inp, run_sampling(inp, d, ws), ref)
 
 
