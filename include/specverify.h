@@ -73,8 +73,9 @@ enum {
 #define SV_ST_BAD_TOKEN 0x2   /* a draft token outside [0, V) */
 #define SV_ST_BAD_TEMP 0x4    /* temperature not finite or below 2^-126 */
 #define SV_ST_TIMEOUT 0x8     /* an internal wait gave up (results of the call are void) */
-#define SV_ST_WORKSPACE 0x10  /* workspace was not in its ready state (results void; it is
-                                 repaired by the call that reports this) */
+#define SV_ST_WORKSPACE 0x10  /* the workspace's control block was not in its ready state
+                                 (another call's work overlapped, or it was overwritten);
+                                 the call that reports this leaves it ready again */
 #define SV_ST_DEGENERATE 0x20 /* informational: a residual summed to 0 and the target row
                                  was sampled instead */
 
@@ -84,7 +85,7 @@ enum {
 size_t sv_workspace_bytes(int B, int gamma, int V);
 
 /* Zero a workspace on `stream` (a cudaMemsetAsync).  Call once after
- * allocating it, or after a call reported SV_ST_TIMEOUT. */
+ * allocating it. */
 int sv_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /*
@@ -144,10 +145,9 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
  *   - The first call on a device looks up the scratch array's device
  *     address (cudaGetSymbolAddress) with that device current; make that
  *     first call before any stream capture.
- *   - Each call clears the scratch's task and exit counters on `stream`
- *     before its launch; the rest of the scratch keeps the previous call's
- *     contents, which is safe because every record in it is tagged with the
- *     launch that wrote it.
+ *   - Each call resets the scratch's 64-byte control block on `stream`
+ *     before its launches; every other byte of the scratch that a call reads
+ *     is written earlier in the same call.
  *   - All calls on a device share the one array: calls that may overlap on
  *     the GPU (different streams, or different host threads) race and must
  *     be serialised by the caller.
@@ -159,11 +159,12 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
                         int32_t* out_num_accepted, int32_t* dev_status, void* stream);
 
 /*
- * Process-wide tuning overrides for benchmarking sweeps (0 = automatic):
- * elements per phase-1 chunk (rounded up to a multiple of 64, capped at 16 KB
- * of logits), and the phase-2 lag in requests; ctas_per_sm is accepted for
- * compatibility and ignored (the kernel runs one CTA per SM).  Not
- * thread-safe; set it before issuing calls.  Returns SV_OK.
+ * Process-wide tuning override for benchmarking sweeps (0 = automatic):
+ * elements per phase-1 chunk (rounded up to a multiple of 64, capped at 32 KB
+ * of logits).  ctas_per_sm and lag_requests are accepted for compatibility
+ * and ignored (the streaming kernel runs one CTA per SM; the stages are
+ * separate kernels, so there is no lag).  Not thread-safe; set it before
+ * issuing calls.  Returns SV_OK.
  */
 int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests);
 

@@ -8,39 +8,26 @@
 // scheduler section "动态推迟投机验证调度器设计": tempered softmax, accept in
 // draft order, stop at the first rejection, index-order inverse CDF).
 //
-// GPU structure: ONE persistent launch per call, one CTA per SM, warp
-// specialised:
-//   producer  (warp 0, one lane) claims task ids from an atomic counter (two
-//             claims in flight) in a fixed global order and streams each
-//             task's row chunks from HBM into a ring of shared-memory slots
-//             with TMA bulk copies (cp.async.bulk, completion counted on an
-//             mbarrier);
-//   consumers (NCW warps) reduce each slot from shared memory and stage one
-//             partial per warp; the warp of index (slot sequence mod NCW)
-//             books the slot: it combines the staged partials, frees the
-//             slot and publishes the result.
-// Published values are 64-bit words whose high half is the launch epoch, so
-// a reader knows a value is this launch's without any fence or counter; the
-// per-task path has no atomics besides the task claim.
-// Tasks, in a global order where every request's tasks follow each other at
-// a distance of `lag` requests:
-//   P1(b, i, c)  chunk c of target row i and draft row i of request b:
-//                per-warp max (packed bf16 max) then sum 2^((l-max)*log2e/T);
-//                the row chunk's (max, sum) pair is published.
-//   D(b)         the decision: every consumer warp combines rows of b in fp64
-//                (P_t(x_i), P_d(x_i), accept bit); the booking warp takes the
-//                first rejection k, writes all outputs but token k and
-//                publishes a decision record (release of the launch epoch).
-//   P2(b, c)     chunk c of the row the last token is drawn from (residual of
-//                row k, or target row gamma for the bonus), re-read from L2:
-//                the mass of each warp's contiguous sub-range.
-//   T3(b)        finds the sub-range where the running mass crosses u * Z and
-//                scans it in index order with warp prefix sums: token k.
-// A task only ever waits for tasks claimed before it (D for b's P1 chunks, P2
-// for D's record, T3 for P2's masses), and nothing waits for a later task,
-// so every wait ends; each wait still gives up after one second
-// (SV_ST_TIMEOUT) instead of hanging.
-// Greedy verification runs P1 (chunk argmax) and D only.
+// GPU structure: four kernels in stream order per call (the stream order is
+// the only synchronisation between them):
+//   reduce   one CTA per SM, each streaming a contiguous range of row chunks
+//            (chunk c of target row i and draft row i of request b) from HBM
+//            into a ring of shared-memory slots with TMA bulk copies
+//            (cp.async.bulk, completion counted on an mbarrier) issued by one
+//            producer lane; NCW consumer warps reduce each slot from
+//            registers and publish one partial per warp: (max, sum of
+//            2^((l - max) * log2e / T)) of the target and draft shares, or
+//            (max, lowest index, NaN seen) for greedy verification.
+//   decide   one CTA per request: every row's partials combined (maxima, sums
+//            as float pairs), then per position the acceptance test in fp64,
+//            the first rejection k, all outputs but token k, and a decision
+//            record (row k's normalisers) for the draw.
+//   residual one CTA per (request, phase-2 chunk) of the row token k is drawn
+//            from (residual of row k, or target row gamma for the bonus): the
+//            mass of each warp's contiguous sub-range.
+//   draw     one warp per request: the sub-range where the running mass
+//            crosses u * Z, scanned in index order: token k.
+// Greedy verification runs reduce (chunk argmax) and decide only.
 #include <cuda_runtime.h>
 #include <limits.h>
 #include <math.h>
@@ -55,9 +42,13 @@
 
 namespace {
 
-constexpr int NCW = 14;                // consumer warps (16 warps in all: 4 per SM sub-partition)
-constexpr int NTHR = 32 * (NCW + 2);   // plus the producer warp and the booking warp
-constexpr int NSTAGE = 8;              // staging ring depth (how far booking may lag)
+// ------------------------------------------------------------ constants
+
+// reduce: 15 warps, the producer (warp 0) and NCW consumer warps.  Warp w runs
+// on SM sub-partition w % 4, so sub-partitions 1..3 hold four consumer warps
+// and sub-partition 0 three besides the producer.
+constexpr int NCW = 14;
+constexpr int NTHR = 32 * (NCW + 1);
 constexpr int NSLOT = 3;               // shared-memory ring depth
 constexpr int HALF = 32768;            // bytes of one row chunk in a slot
 constexpr int SLOT = 2 * HALF;         // target chunk + draft chunk
@@ -65,59 +56,47 @@ constexpr int CH1_MIN = 1024;          // smallest phase-1 chunk (elements)
 constexpr int CH2_F32 = HALF / 4;      // phase-2 chunk for fp32 (the workspace bound)
 constexpr unsigned SUSPEND_HINT_NS = 1000000u;  // a waiting warp sleeps until the phase completes
 constexpr int SMS_CAP = 256;           // the chunk heuristic assumes at most this many SMs
-constexpr int KF_CAP = 2048;           // requests whose log2(e)/T is kept in shared memory
 constexpr int MAXR = SV_MAX_GAMMA + 1;
+constexpr int DECIDE_WARPS = 8;        // decide: warps per request
+constexpr int DRAW_WARPS = 4;          // draw: requests per CTA
 constexpr float LOG2E_F = 1.4426950408889634f;
 constexpr double LOG2E_D = 1.4426950408889634;
 constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;  // one second
 
-enum : int { MODE_INVALID = 0, MODE_REJECT = 1, MODE_BONUS = 2, MODE_TARGET = 3 };
-enum : int { K_END = 0, K_P1 = 1, K_D = 2, K_P2 = 3, K_T3 = 4, K_SKIP = 5 };
-
 // ------------------------------------------------------------ workspace
 
 struct Ctrl {                 // 64 bytes at the start of the workspace
-  unsigned long long task;    // next task id
-  unsigned exit_count;        // CTAs that finished
-  unsigned epoch_counter;     // launch epoch = epoch_counter + 1
-  int abort;                  // set when a wait gave up
-  int pad[11];
+  // both 0 between calls (the ready state); state is 1 while a call runs
+  unsigned long long state, reserved;
+  unsigned long long pad[6];
 };
-struct ReqCtl {               // per request, 16 bytes
-  unsigned flag;              // epoch of the published decision record
-  unsigned pad[3];
+struct Partial {              // per (request, position, chunk, consumer warp)
+  float a, b, c, d;           // sampling: m_t, s_t, m_d, s_d; greedy: value, index, nan, 0
 };
+// Decision record of a request (written by decide, read by residual and draw).
+enum { MODE_INVALID = 0, MODE_REJECT = 1, MODE_BONUS = 2, MODE_TARGET = 3 };
 struct Record {               // per request, 48 bytes
   int k, mode;
   float mt, kf;               // max logit of target row k; log2(e)/T in fp32
-  unsigned epoch;
   float ist_hi, ist_lo;       // 1/S_t of row k as an unevaluated float pair (fp64 precision)
   float c0_hi, c0_lo;         // log2(P_d/P_t) = (l_d - l_t) * kf + c0 on row k, c0 as a pair
-  int pad[3];
+  int pad[4];
 };
-// Published values: (epoch << 32) | 32-bit payload, written with aligned
-// 8-byte stores (single-copy atomic), so each word is either this launch's
-// or visibly not.
-struct Partial {              // per (request, position, chunk, consumer warp), 32 bytes
-  unsigned long long w[4];    // sampling: m_t, s_t, m_d, s_d; greedy: value, index, nan, 0
+struct Mass {                 // per (request, phase-2 chunk, consumer warp)
+  float hi, lo;               // the sub-range's mass as an unevaluated float pair
 };
-struct ZPart {                // per (request, phase-2 chunk), 128 bytes
-  unsigned long long w[2 * NCW];  // each sub-range's fp64 mass as (lo, hi) halves
-};
-// A row's decision inputs, staged in shared memory by the D task's warps.
+// A row's decision inputs, in shared memory of the decide kernel.
 struct RowStat {
   float mt, md;               // row maxima
-  double St, Sd;              // sum of 2^((l - max) * kf) over the row, fp64
-  float pt, pd;               // P_t(x_i), P_d(x_i)
-  int acc, bad, amax, pad;    // accept bit, SV_ST_* bits, greedy argmax
+  double St, Sd;              // sum of 2^((l - max) * kf) over the row
+  int bad, amax;              // SV_ST_* bits, greedy argmax
 };
-
-static_assert(sizeof(Ctrl) == 64 && sizeof(ReqCtl) == 16 && sizeof(Record) == 48 &&
-                  sizeof(Partial) == 32 && sizeof(ZPart) == 16 * NCW && sizeof(RowStat) == 48,
-              "workspace record sizes");
+static_assert(sizeof(Ctrl) == 64 && sizeof(Partial) == 16 && sizeof(Record) == 48 &&
+                  sizeof(Mass) == 8,
+              "layout");
 
 struct Layout {
-  size_t ctrl, req, rec, part, z2, total;
+  size_t ctrl, part, rec, mass, total;
   int nch1_max, nch2_max;
 };
 
@@ -134,11 +113,10 @@ Layout make_layout(int B, int gamma, int V) {
   L.nch1_max = int(min((long long)(V + CH1_MIN - 1) / CH1_MIN, max(by_bytes, by_tasks)));
   L.nch2_max = (V + CH2_F32 - 1) / CH2_F32;
   L.ctrl = 0;
-  L.req = align256(sizeof(Ctrl));
-  L.rec = L.req + align256(size_t(B) * sizeof(ReqCtl));
-  L.part = L.rec + align256(size_t(B) * sizeof(Record));
-  L.z2 = L.part + align256(size_t(B) * R * L.nch1_max * NCW * sizeof(Partial));
-  L.total = L.z2 + align256(size_t(B) * L.nch2_max * sizeof(ZPart));
+  L.part = align256(sizeof(Ctrl));
+  L.rec = L.part + align256(size_t(B) * R * L.nch1_max * NCW * sizeof(Partial));
+  L.mass = L.rec + align256(size_t(B) * sizeof(Record));
+  L.total = L.mass + align256(size_t(B) * L.nch2_max * NCW * sizeof(Mass));
   return L;
 }
 
@@ -152,50 +130,19 @@ struct Params {
   const float* u_res;
   const float* temp;
   int B, gamma, V, R;
-  int ch1, nch1, ch2, nch2, sub, lag;
+  int ch1, nch1, ch2, nch2, sub;
   int np1;                    // phase-1 partials per row: one per (chunk, consumer warp)
-  long long n1, n2, total;
-  bool draw;                  // sampling: the task order has P2 and T3 tasks
-  // the task order as regions of blocks of constant composition: region r
-  // covers blocks [rj[r], rj[r+1]) of rsz[r] tasks each, starting at task rc[r]
-  int nreg;
-  long long rj[9], rc[9];
-  int rsz[8];
+  long long tasks;            // phase-1 chunks, B * R * nch1
   int32_t* out_tokens;
   int32_t* out_n;
   float* out_p;
   float* out_Z;
   int32_t* status;
   Ctrl* ctrl;
-  ReqCtl* req;
-  Record* rec;
   Partial* part;
-  ZPart* z2;
+  Record* rec;
+  Mass* mass;
 };
-
-// Shared-memory control block (after the slots).
-struct Desc {                 // one slot's task, written by the producer, 96 bytes
-  int kind, b, i, c;          // i: row position (P1) or the drawn row (P2); c: chunk
-  int e0, n;                  // element range of the chunk within the row
-  int head_t, nb_t;           // target: leading single elements, aligned body elements in smem
-  int head_d, nb_d;           // draft likewise
-  float kf;                   // sampling: log2(e) / T of the request
-  int pad;
-  Record rec;                 // P2: the request's decision record
-};
-struct SmemCtl {
-  unsigned long long full[NSLOT], empty[NSLOT];      // data ring: producer <-> consumers
-  unsigned long long staged[NSTAGE], freed[NSTAGE];  // staging ring: consumers <-> booking warp
-  Desc desc[NSLOT];
-  Desc sdesc[NSTAGE];                                // the task of each staging entry
-  RowStat rows[NSTAGE][MAXR];
-  int defer[16];                                     // T3 requests held back by the booking warp
-  float kf_tab[2048];                                // log2(e)/T of the first 2048 requests
-  unsigned epoch;
-  int abort;
-};
-constexpr size_t SMEM_BYTES = size_t(NSLOT) * SLOT + sizeof(SmemCtl);
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 // -------------------------------------------------------- device helpers
 
@@ -252,30 +199,10 @@ __device__ __forceinline__ uint32_t bmax_nan(uint32_t a, uint32_t b) {
 }
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
-}
-
-// A decision record as stored by another CTA (read through L2).
-__device__ __forceinline__ Record load_record(const Record* p) {
-  Record r;
-  const int4 a = __ldcg(reinterpret_cast<const int4*>(p));
-  const int4 b = __ldcg(reinterpret_cast<const int4*>(p) + 1);
-  const int4 c = __ldcg(reinterpret_cast<const int4*>(p) + 2);
-  r.k = a.x; r.mode = a.y; r.mt = __int_as_float(a.z); r.kf = __int_as_float(a.w);
-  r.epoch = unsigned(b.x); r.ist_hi = __int_as_float(b.y); r.ist_lo = __int_as_float(b.z);
-  r.c0_hi = __int_as_float(b.w);
-  r.c0_lo = __int_as_float(c.x);
-  r.pad[0] = r.pad[1] = r.pad[2] = 0;
-  return r;
 }
 
 // ----------------------------------------------------- mbarrier and TMA
@@ -318,51 +245,26 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
 __device__ __forceinline__ void set_status(const Params& P, int bits) {
   if (bits && P.status) atomicOr(P.status, bits);
 }
-// Evidence that the workspace did not hold what this launch wrote (a record
-// or partial with another epoch): the call's results are void.
-__device__ __forceinline__ void mark_dirty(const Params& P) { set_status(P, SV_ST_WORKSPACE); }
 
-__device__ __forceinline__ void give_up(const Params& P, SmemCtl& C) {
-  atomicExch(&P.ctrl->abort, 1);
-  set_status(P, SV_ST_TIMEOUT);
-  *reinterpret_cast<volatile int*>(&C.abort) = 1;
-}
-
-// Wait for phase `parity` of an mbarrier; false after one second or when the
-// launch was aborted.
-__device__ bool mbar_wait(unsigned long long* bar, unsigned parity, const Params& P, SmemCtl& C) {
+// Bounded wait for phase `parity` of an mbarrier (the reduce kernel's waits are
+// all within one CTA): false once the CTA gave up, or after one second, which
+// records SV_ST_TIMEOUT and makes the CTA's other waiters give up too.
+__device__ bool mbar_wait(unsigned long long* bar, unsigned parity, const Params& P,
+                          volatile int* cta_abort) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  for (unsigned it = 1;; ++it) {
+  for (;;) {
     if (mbar_try(bar, parity)) return true;
-    if ((it & 3u) == 0u) {
-      if (*reinterpret_cast<volatile int*>(&C.abort)) return false;
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-        give_up(P, C);
-        return false;
-      }
+    if (*cta_abort) return false;
+    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+      *cta_abort = 1;
+      set_status(P, SV_ST_TIMEOUT);
+      return false;
     }
   }
 }
 
-// Published words: (epoch << 32) | payload.
-__device__ __forceinline__ unsigned long long tagged(unsigned epoch, uint32_t v) {
-  return ((unsigned long long)epoch << 32) | v;
-}
-__device__ __forceinline__ void st_pair(void* p, unsigned long long a, unsigned long long b) {
-  asm volatile("st.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
-}
-__device__ __forceinline__ void ld_pair(const void* p, unsigned long long& a, unsigned long long& b) {
-  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
-__device__ __forceinline__ bool is_mine(unsigned long long w, unsigned epoch) {
-  return unsigned(w >> 32) == epoch;
-}
-__device__ __forceinline__ float payload_f(unsigned long long w) {
-  return __uint_as_float(unsigned(w & 0xffffffffull));
-}
-
-// ------------------------------------------------------- element types
+// ------------------------------------------------- element access
 
 template <int DT>
 struct Elem;
@@ -371,9 +273,6 @@ struct Elem<SV_F32> {
   static constexpr int ES = 4, VEC = 4;
   __device__ static float load(const unsigned char* base, long long idx) {
     return __ldg(reinterpret_cast<const float*>(base) + idx);
-  }
-  __device__ static float lds(const unsigned char* base, int idx) {
-    return reinterpret_cast<const float*>(base)[idx];
   }
   __device__ static void unpack(const uint4& v, float* f) {
     f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
@@ -408,9 +307,6 @@ struct Elem<SV_BF16> {
     return __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short*>(base) + idx))
                            << 16);
   }
-  __device__ static float lds(const unsigned char* base, int idx) {
-    return __uint_as_float(uint32_t(reinterpret_cast<const unsigned short*>(base)[idx]) << 16);
-  }
   __device__ static void unpack(const uint4& v, float* f) {
     f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
     f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
@@ -434,31 +330,109 @@ struct Elem<SV_BF16> {
 };
 
 // ------------------------------------------------- reductions and merges
-// (m, s) pairs: s = sum of 2^((l - m) * kf).  NaN sticks in s; an all -inf
-// set keeps m = -inf, s = 0.  Argmax triples (value, lowest index, NaN seen):
+
+// Argmax triples (value, lowest index, NaN seen).
 __device__ __forceinline__ void am_merge(float& best, int& bi, int& nan, float b2, int i2, int n2) {
   if (b2 > best || (b2 == best && i2 < bi)) { best = b2; bi = i2; }
   nan |= n2;
 }
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+// Error-free sum of two floats (Knuth's two-sum): s + err == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& err) {
+  s = a + b;
+  const float bb = s - a;
+  err = (a - (s - bb)) + (b - bb);
 }
-__device__ __forceinline__ double warp_incl_scan_d(double v, int lane) {
+// Running sum as an unevaluated float pair (hi, lo): add x and renormalise.
+__device__ __forceinline__ void ff_add(float& hi, float& lo, float x) {
+  float s, e;
+  two_sum(hi, x, s, e);
+  const float t = lo + e;
+  hi = s + t;
+  lo = t - (hi - s);
+}
+// Sum of two float pairs.
+__device__ __forceinline__ void ff_add2(float& hi, float& lo, float h2, float l2) {
+  float s, e;
+  two_sum(hi, h2, s, e);
+  const float t = lo + l2 + e;
+  hi = s + t;
+  lo = t - (hi - s);
+}
+// Warp-wide sum of float pairs (about 48 significant bits), valid in every lane.
+__device__ __forceinline__ void warp_sum_ff(float& hi, float& lo) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    ff_add2(hi, lo, h2, l2);
+  }
+}
+// Inclusive warp prefix sum of float pairs, lane order.
+__device__ __forceinline__ void warp_scan_ff(float& hi, float& lo, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
+    const float h2 = __shfl_up_sync(0xffffffffu, hi, o);
+    const float l2 = __shfl_up_sync(0xffffffffu, lo, o);
+    if (lane >= o) ff_add2(hi, lo, h2, l2);
   }
-  return v;
+}
+__device__ __forceinline__ double ff_val(float hi, float lo) { return double(hi) + double(lo); }
+
+// 2^x in fp64 for the acceptance test: x = n + f with n = rint(x) and
+// |f| <= 1/2, e^(f ln 2) by its Taylor series to degree 11 (truncation below
+// 1e-14 relative), scaled by 2^n built in the exponent field in two factors.
+// Out-of-range x saturate to 0 or +inf; NaN stays NaN.
+__device__ __forceinline__ double exp2_d(double x) {
+  if (!(x > -1075.0)) return x != x ? x : 0.0;
+  if (x > 1024.0) return INFINITY;
+  const double n = rint(x);
+  const double t = (x - n) * 0.69314718055994530942;
+  double p = 1.0 / 39916800.0;                    // 1/11!
+  p = fma(p, t, 1.0 / 3628800.0);
+  p = fma(p, t, 1.0 / 362880.0);
+  p = fma(p, t, 1.0 / 40320.0);
+  p = fma(p, t, 1.0 / 5040.0);
+  p = fma(p, t, 1.0 / 720.0);
+  p = fma(p, t, 1.0 / 120.0);
+  p = fma(p, t, 1.0 / 24.0);
+  p = fma(p, t, 1.0 / 6.0);
+  p = fma(p, t, 0.5);
+  p = fma(p, t, 1.0);
+  p = fma(p, t, 1.0);
+  const int ni = int(n);
+  const int n1 = ni / 2, n2 = ni - n1;
+  return p * __longlong_as_double((long long)(n1 + 1023) << 52) *
+         __longlong_as_double((long long)(n2 + 1023) << 52);
 }
 
-// ------------------------------------------------ P1: consumer reductions
+__device__ __forceinline__ bool row_ok(float m, double S) {
+  return (m > -INFINITY) && (m < INFINITY) && (S > 0.0) && (S < INFINITY);
+}
 
-// Vectors of one row chunk a consumer thread owns: body vector j belongs to
-// consumer thread j mod (NCW*32); a 16 KB chunk gives each thread at most
-// MAXV vectors, held in registers.
+// ------------------------------------------------ reduce: slots
+
+// One slot's chunk, written by the producer.
+struct alignas(16) Desc {
+  int end;                    // 1: no more chunks for this CTA
+  int b, i, c;                // request, row position, chunk
+  int e0, n;                  // element range of the chunk within the row
+  int head_t, nb_t;           // target: leading single elements, aligned body elements in smem
+  int head_d, nb_d;           // draft likewise
+  float kf;                   // sampling: log2(e) / T of the request
+  int pad;
+};
+// Shared-memory control block of the reduce kernel (after the slots).
+struct SmemCtl {
+  unsigned long long full[NSLOT], empty[NSLOT];
+  Desc desc[NSLOT];
+  int abort;
+};
+constexpr size_t SMEM_BYTES = size_t(NSLOT) * SLOT + sizeof(SmemCtl);
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+
+// ------------------------------------------------ phase 1: consumer reductions
+
 constexpr int MAXV = (HALF / 16 + NCW * 32 - 1) / (NCW * 32);
 static_assert(MAXV * 16 * NCW * 32 >= HALF, "chunk split");
 
@@ -691,256 +665,187 @@ __device__ __forceinline__ float vec_weights(const Record& r, const uint4& t, co
   return a + b;
 }
 
-// Mass of this warp's contiguous sub-range [cw*sub, (cw+1)*sub) of a P2
-// chunk held in a slot (target body at +0, draft body at +HALF).
-template <int DT, typename Release>
-__device__ double warp_p2_mass(const Params& P, const Desc& d, const unsigned char* slot,
-                               int cw, int lane, Release release) {
+// ------------------------------------------------------------ reduce
+
+// Split a chunk at `p` of d.n elements into single leading elements (up to the
+// first 16-byte boundary) and an aligned body of whole vectors.
+template <int DT>
+__device__ __forceinline__ void split(const unsigned char* p, int n, int& head, int& nb) {
   using E = Elem<DT>;
-  const Record& r = d.rec;
-  const bool two = (r.mode == MODE_REJECT);
-  const int lo = cw * P.sub;
-  const int hi = min(lo + P.sub, d.n);
-  if (lo >= hi) {
-    release();
-    return 0.0;
-  }
-  const unsigned char* trow =
-      P.Lt + ((size_t(d.b) * P.R + d.i) * size_t(P.V) + d.e0) * E::ES;
+  const int h = int(((16u - unsigned(reinterpret_cast<uintptr_t>(p) & 15u)) & 15u) / E::ES);
+  head = h < n ? h : n;
+  nb = ((n - head) / E::VEC) * E::VEC;
+}
+
+// Producer (one lane): this CTA's contiguous range of chunks, in order, into
+// the slot ring.  Chunk t is chunk t % nch1 of row t / nch1 (row = b * R + i).
+template <int DT, bool GREEDY>
+__device__ void producer(const Params& P, SmemCtl& C, unsigned char* slots) {
+  using E = Elem<DT>;
+  const long long G = gridDim.x;
+  const long long t0 = P.tasks * blockIdx.x / G, t1 = P.tasks * (blockIdx.x + 1) / G;
+  const long long row0 = t0 / P.nch1;
+  int c = int(t0 - row0 * P.nch1);
+  int b = int(row0 / P.R), i = int(row0 - (long long)b * P.R);
+  float T = GREEDY ? 1.f : __ldg(P.temp + b);
+  float T_next = (!GREEDY && b + 1 < P.B) ? __ldg(P.temp + b + 1) : 1.f;
+  const unsigned char* trow = P.Lt + (size_t(b) * P.R + i) * size_t(P.V) * E::ES;
   const unsigned char* drow =
-      two ? P.Ld + ((size_t(d.b) * P.gamma + r.k) * size_t(P.V) + d.e0) * E::ES : nullptr;
-  float acc = 0.f;
-  if (d.head_t == 0 && (!two || d.head_d == 0)) {
-    // aligned: whole 16-byte vectors from shared memory, held in registers
-    constexpr int PV = 5;  // vectors per lane held in registers (a sub-range has <= 32*PV)
-    const uint4* tv = reinterpret_cast<const uint4*>(slot);
-    const uint4* dv = reinterpret_cast<const uint4*>(slot + HALF);
-    const int j0 = lo / E::VEC, vhi = min(hi, d.nb_t) / E::VEC;
-    uint4 vt[PV], vd[PV];
-#pragma unroll
-    for (int u = 0; u < PV; ++u) {
-      const int j = j0 + lane + 32 * u;
-      vt[u] = j < vhi ? tv[j] : make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD,
-                                           E::NEG_INF_WORD);
-      vd[u] = (two && j < vhi) ? dv[j] : vt[u];
+      (!GREEDY && i < P.gamma) ? P.Ld + (size_t(b) * P.gamma + i) * size_t(P.V) * E::ES : nullptr;
+  for (long long t = t0, seq = 0; t <= t1; ++t, ++seq) {
+    const int s = int(seq % NSLOT);
+    const unsigned use = unsigned(seq / NSLOT);
+    if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, &C.abort)) return;
+    Desc& d = C.desc[s];
+    if (t == t1 || C.abort) {
+      d.end = 1;
+      mbar_arrive(&C.full[s]);
+      return;
     }
-    for (int j = j0 + lane + 32 * PV; j < vhi; j += 32)  // only if sub exceeds 32*PV vectors
-      acc += vec_weights<DT>(r, tv[j], two ? dv[j] : tv[j], two);
-    release();
-#pragma unroll
-    for (int u = 0; u < PV; ++u) acc += vec_weights<DT>(r, vt[u], vd[u], two);
-    for (int e = max(lo, d.nb_t) + lane; e < hi; e += 32)
-      acc += weight(r, E::load(trow, e), two ? E::load(drow, e) : 0.f);
-  } else {
-    // unaligned rows: element by element, from shared memory where held
-    for (int e = lo + lane; e < hi; e += 32) {
-      const int et = e - d.head_t, ed = e - d.head_d;
-      const float lt = (et >= 0 && et < d.nb_t) ? E::lds(slot, et) : E::load(trow, e);
-      float ld = 0.f;
-      if (two) ld = (ed >= 0 && ed < d.nb_d) ? E::lds(slot + HALF, ed) : E::load(drow, e);
-      acc += weight(r, lt, ld);
+    d.end = 0;
+    d.b = b; d.i = i; d.c = c;
+    d.e0 = c * P.ch1;
+    d.n = min(P.ch1, P.V - d.e0);
+    d.kf = LOG2E_F / T;
+    const unsigned char* tseg = trow + size_t(d.e0) * E::ES;
+    const unsigned char* dseg = drow ? drow + size_t(d.e0) * E::ES : nullptr;
+    split<DT>(tseg, d.n, d.head_t, d.nb_t);
+    d.head_d = d.nb_d = 0;
+    if (dseg) split<DT>(dseg, d.n, d.head_d, d.nb_d);
+    const unsigned bt = unsigned(d.nb_t) * E::ES, bd = unsigned(d.nb_d) * E::ES;
+    if (bt + bd == 0u) {
+      mbar_arrive(&C.full[s]);
+    } else {
+      mbar_arrive_tx(&C.full[s], bt + bd);
+      if (bt) bulk_g2s(slots + size_t(s) * SLOT, tseg + size_t(d.head_t) * E::ES, bt, &C.full[s]);
+      if (bd)
+        bulk_g2s(slots + size_t(s) * SLOT + HALF, dseg + size_t(d.head_d) * E::ES, bd,
+                 &C.full[s]);
     }
-    release();
-  }
-  return warp_sum_d(double(acc));
-}
-
-// ------------------------------------------------------------ waiting
-
-// Poll until every lane's `ready` is true (re-evaluated by `probe`), for at
-// most one second; false on timeout or abort.
-template <typename Probe>
-__device__ bool warp_poll(const Params& P, SmemCtl& C, Probe probe) {
-  if (__all_sync(0xffffffffu, probe())) return true;
-  const unsigned long long t0 = globaltimer();
-  unsigned ns = 64;
-  for (;;) {
-    __nanosleep(ns);
-    ns = ns < 2048 ? 2 * ns : ns;
-    if (__all_sync(0xffffffffu, probe())) return true;
-    const bool stop = *reinterpret_cast<volatile int*>(&P.ctrl->abort) ||
-                      *reinterpret_cast<volatile int*>(&C.abort);
-    if (__any_sync(0xffffffffu, stop)) return false;
-    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-      if ((threadIdx.x & 31) == 0) give_up(P, C);
-      __syncwarp();
-      return false;
+    // the next chunk
+    if (++c == P.nch1) {
+      c = 0;
+      if (++i == P.R) {
+        i = 0;
+        ++b;
+        T = T_next;
+        if (!GREEDY && b + 1 < P.B) T_next = __ldg(P.temp + b + 1);
+      }
+      trow = P.Lt + (size_t(b) * P.R + i) * size_t(P.V) * E::ES;
+      drow = (!GREEDY && i < P.gamma) ? P.Ld + (size_t(b) * P.gamma + i) * size_t(P.V) * E::ES
+                                      : nullptr;
     }
   }
 }
 
-// ------------------------------------------------------------ decisions
-
-__device__ __forceinline__ bool row_ok(float m, double S) {
-  return (m > -INFINITY) && (m < INFINITY) && (S > 0.0) && (S < INFINITY);
-}
-
-// A row's published partials: one per (chunk, consumer warp), row-major.
-__device__ __forceinline__ const Partial* row_partials(const Params& P, int b, int i) {
-  return P.part + (size_t(b) * P.R + i) * size_t(P.np1);
-}
-
-// Wait until all chunk partials of one row carry this launch's epoch.
-__device__ bool wait_partials(const Params& P, SmemCtl& C, const Partial* pp) {
-  const unsigned epoch = C.epoch;
-  const int lane = threadIdx.x & 31;
-  return warp_poll(P, C, [&]() {
-    bool ok = true;
-    for (int c = lane; c < P.np1; c += 32) {
-      unsigned long long a, b, c2, d;
-      ld_pair(&pp[c].w[0], a, b);
-      ld_pair(&pp[c].w[2], c2, d);
-      ok = ok && is_mine(a, epoch) && is_mine(b, epoch) && is_mine(c2, epoch) && is_mine(d, epoch);
-    }
-    return ok;
-  });
-}
-
-// Combine of one row's partials (m_c, s_c) held in words (0, 1)
-// or (2, 3); one warp, result valid in every lane.
-__device__ void warp_row_combine(const Partial* pp, int nch, int f, float kf, float& m_out,
-                                 double& S_out) {
-  const int lane = threadIdx.x & 31;
-  float m = -INFINITY;
-  for (int c = lane; c < nch; c += 32) {
-    unsigned long long a, b;
-    ld_pair(&pp[c].w[f], a, b);
-    m = fmaxf(m, payload_f(a));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  double S = 0.0;
-  for (int c = lane; c < nch; c += 32) {
-    unsigned long long a, b;
-    ld_pair(&pp[c].w[f], a, b);
-    const float mc = payload_f(a), sc = payload_f(b);
-    S += (m == -INFINITY) ? double(sc) : double(sc) * double(ex2((mc - m) * kf));
-  }
-  m_out = m;
-  S_out = warp_sum_d(S);
-}
-
-// Row i of request b for the D task (one warp): lane 0 fills `out`.  The
-// loads that do not depend on the partials (the draft token, its logits, the
-// uniform) are issued first; the row's chunk partials are read into
-// registers as soon as all carry this launch's epoch, the row maximum taken,
-// and the sum rescaled in fp64 (one exponential per chunk).
-constexpr int PCAP = 5;  // partials per lane held in registers (rows of <= 160 partials)
-
-template <int DT>
-__device__ void row_decide_sample(const Params& P, SmemCtl& C, int b, int i, float kf,
-                                  RowStat& out) {
+// Consumers: every warp reduces its share of each slot from registers (the
+// slot is handed back as soon as the share is loaded) and publishes its own
+// partial.
+template <int DT, bool GREEDY>
+__device__ void consumer(const Params& P, SmemCtl& C, const unsigned char* slots) {
   using E = Elem<DT>;
-  const int g = P.gamma, R = P.R, V = P.V;
-  const int lane = threadIdx.x & 31;
-  const unsigned epoch = C.epoch;
-  const float T = __ldg(P.temp + b);
-  const bool t_ok = isfinite(T) && T >= 0x1p-126f;
-  const double k64 = LOG2E_D / double(T);
-  int xi = 0;
-  float lt = 0.f, ld = 0.f, u = 0.f;
-  bool tok_ok = true;
-  if (lane == 0 && i < g) {
-    xi = __ldg(P.x + size_t(b) * g + i);
-    u = __ldg(P.u_acc + size_t(b) * g + i);
-    tok_ok = xi >= 0 && xi < V;
-    if (tok_ok) {
-      lt = E::load(P.Lt, (long long)(size_t(b) * R + i) * V + xi);
-      ld = E::load(P.Ld, (long long)(size_t(b) * g + i) * V + xi);
+  const int cw = int(threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
+  for (long long seq = 0;; ++seq) {
+    const int s = int(seq % NSLOT);
+    const unsigned use = unsigned(seq / NSLOT);
+    if (!mbar_wait(&C.full[s], use & 1u, P, &C.abort)) return;
+    const Desc d = C.desc[s];
+    const unsigned char* slot = slots + size_t(s) * SLOT;
+    auto release = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&C.empty[s]);
+    };
+    if (d.end) return;
+    const unsigned char* tseg = P.Lt + ((size_t(d.b) * P.R + d.i) * size_t(P.V) + d.e0) * E::ES;
+    float4 out;
+    if (GREEDY) {
+      float best;
+      int bi, nan;
+      warp_argmax<DT>(slot, d.nb_t, tseg, d.head_t, d.n, d.e0, cw, lane, best, bi, nan, release);
+      out = make_float4(best, __int_as_float(bi), __int_as_float(nan), 0.f);
+    } else {
+      const bool has_d = d.i < P.gamma;
+      const unsigned char* dseg =
+          has_d ? P.Ld + ((size_t(d.b) * P.gamma + d.i) * size_t(P.V) + d.e0) * E::ES : nullptr;
+      warp_ms2<DT>(slot, slot + HALF, d, tseg, dseg, has_d, d.kf, cw, lane, out, release);
     }
-  }
-  const Partial* pp = row_partials(P, b, i);
-  float mt = -INFINITY, md = -INFINITY;
-  double St = 0.0, Sd = 0.0;
-  bool ready;
-  if (P.np1 <= 32 * PCAP) {
-    unsigned long long w[PCAP][4];
-    ready = warp_poll(P, C, [&]() {
-      bool ok = true;
-#pragma unroll
-      for (int q = 0; q < PCAP; ++q) {
-        const int c = lane + 32 * q;
-        if (c < P.np1) {
-          ld_pair(&pp[c].w[0], w[q][0], w[q][1]);
-          ld_pair(&pp[c].w[2], w[q][2], w[q][3]);
-          ok = ok && is_mine(w[q][0], epoch) && is_mine(w[q][1], epoch) &&
-               is_mine(w[q][2], epoch) && is_mine(w[q][3], epoch);
-        }
-      }
-      return ok;
-    });
-    if (ready) {
-#pragma unroll
-      for (int q = 0; q < PCAP; ++q)
-        if (lane + 32 * q < P.np1) {
-          mt = fmaxf(mt, payload_f(w[q][0]));
-          md = fmaxf(md, payload_f(w[q][2]));
-        }
-      mt = warp_max(mt);
-      md = warp_max(md);
-#pragma unroll
-      for (int q = 0; q < PCAP; ++q)
-        if (lane + 32 * q < P.np1) {
-          const float m0 = payload_f(w[q][0]), s0 = payload_f(w[q][1]);
-          const float m1 = payload_f(w[q][2]), s1 = payload_f(w[q][3]);
-          St += (mt == -INFINITY) ? double(s0) : double(s0) * double(ex2((m0 - mt) * kf));
-          Sd += (md == -INFINITY) ? double(s1) : double(s1) * double(ex2((m1 - md) * kf));
-        }
-      St = warp_sum_d(St);
-      Sd = warp_sum_d(Sd);
+    if (lane == 0) {
+      Partial* dst = P.part + ((size_t(d.b) * P.R + d.i) * P.nch1 + d.c) * NCW + cw;
+      *reinterpret_cast<float4*>(dst) = out;
     }
-  } else {  // very long rows: poll, then two passes over the partials
-    ready = wait_partials(P, C, pp);
-    if (ready) {
-      warp_row_combine(pp, P.np1, 0, kf, mt, St);
-      warp_row_combine(pp, P.np1, 2, kf, md, Sd);
-    }
-  }
-  if (i >= g) { md = 0.f; Sd = 1.0; }
-  if (lane == 0) {
-    int bad = ready ? 0 : SV_ST_TIMEOUT;
-    if (!row_ok(mt, St) || (i < g && !row_ok(md, Sd))) bad |= SV_ST_NONFINITE;
-    float pt = NAN, pd = NAN;
-    int acc = 1;
-    if (i < g) {
-      if (!tok_ok) {
-        bad |= SV_ST_BAD_TOKEN;
-      } else if (bad == 0 && t_ok) {
-        const double dpt = exp2((double(lt) - double(mt)) * k64) / St;
-        const double dpd = exp2((double(ld) - double(md)) * k64) / Sd;
-        const double r = dpd > 0.0 ? fmin(1.0, dpt / dpd) : 1.0;
-        acc = double(u) <= r;
-        pt = float(dpt);
-        pd = float(dpd);
-      }
-    }
-    out.mt = mt; out.md = md; out.St = St; out.Sd = Sd; out.pt = pt; out.pd = pd;
-    out.acc = acc; out.bad = bad; out.amax = -1; out.pad = 0;
   }
 }
 
-template <int DT>
-__device__ void row_decide_greedy(const Params& P, SmemCtl& C, int b, int i, RowStat& out) {
-  const int g = P.gamma, V = P.V;
-  const int lane = threadIdx.x & 31;
-  const unsigned epoch = C.epoch;
-  const Partial* pp = row_partials(P, b, i);
-  const int np = P.np1;
-  float best = -INFINITY;
-  int bi = INT_MAX, nan = 0;
-  const bool ready = warp_poll(P, C, [&]() {
-    best = -INFINITY; bi = INT_MAX; nan = 0;
-    bool ok = true;
-    for (int q = lane; q < np; q += 32) {
-      unsigned long long a, bb, cc, dd;
-      ld_pair(&pp[q].w[0], a, bb);
-      ld_pair(&pp[q].w[2], cc, dd);
-      ok = ok && is_mine(a, epoch) && is_mine(bb, epoch) && is_mine(cc, epoch) &&
-           is_mine(dd, epoch);
-      am_merge(best, bi, nan, payload_f(a), int(bb & 0xffffffffull), int(cc & 0xffffffffull));
+template <int DT, bool GREEDY>
+__global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* slots = smem;
+  SmemCtl& C = *reinterpret_cast<SmemCtl*>(smem + size_t(NSLOT) * SLOT);
+  if (threadIdx.x == 0) {
+    C.abort = 0;
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&C.full[s], 1);
+      mbar_init(&C.empty[s], NCW);
     }
-    return ok;
-  });
+    // the workspace is in its ready state between calls; mark this call
+    if (blockIdx.x == 0) {
+      if (P.ctrl->state != 0ull || P.ctrl->reserved != 0ull) set_status(P, SV_ST_WORKSPACE);
+      P.ctrl->state = 1ull;
+      P.ctrl->reserved = 0ull;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    if (threadIdx.x == 0) producer<DT, GREEDY>(P, C, slots);
+  } else {
+    consumer<DT, GREEDY>(P, C, slots);
+  }
+}
+
+// ------------------------------------------------------------ decide
+
+// Combine of row i of request b (one warp): the maximum m of the partials'
+// maxima and S = sum s_c * 2^((m_c - m) * kf), accumulated as float pairs.
+// Target in fields (a, b), draft in (c, d).  Result valid in every lane.
+__device__ void row_combine(const Partial* pp, int np, float kf, bool draft, float& mt,
+                            double& St, float& md, double& Sd) {
+  const int lane = threadIdx.x & 31;
+  mt = -INFINITY;
+  md = -INFINITY;
+  for (int c = lane; c < np; c += 32) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(pp + c));
+    mt = fmaxf(mt, v.x);
+    md = fmaxf(md, v.z);
+  }
+  mt = warp_max(mt);
+  md = warp_max(md);
+  float th = 0.f, tl = 0.f, dh = 0.f, dl = 0.f;
+  for (int c = lane; c < np; c += 32) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(pp + c));
+    ff_add(th, tl, (mt == -INFINITY) ? v.y : v.y * ex2((v.x - mt) * kf));
+    if (draft) ff_add(dh, dl, (md == -INFINITY) ? v.w : v.w * ex2((v.z - md) * kf));
+  }
+  warp_sum_ff(th, tl);
+  St = ff_val(th, tl);
+  if (draft) {
+    warp_sum_ff(dh, dl);
+    Sd = ff_val(dh, dl);
+  } else {
+    md = 0.f;
+    Sd = 1.0;
+  }
+}
+
+// Argmax of row i of request b (one warp) over its partials.
+__device__ void row_argmax(const Partial* pp, int np, float& best, int& bi, int& nan) {
+  const int lane = threadIdx.x & 31;
+  best = -INFINITY;
+  bi = INT_MAX;
+  nan = 0;
+  for (int c = lane; c < np; c += 32) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(pp + c));
+    am_merge(best, bi, nan, v.x, __float_as_int(v.y), __float_as_int(v.z));
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
@@ -948,35 +853,40 @@ __device__ void row_decide_greedy(const Params& P, SmemCtl& C, int b, int i, Row
     const int n2 = __shfl_xor_sync(0xffffffffu, nan, o);
     am_merge(best, bi, nan, b2, i2, n2);
   }
-  if (lane == 0) {
-    int bad = ready ? 0 : SV_ST_TIMEOUT;
-    if (nan || bi == INT_MAX || best == INFINITY) bad |= SV_ST_NONFINITE;
-    if (i < g) {
-      const int xi = __ldg(P.x + size_t(b) * g + i);
-      if (xi < 0 || xi >= V) bad |= SV_ST_BAD_TOKEN;
-    }
-    out.mt = best; out.md = 0.f; out.St = out.Sd = 0.0; out.pt = out.pd = 0.f;
-    out.acc = 0; out.bad = bad; out.amax = bi; out.pad = 0;
-  }
 }
 
-// Request decision of the D task, by the booking warp, from the rows staged
-// in shared memory: first rejection k, every output but token k, and the
-// decision record.  The slot is freed as soon as the rows are in registers.
+// Sampling decision of request b (warp 0 of the CTA, rows in `rows`): lane
+// i < gamma tests position i, accept iff u <= min(1, P_t / P_d) with
+// P_t / P_d = 2^((l_t - m_t) * k - (l_d - m_d) * k) * S_d / S_t in fp64;
+// then the first rejection k, the outputs but token k, and the record.
 template <int DT>
-__device__ void request_decide_sample(const Params& P, SmemCtl& C, int e, int b) {
+__device__ void decide_sample(const Params& P, int b, const RowStat* rows, float lt, float ld,
+                              float u, bool tok_ok, int xi) {
   const int g = P.gamma, R = P.R;
   const int lane = threadIdx.x & 31;
-  const unsigned epoch = C.epoch;
   const float T = __ldg(P.temp + b);
   const bool t_ok = isfinite(T) && T >= 0x1p-126f;
   const float kf = LOG2E_F / T;
+  const double k64 = LOG2E_D / double(T);
   int bad = 0, acc = 1;
   float pt = NAN, pd = NAN;
-  for (int i = lane; i < R; i += 32) {
-    const RowStat& r = C.rows[e][i];
-    bad |= r.bad;
-    if (i == lane) { acc = r.acc; pt = r.pt; pd = r.pd; }
+  for (int i = lane; i < R; i += 32) bad |= rows[i].bad;
+  if (lane < g) {
+    const RowStat& r = rows[lane];
+    if (!tok_ok) {
+      bad |= SV_ST_BAD_TOKEN;
+    } else if (bad == 0 && t_ok) {
+      const double et = (double(lt) - double(r.mt)) * k64;  // log2(P_t * S_t)
+      const double ed = (double(ld) - double(r.md)) * k64;
+      // P_d = 0 (including its fp64 underflow, ed far below -1000) accepts
+      const bool pd_zero = ld == -INFINITY || (ed < -1000.0 && exp2_d(ed) / r.Sd == 0.0);
+      const double ratio = pd_zero ? 1.0 : fmin(1.0, exp2_d(et - ed) * (r.Sd / r.St));
+      acc = double(u) <= ratio;
+      if (P.out_p) {
+        pt = float(exp2_d(et) / r.St);
+        pd = float(exp2_d(ed) / r.Sd);
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
@@ -984,13 +894,9 @@ __device__ void request_decide_sample(const Params& P, SmemCtl& C, int e, int b)
   const bool valid = (bad == 0);
   const unsigned rej = __ballot_sync(0xffffffffu, lane < g && !acc);
   const int k = rej ? __ffs(rej) - 1 : g;
-  const RowStat rk = C.rows[e][k];
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&C.freed[e]);  // the staging entry may be reused now
   for (int i = lane; i < R; i += 32) {
-    int tok = -1;
-    if (valid && i < k) tok = __ldg(P.x + size_t(b) * g + i);
-    if (!valid || i != k) P.out_tokens[size_t(b) * R + i] = tok;
+    const int tok = __shfl_sync(0xffffffffu, xi, i & 31);
+    if (!valid || i != k) P.out_tokens[size_t(b) * R + i] = (valid && i < k) ? tok : -1;
   }
   if (P.out_p && lane < g) {
     P.out_p[(size_t(b) * g + lane) * 2] = valid ? pt : NAN;
@@ -1004,10 +910,11 @@ __device__ void request_decide_sample(const Params& P, SmemCtl& C, int e, int b)
     r.k = k;
     r.mode = !valid ? MODE_INVALID : (k < g ? MODE_REJECT : MODE_BONUS);
     r.kf = kf;
-    r.epoch = epoch;
-    r.mt = 0.f; r.ist_hi = r.ist_lo = r.c0_hi = r.c0_lo = 0.f;
-    r.pad[0] = r.pad[1] = r.pad[2] = 0;
+    r.mt = 0.f;
+    r.ist_hi = r.ist_lo = r.c0_hi = r.c0_lo = 0.f;
+    r.pad[0] = r.pad[1] = r.pad[2] = r.pad[3] = 0;
     if (valid) {
+      const RowStat& rk = rows[k];
       r.mt = rk.mt;
       const double ist = 1.0 / rk.St;
       r.ist_hi = float(ist);
@@ -1021,27 +928,30 @@ __device__ void request_decide_sample(const Params& P, SmemCtl& C, int e, int b)
     int4* d = reinterpret_cast<int4*>(P.rec + b);
     const int4* src = reinterpret_cast<const int4*>(&r);
     d[0] = src[0]; d[1] = src[1]; d[2] = src[2];
-    __threadfence();
-    if (atomicExch(&P.req[b].flag, epoch) == epoch) mark_dirty(P);
   }
 }
 
-__device__ void request_decide_greedy(const Params& P, SmemCtl& C, int e, int b) {
+// Greedy decision of request b (warp 0, rows in `rows`).
+__device__ void decide_greedy(const Params& P, int b, const RowStat* rows) {
   const int g = P.gamma, R = P.R;
   const int lane = threadIdx.x & 31;
   int bad = 0;
   int am[2] = {-1, -1};
   for (int i = lane, q = 0; i < R; i += 32, ++q) {
-    bad |= C.rows[e][i].bad;
-    am[q] = C.rows[e][i].amax;
+    bad |= rows[i].bad;
+    am[q] = rows[i].amax;
   }
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&C.freed[e]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+  int xi = -1;
+  if (lane < g) {
+    xi = __ldg(P.x + size_t(b) * g + lane);
+    if (xi < 0 || xi >= P.V) bad |= SV_ST_BAD_TOKEN;
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
   const bool valid = (bad == 0);
-  const unsigned mis =
-      __ballot_sync(0xffffffffu, lane < g && __ldg(P.x + size_t(b) * g + lane) != am[0]);
+  const unsigned mis = __ballot_sync(0xffffffffu, lane < g && xi != am[0]);
   const int k = mis ? __ffs(mis) - 1 : g;
   for (int i = lane, q = 0; i < R; i += 32, ++q)
     P.out_tokens[size_t(b) * R + i] = (valid && i <= k) ? am[q] : -1;
@@ -1051,127 +961,256 @@ __device__ void request_decide_greedy(const Params& P, SmemCtl& C, int e, int b)
   }
 }
 
-// ------------------------------------------------------------------ T3
+// One CTA per request: DECIDE_WARPS warps combine the rows (row i by warp
+// i % DECIDE_WARPS), then warp 0 decides.  The draft tokens, their logits and
+// the uniforms are loaded by warp 0 before its rows.
+template <int DT, bool GREEDY>
+__global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, bool last) {
+  using E = Elem<DT>;
+  __shared__ RowStat rows[MAXR];
+  const int b = blockIdx.x, warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int g = P.gamma, R = P.R, V = P.V;
+  float lt = 0.f, ld = 0.f, u = 0.f;
+  bool tok_ok = true;
+  int xi = -1;
+  if (!GREEDY && warp == 0 && lane < g) {
+    xi = __ldg(P.x + size_t(b) * g + lane);
+    u = __ldg(P.u_acc + size_t(b) * g + lane);
+    tok_ok = xi >= 0 && xi < V;
+    if (tok_ok) {
+      lt = E::load(P.Lt, (long long)(size_t(b) * R + lane) * V + xi);
+      ld = E::load(P.Ld, (long long)(size_t(b) * g + lane) * V + xi);
+    }
+  }
+  const float kf = GREEDY ? 0.f : LOG2E_F / __ldg(P.temp + b);
+  for (int i = warp; i < R; i += DECIDE_WARPS) {
+    const Partial* pp = P.part + (size_t(b) * R + i) * size_t(P.np1);
+    if (GREEDY) {
+      float best;
+      int bi, nan;
+      row_argmax(pp, P.np1, best, bi, nan);
+      if (lane == 0) {
+        RowStat r;
+        r.mt = best; r.md = 0.f; r.St = r.Sd = 0.0;
+        r.bad = (nan || bi == INT_MAX || best == INFINITY) ? SV_ST_NONFINITE : 0;
+        r.amax = bi;
+        rows[i] = r;
+      }
+    } else {
+      float mt, md;
+      double St, Sd;
+      row_combine(pp, P.np1, kf, i < g, mt, St, md, Sd);
+      if (lane == 0) {
+        RowStat r;
+        r.mt = mt; r.md = md; r.St = St; r.Sd = Sd;
+        r.bad = (!row_ok(mt, St) || (i < g && !row_ok(md, Sd))) ? SV_ST_NONFINITE : 0;
+        r.amax = -1;
+        rows[i] = r;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    if (GREEDY) decide_greedy(P, b, rows);
+    else decide_sample<DT>(P, b, rows, lt, ld, u, tok_ok, xi);
+  }
+  // greedy verification ends here: the workspace is ready for the next call
+  if (last && b == 0 && threadIdx.x == 0) P.ctrl->state = 0ull;
+}
 
-// Token k of request b (one warp): wait for the sub-range masses of every
-// phase-2 chunk, find the sub-range where the running mass crosses u * Z and
-// scan it in index order.
+// ------------------------------------------------------------ residual
+
+// Mass of elements [lo, hi) of the row token k is drawn from: target row
+// `trow` and (after a rejection) draft row `drow`; one warp, fp32 weights,
+// lane sums added as float pairs.  Aligned spans are read as 16-byte vectors,
+// PV per lane in flight.
 template <int DT>
-__device__ void task_t3(const Params& P, SmemCtl& C, int b) {
+__device__ void span_mass(const Record& r, const unsigned char* trow, const unsigned char* drow,
+                          int lo, int hi, float& mh, float& ml) {
   using E = Elem<DT>;
   const int lane = threadIdx.x & 31;
-  const unsigned epoch = C.epoch;
-  // the decision record: D(b) was claimed before this task but may still be running
-  const bool decided =
-      warp_poll(P, C, [&]() { return lane != 0 || ld_acquire(&P.req[b].flag) == epoch; });
-  if (!decided) return;  // only after a timeout, which the status reports
-  Record r = load_record(P.rec + b);
+  const bool two = (r.mode == MODE_REJECT);
+  float acc = 0.f;
+  int e_tail = lo;
+  const unsigned char* t0 = trow + size_t(lo) * E::ES;
+  const unsigned char* d0 = two ? drow + size_t(lo) * E::ES : t0;
+  if (((reinterpret_cast<uintptr_t>(t0) | reinterpret_cast<uintptr_t>(d0)) & 15u) == 0) {
+    constexpr int PV = (HALF / 16 + 32 * NCW - 1) / (32 * NCW);
+    const int nv = (hi - lo) / E::VEC;
+    const uint4* tv = reinterpret_cast<const uint4*>(t0);
+    const uint4* dv = reinterpret_cast<const uint4*>(d0);
+    for (int v0 = 0; v0 < nv; v0 += 32 * PV) {
+      uint4 vt[PV], vd[PV];
+#pragma unroll
+      for (int u = 0; u < PV; ++u) {
+        const int j = v0 + lane + 32 * u;
+        const uint4 neg = make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD,
+                                     E::NEG_INF_WORD);
+        vt[u] = j < nv ? __ldg(tv + j) : neg;
+        vd[u] = (two && j < nv) ? __ldg(dv + j) : vt[u];
+      }
+#pragma unroll
+      for (int u = 0; u < PV; ++u) acc += vec_weights<DT>(r, vt[u], vd[u], two);
+    }
+    e_tail = lo + nv * E::VEC;
+  }
+  for (int e = e_tail + lane; e < hi; e += 32)
+    acc += weight(r, E::load(trow, e), two ? E::load(drow, e) : 0.f);
+  mh = acc;
+  ml = 0.f;
+  warp_sum_ff(mh, ml);
+}
+
+// One CTA per (phase-2 chunk c, request b), flattened: NCW warps, warp w
+// publishes the mass of sub-range [c * ch2 + w * sub, +sub) (clipped).
+template <int DT>
+__global__ void __launch_bounds__(32 * NCW) sv_residual(const Params P) {
+  using E = Elem<DT>;
+  const int c = int(blockIdx.x % unsigned(P.nch2)), b = int(blockIdx.x / unsigned(P.nch2));
+  const int cw = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
+  Record r;
+  {
+    const int4* src = reinterpret_cast<const int4*>(P.rec + b);
+    int4* dst = reinterpret_cast<int4*>(&r);
+    dst[0] = __ldg(src); dst[1] = __ldg(src + 1); dst[2] = __ldg(src + 2);
+  }
+  if (r.mode != MODE_REJECT && r.mode != MODE_BONUS) return;
+  const int rowk = (r.mode == MODE_BONUS) ? P.gamma : r.k;
+  const unsigned char* trow = P.Lt + (size_t(b) * P.R + rowk) * size_t(P.V) * E::ES;
+  const unsigned char* drow =
+      r.mode == MODE_REJECT ? P.Ld + (size_t(b) * P.gamma + r.k) * size_t(P.V) * E::ES : nullptr;
+  const int lo = c * P.ch2 + cw * P.sub;
+  const int hi = min(lo + P.sub, min(P.V, (c + 1) * P.ch2));
+  float mh = 0.f, ml = 0.f;
+  if (lo < hi) span_mass<DT>(r, trow, drow, lo, hi, mh, ml);
+  if (lane == 0) P.mass[(size_t(b) * P.nch2 + c) * NCW + cw] = Mass{mh, ml};
+}
+
+// ------------------------------------------------------------ draw
+
+// Token k of request b (one warp): Z = the sum of the sub-range masses, the
+// sub-range where the running mass crosses u * Z, scanned in index order.
+template <int DT>
+__device__ void draw_one(const Params& P, int b) {
+  using E = Elem<DT>;
+  const int lane = threadIdx.x & 31;
+  Record r;
+  {
+    const int4* src = reinterpret_cast<const int4*>(P.rec + b);
+    int4* dst = reinterpret_cast<int4*>(&r);
+    dst[0] = __ldg(src); dst[1] = __ldg(src + 1); dst[2] = __ldg(src + 2);
+  }
   if (r.mode == MODE_INVALID) return;
   const int R = P.R, V = P.V;
   const int nq = P.nch2 * NCW;
-  ZPart* zp = P.z2 + size_t(b) * P.nch2;
-  auto zword = [&](int q, unsigned long long& lo, unsigned long long& hi) {
-    ld_pair(&zp[q / NCW].w[2 * (q % NCW)], lo, hi);
-  };
-  auto zval = [&](int q) {
-    unsigned long long lo, hi;
-    zword(q, lo, hi);
-    return __hiloint2double(int(hi & 0xffffffffull), int(lo & 0xffffffffull));
-  };
-  const bool ready = warp_poll(P, C, [&]() {
-    bool ok = true;
-    for (int q = lane; q < nq; q += 32) {
-      unsigned long long lo, hi;
-      zword(q, lo, hi);
-      ok = ok && is_mine(lo, epoch) && is_mine(hi, epoch);
-    }
-    return ok;
-  });
-  if (!ready) return;
+  const Mass* ms = P.mass + size_t(b) * P.nch2 * NCW;
   const float u = __ldg(P.u_res + size_t(b) * R + r.k);
   const int rowk = (r.mode == MODE_BONUS) ? P.gamma : r.k;
   const unsigned char* trow = P.Lt + (size_t(b) * R + rowk) * size_t(V) * E::ES;
-  const bool two = (r.mode == MODE_REJECT);
+  bool two = (r.mode == MODE_REJECT);
   const unsigned char* drow =
       two ? P.Ld + (size_t(b) * P.gamma + r.k) * size_t(V) * E::ES : nullptr;
-
-  // Z over all sub-ranges, in (chunk, sub-range) order, 32 at a time
-  double Z = 0.0;
-  for (int q0 = 0; q0 < nq; q0 += 32) {
-    const int q = q0 + lane;
-    const double z = q < nq ? zval(q) : 0.0;
-    Z += __shfl_sync(0xffffffffu, warp_incl_scan_d(z, lane), 31);
-  }
+  auto sub_lo = [&](int q) { return (q / NCW) * P.ch2 + (q % NCW) * P.sub; };
+  auto sub_hi = [&](int q) { return min(sub_lo(q) + P.sub, min(V, (q / NCW + 1) * P.ch2)); };
   bool degenerate = false;
+  // sub-range mass: published by the residual kernel, or (degenerate case)
+  // recomputed here for target row k
+  auto zq = [&](int q, float& h, float& l) {
+    if (!degenerate) {
+      const Mass m = ms[q];
+      h = m.hi;
+      l = m.lo;
+    } else {
+      const int lo = sub_lo(q), hi = sub_hi(q);
+      h = l = 0.f;
+      if (lo < hi) span_mass<DT>(r, trow, nullptr, lo, hi, h, l);
+    }
+  };
+  // Z over all sub-ranges, 32 at a time
+  auto total = [&]() {
+    float zh = 0.f, zl = 0.f;
+    for (int q0 = 0; q0 < nq; q0 += 32) {
+      float h = 0.f, l = 0.f;
+      if (q0 + lane < nq) {
+        if (!degenerate) zq(q0 + lane, h, l);
+      }
+      if (degenerate)  // one sub-range at a time, by the whole warp
+        for (int j = 0; j < 32 && q0 + j < nq; ++j) {
+          float hj, lj;
+          zq(q0 + j, hj, lj);
+          if (lane == j) { h = hj; l = lj; }
+        }
+      warp_sum_ff(h, l);
+      ff_add2(zh, zl, h, l);
+    }
+    return ff_val(zh, zl);
+  };
+  double Z = total();
   if (!(Z > 0.0)) {
     // the residual vanished in fp32: sample target row k instead (reading of
-    // the Z = 0 case); recompute every sub-range mass for that distribution
+    // the Z = 0 case)
     degenerate = true;
+    two = false;
     r.mode = MODE_TARGET;
-    Z = 0.0;
-    for (int q = 0; q < nq; ++q) {
-      const int lo = (q / NCW) * P.ch2 + (q % NCW) * P.sub;
-      const int hi = min(lo + P.sub, min(V, (q / NCW + 1) * P.ch2));
-      float acc = 0.f;
-      for (int e = lo + lane; e < hi; e += 32) acc += weight(r, E::load(trow, e), 0.f);
-      const double zq = warp_sum_d(double(acc));
-      if (lane == 0) {
-        unsigned long long wlo = tagged(epoch, unsigned(__double2loint(zq)));
-        unsigned long long whi = tagged(epoch, unsigned(__double2hiint(zq)));
-        st_pair(&zp[q / NCW].w[2 * (q % NCW)], wlo, whi);
-      }
-      Z += zq;
-    }
-    __threadfence();
-    __syncwarp();
+    Z = total();
   }
   const double tau = double(u) * Z;
-  // the (chunk, sub-range) where the running mass crosses tau
+  // the sub-range where the running mass crosses tau
   double base = 0.0, before = 0.0;
   int qstar = -1, qlast = 0;
+  double before_last = 0.0;
   for (int q0 = 0; q0 < nq && qstar < 0; q0 += 32) {
-    const int q = q0 + lane;
-    const double z = (q < nq) ? zval(q) : 0.0;
-    const double incl = warp_incl_scan_d(z, lane);
-    const unsigned pos = __ballot_sync(0xffffffffu, q < nq && z > 0.0);
-    if (pos) qlast = q0 + 31 - __clz(pos);
-    const unsigned hit = __ballot_sync(0xffffffffu, q < nq && z > 0.0 && base + incl > tau);
+    float h = 0.f, l = 0.f;
+    if (!degenerate) {
+      if (q0 + lane < nq) zq(q0 + lane, h, l);
+    } else {
+      for (int j = 0; j < 32 && q0 + j < nq; ++j) {
+        float hj, lj;
+        zq(q0 + j, hj, lj);
+        if (lane == j) { h = hj; l = lj; }
+      }
+    }
+    const double z = ff_val(h, l);
+    float sh = h, sl = l;
+    warp_scan_ff(sh, sl, lane);
+    const double incl = ff_val(sh, sl);
+    const unsigned pos = __ballot_sync(0xffffffffu, q0 + lane < nq && z > 0.0);
+    if (pos) {
+      const int l_last = 31 - __clz(pos);
+      qlast = q0 + l_last;
+      before_last = base + __shfl_sync(0xffffffffu, incl - z, l_last);
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, q0 + lane < nq && z > 0.0 && base + incl > tau);
     if (hit) {
-      const int l = __ffs(hit) - 1;
-      qstar = q0 + l;
-      before = base + __shfl_sync(0xffffffffu, incl - z, l);
+      const int l0 = __ffs(hit) - 1;
+      qstar = q0 + l0;
+      before = base + __shfl_sync(0xffffffffu, incl - z, l0);
     }
     base += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (qstar < 0) {  // rounding: take the last sub-range with mass
     qstar = qlast;
-    before = 0.0;
-    for (int q0 = 0; q0 < qstar; q0 += 32) {
-      const int q = q0 + lane;
-      const double z = (q < qstar) ? zval(q) : 0.0;
-      before += __shfl_sync(0xffffffffu, warp_incl_scan_d(z, lane), 31);
-    }
+    before = before_last;
   }
-  // scan the sub-range in index order
-  const int lo = (qstar / NCW) * P.ch2 + (qstar % NCW) * P.sub;
-  const int hi = min(lo + P.sub, min(V, (qstar / NCW + 1) * P.ch2));
+  // scan the sub-range in index order, 32 lanes x runs of consecutive weights
+  const int lo = sub_lo(qstar), hi = sub_hi(qstar);
   const double tau2 = tau - before;
   double run = 0.0;
   int tok = -1, last_pos = -1;
-  // One round: lane l holds `cnt` consecutive weights w[] starting at element
-  // e0 (the lanes' runs are consecutive); finds the crossing, if any.
   auto round = [&](const float* w, int cnt, int e0) {
-    float tot = 0.f;
+    float th = 0.f, tl = 0.f;
     for (int q = 0; q < cnt; ++q) {
-      tot += w[q];
+      ff_add(th, tl, w[q]);
       if (w[q] > 0.f) last_pos = e0 + q;
     }
-    const double incl = warp_incl_scan_d(double(tot), lane);
-    const unsigned hit = __ballot_sync(0xffffffffu, tot > 0.f && run + incl > tau2);
+    const double tot = ff_val(th, tl);
+    warp_scan_ff(th, tl, lane);
+    const double incl = ff_val(th, tl);
+    const unsigned hit = __ballot_sync(0xffffffffu, tot > 0.0 && run + incl > tau2);
     if (hit) {
-      const int l = __ffs(hit) - 1;
-      if (lane == l) {
-        double acc = run + incl - double(tot);
+      const int l0 = __ffs(hit) - 1;
+      if (lane == l0) {
+        double acc = run + incl - tot;
         int v = -1, lp = -1;
         for (int q = 0; q < cnt; ++q) {
           acc += double(w[q]);
@@ -1180,7 +1219,7 @@ __device__ void task_t3(const Params& P, SmemCtl& C, int b) {
         }
         tok = (v >= 0) ? v : lp;
       }
-      tok = __shfl_sync(0xffffffffu, tok, l);
+      tok = __shfl_sync(0xffffffffu, tok, l0);
     }
     run += __shfl_sync(0xffffffffu, incl, 31);
   };
@@ -1190,8 +1229,8 @@ __device__ void task_t3(const Params& P, SmemCtl& C, int b) {
                       (!two || (reinterpret_cast<uintptr_t>(dsub) & 15u) == 0);
   int done_e = lo;  // elements before done_e have been scanned
   if (vec_ok) {
-    // whole 16-byte vectors: loaded UMAX per lane at a time (one round trip),
-    // then scanned in rounds of 32 consecutive vectors
+    // whole 16-byte vectors: UMAX per lane loaded at once, then scanned in
+    // rounds of 32 consecutive vectors
     constexpr int UMAX = 5;
     const int nv = (hi - lo) / E::VEC;
     const uint4* tv = reinterpret_cast<const uint4*>(tsub);
@@ -1199,18 +1238,18 @@ __device__ void task_t3(const Params& P, SmemCtl& C, int b) {
     for (int v0 = 0; v0 < nv && tok < 0; v0 += 32 * UMAX) {
       uint4 vt[UMAX], vd[UMAX];
 #pragma unroll
-      for (int u = 0; u < UMAX; ++u) {
-        const int j = v0 + 32 * u + lane;
-        vt[u] = j < nv ? __ldg(tv + j) : make_uint4(0u, 0u, 0u, 0u);
-        vd[u] = (two && j < nv) ? __ldg(dvp + j) : vt[u];
+      for (int uu = 0; uu < UMAX; ++uu) {
+        const int j = v0 + 32 * uu + lane;
+        vt[uu] = j < nv ? __ldg(tv + j) : make_uint4(0u, 0u, 0u, 0u);
+        vd[uu] = (two && j < nv) ? __ldg(dvp + j) : vt[uu];
       }
 #pragma unroll
-      for (int u = 0; u < UMAX; ++u) {
-        if (tok >= 0 || v0 + 32 * u >= nv) break;
-        const int j = v0 + 32 * u + lane;
+      for (int uu = 0; uu < UMAX; ++uu) {
+        if (tok >= 0 || v0 + 32 * uu >= nv) break;
+        const int j = v0 + 32 * uu + lane;
         float ft[E::VEC], fd[E::VEC], w[E::VEC];
-        E::unpack(vt[u], ft);
-        E::unpack(vd[u], fd);
+        E::unpack(vt[uu], ft);
+        E::unpack(vd[uu], fd);
 #pragma unroll
         for (int q = 0; q < E::VEC; ++q) w[q] = j < nv ? weight(r, ft[q], two ? fd[q] : 0.f) : 0.f;
         round(w, E::VEC, lo + j * E::VEC);
@@ -1242,386 +1281,18 @@ __device__ void task_t3(const Params& P, SmemCtl& C, int b) {
   }
 }
 
-// ------------------------------------------------------------ producer
-
-// The global task order is a sequence of blocks j = 0, 1, ...: block j holds
-// P1 of request j, then D of request j - L, then P2 of request j - 2L, then
-// T3 of request j - 3L (each where that request exists; greedy has P1 and D
-// only).  tasks_before(j) counts the tasks of blocks 0..j-1.
-__device__ void decode(const Params& P, long long t, int& kind, int& b, int& sub) {
-  const long long B = P.B, L = P.lag;
-  int r = 0;
-  while (r + 1 < P.nreg && t >= P.rc[r + 1]) ++r;
-  const unsigned off = unsigned(t - P.rc[r]);
-  const unsigned sz = unsigned(P.rsz[r]);
-  const long long j = P.rj[r] + off / sz;
-  long long rem = off % sz;
-  sub = 0;
-  if (j < B) {
-    if (rem < P.n1) { kind = K_P1; b = int(j); sub = int(rem); return; }
-    rem -= P.n1;
-  }
-  if (j >= L && j < B + L) {
-    if (rem < 1) { kind = K_D; b = int(j - L); return; }
-    rem -= 1;
-  }
-  if (P.draw && j >= 2 * L && j < B + 2 * L) {
-    if (rem < P.n2) { kind = K_P2; b = int(j - 2 * L); sub = int(rem); return; }
-    rem -= P.n2;
-  }
-  kind = K_T3;
-  b = int(j - 3 * L);
-}
-
-// Bulk-copy the aligned bodies of a target (and draft) row chunk into slot s.
 template <int DT>
-__device__ void issue(SmemCtl& C, int s, unsigned char* slot, Desc& d, const unsigned char* tseg,
-                      const unsigned char* dseg) {
-  using E = Elem<DT>;
-  auto split = [&](const unsigned char* p, int& head, int& nb) {
-    int h = int(((16u - unsigned(reinterpret_cast<uintptr_t>(p) & 15u)) & 15u) / E::ES);
-    head = h < d.n ? h : d.n;
-    nb = ((d.n - head) / E::VEC) * E::VEC;
-  };
-  split(tseg, d.head_t, d.nb_t);
-  d.head_d = d.nb_d = 0;
-  if (dseg) split(dseg, d.head_d, d.nb_d);
-  const unsigned bt = unsigned(d.nb_t) * E::ES, bd = unsigned(d.nb_d) * E::ES;
-  if (bt + bd == 0u) {
-    mbar_arrive(&C.full[s]);
-    return;
-  }
-  mbar_arrive_tx(&C.full[s], bt + bd);
-  if (bt) bulk_g2s(slot, tseg + size_t(d.head_t) * E::ES, bt, &C.full[s]);
-  if (bd) bulk_g2s(slot + HALF, dseg + size_t(d.head_d) * E::ES, bd, &C.full[s]);
-}
-
-// Wait (bounded) for request b's decision record of this launch.
-__device__ bool wait_flag(const Params& P, SmemCtl& C, int b, unsigned epoch) {
-  const unsigned* flag = &P.req[b].flag;
-  if (ld_acquire(flag) == epoch) return true;
-  const unsigned long long t0 = globaltimer();
-  unsigned ns = 64;
-  for (;;) {
-    if (ld_acquire(flag) == epoch) return true;
-    if (*reinterpret_cast<volatile int*>(&P.ctrl->abort) ||
-        *reinterpret_cast<volatile int*>(&C.abort))
-      return false;
-    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-      give_up(P, C);
-      return false;
-    }
-    __nanosleep(ns);
-    ns = ns < 2048 ? ns * 2 : ns;
-  }
-}
-
-// Claims are kept two deep so the claim latency overlaps the copies; every
-// CTA therefore ends holding exactly two claims at or beyond `total`.
-template <int DT, bool GREEDY>
-__device__ void producer(const Params& P, SmemCtl& C, unsigned char* slots) {
-  using E = Elem<DT>;
-  const unsigned epoch = C.epoch;
-  unsigned long long q0 = atomicAdd(&P.ctrl->task, 1ull);
-  unsigned long long q1 = atomicAdd(&P.ctrl->task, 1ull);
-  for (long long seq = 0;; ++seq) {
-    const int s = int(seq % NSLOT);
-    const unsigned use = unsigned(seq / NSLOT);
-    Desc& d = C.desc[s];
-    unsigned char* slot = slots + size_t(s) * SLOT;
-    const long long t = (long long)q0;
-    q0 = q1;
-    if (t >= P.total || *reinterpret_cast<volatile int*>(&C.abort)) {
-      if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, C)) return;
-      d.kind = K_END;
-      mbar_arrive(&C.full[s]);
-      return;
-    }
-    q1 = atomicAdd(&P.ctrl->task, 1ull);
-    int kind, b, sub;
-    decode(P, t, kind, b, sub);
-    const float kf = GREEDY ? 0.f : (b < KF_CAP ? C.kf_tab[b] : LOG2E_F / __ldg(P.temp + b));
-    if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, C)) return;
-    d.b = b;
-    d.kind = kind;
-    d.kf = kf;
-    if (kind == K_P1) {
-      const int i = sub / P.nch1, c = sub - i * P.nch1;
-      d.i = i; d.c = c;
-      d.e0 = c * P.ch1;
-      d.n = min(P.ch1, P.V - d.e0);
-      const unsigned char* tseg =
-          P.Lt + ((size_t(b) * P.R + i) * size_t(P.V) + d.e0) * E::ES;
-      // greedy verification reads target rows only (it has no draft logits)
-      const unsigned char* dseg =
-          (!GREEDY && i < P.gamma && P.Ld)
-              ? P.Ld + ((size_t(b) * P.gamma + i) * size_t(P.V) + d.e0) * E::ES
-              : nullptr;
-      issue<DT>(C, s, slot, d, tseg, dseg);
-    } else if (kind == K_P2) {
-      d.c = sub;
-      Record r;
-      const bool ok = wait_flag(P, C, b, epoch);
-      if (ok) r = load_record(&P.rec[b]);
-      else r.mode = MODE_INVALID;
-      d.rec = r;
-      if (r.mode == MODE_INVALID) {
-        d.kind = K_SKIP;
-        mbar_arrive(&C.full[s]);
-        continue;
-      }
-      d.i = (r.mode == MODE_BONUS) ? P.gamma : r.k;
-      d.e0 = sub * P.ch2;
-      d.n = min(P.ch2, P.V - d.e0);
-      const unsigned char* tseg =
-          P.Lt + ((size_t(b) * P.R + d.i) * size_t(P.V) + d.e0) * E::ES;
-      const unsigned char* dseg =
-          r.mode == MODE_REJECT
-              ? P.Ld + ((size_t(b) * P.gamma + r.k) * size_t(P.V) + d.e0) * E::ES
-              : nullptr;
-      issue<DT>(C, s, slot, d, tseg, dseg);
-    } else {  // D and T3 carry no data
-      mbar_arrive(&C.full[s]);
-    }
-  }
-}
-
-// --------------------------------------------------- consumers and books
-
-// Staging entry e for a consumer warp: wait until the booking warp freed its
-// previous use.
-__device__ __forceinline__ bool stage_wait(const Params& P, SmemCtl& C, int e, unsigned use) {
-  return use == 0 || mbar_wait(&C.freed[e], (use - 1) & 1u, P, C);
-}
-
-// Consumers: every warp reduces its share of each slot and publishes its own
-// result (P1: the warp's (max, sum) pairs; P2: its sub-range mass) as
-// epoch-tagged words; only D, T3 and the end marker go on to the booking
-// warp through the staging ring (counted by dseq).
-template <int DT, bool GREEDY>
-__device__ void consumer(const Params& P, SmemCtl& C, const unsigned char* slots) {
-  using E = Elem<DT>;
-  const int cw = int(threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
-  const unsigned epoch = C.epoch;
-  long long dseq = 0;
-  for (long long seq = 0;; ++seq) {
-    const int s = int(seq % NSLOT);
-    const unsigned use = unsigned(seq / NSLOT);
-    if (!mbar_wait(&C.full[s], use & 1u, P, C)) return;
-    const Desc d = C.desc[s];
-    const unsigned char* slot = slots + size_t(s) * SLOT;
-    // each warp hands the slot back as soon as it holds its share elsewhere
-    bool released = false;
-    auto release = [&]() {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&C.empty[s]);
-      released = true;
-    };
-    if (d.kind == K_P1) {
-      const unsigned char* tseg =
-          P.Lt + ((size_t(d.b) * P.R + d.i) * size_t(P.V) + d.e0) * E::ES;
-      float4 out;
-      if (GREEDY) {
-        float best;
-        int bi, nan;
-        warp_argmax<DT>(slot, d.nb_t, tseg, d.head_t, d.n, d.e0, cw, lane, best, bi, nan, release);
-        out = make_float4(best, __int_as_float(bi), __int_as_float(nan), 0.f);
-      } else {
-        const bool has_d = d.i < P.gamma;
-        const unsigned char* dseg =
-            has_d ? P.Ld + ((size_t(d.b) * P.gamma + d.i) * size_t(P.V) + d.e0) * E::ES
-                  : nullptr;
-        warp_ms2<DT>(slot, slot + HALF, d, tseg, dseg, has_d, d.kf, cw, lane, out, release);
-      }
-      // every warp publishes its own partial; the D task combines them
-      if (lane == 0) {
-        Partial* dst = P.part + ((size_t(d.b) * P.R + d.i) * P.nch1 + d.c) * NCW + cw;
-        st_pair(&dst->w[0], tagged(epoch, __float_as_uint(out.x)), tagged(epoch, __float_as_uint(out.y)));
-        st_pair(&dst->w[2], tagged(epoch, __float_as_uint(out.z)), tagged(epoch, __float_as_uint(out.w)));
-      }
-    } else if (!GREEDY && (d.kind == K_P2 || d.kind == K_SKIP)) {
-      const double z = d.kind == K_P2 ? warp_p2_mass<DT>(P, d, slot, cw, lane, release) : 0.0;
-      if (lane == 0) {
-        ZPart* zp = P.z2 + size_t(d.b) * P.nch2 + d.c;
-        st_pair(&zp->w[2 * cw], tagged(epoch, unsigned(__double2loint(z))),
-                tagged(epoch, unsigned(__double2hiint(z))));
-      }
-    }
-    if (!released) release();
-    if (d.kind == K_D || d.kind == K_T3 || d.kind == K_END) {
-      const int e = int(dseq % NSTAGE);
-      const unsigned euse = unsigned(dseq / NSTAGE);
-      ++dseq;
-      if (!stage_wait(P, C, e, euse)) return;
-      if (d.kind == K_D)
-        for (int i = cw; i < P.R; i += NCW) {
-          RowStat r;
-          if (GREEDY) row_decide_greedy<DT>(P, C, d.b, i, r);
-          else row_decide_sample<DT>(P, C, d.b, i, d.kf, r);
-          if (lane == 0) C.rows[e][i] = r;
-        }
-      if (lane == 0) {
-        if (cw == 0) C.sdesc[e] = d;
-        mbar_arrive(&C.staged[e]);
-      }
-      if (d.kind == K_END) return;
-    }
-  }
-}
-
-__device__ __forceinline__ bool mbar_test(unsigned long long* bar, unsigned parity) {
-  unsigned ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Are request b's decision and every phase-2 sub-range mass published?
-__device__ bool t3_ready(const Params& P, SmemCtl& C, int b) {
-  const int lane = threadIdx.x & 31;
-  const unsigned epoch = C.epoch;
-  int ok = 1;
-  if (lane == 0) ok = ld_acquire(&P.req[b].flag) == epoch;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (!ok) return false;
-  const ZPart* zp = P.z2 + size_t(b) * P.nch2;
-  bool all = true;
-  for (int q = lane; q < P.nch2 * NCW; q += 32) {
-    unsigned long long lo, hi;
-    ld_pair(&zp[q / NCW].w[2 * (q % NCW)], lo, hi);
-    all = all && is_mine(lo, epoch) && is_mine(hi, epoch);
-  }
-  return __all_sync(0xffffffffu, all);
-}
-
-constexpr int DEFCAP = 16;  // T3 tasks the booking warp may hold back
-
-// The booking warp: request decisions of D tasks, and T3 draws, which it
-// holds back (up to DEFCAP) while their inputs are not yet published and
-// re-probes when idle, so that a slow request never delays another's decision.
-template <int DT, bool GREEDY>
-__device__ void booking(const Params& P, SmemCtl& C) {
-  const int lane = threadIdx.x & 31;
-  int* defer = C.defer;
-  int ndef = 0;
-  unsigned long long last_probe = 0, last_progress = globaltimer();
-  for (long long dseq = 0;;) {
-    const int e = int(dseq % NSTAGE);
-    const unsigned euse = unsigned(dseq / NSTAGE);
-    if (mbar_test(&C.staged[e], euse & 1u)) {
-      const Desc d = C.sdesc[e];
-      ++dseq;
-      last_progress = globaltimer();
-      if (d.kind == K_END) break;
-      if (d.kind == K_D) {  // frees the entry itself once the rows are read
-        if (GREEDY) request_decide_greedy(P, C, e, d.b);
-        else request_decide_sample<DT>(P, C, e, d.b);
-        continue;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&C.freed[e]);
-      if (GREEDY) continue;
-      if (ndef == 0 && t3_ready(P, C, d.b)) {
-        task_t3<DT>(P, C, d.b);
-      } else {
-        if (ndef == DEFCAP) {  // full: finish the oldest (bounded wait)
-          task_t3<DT>(P, C, defer[0]);
-          if (lane == 0)
-            for (int k = 1; k < ndef; ++k) defer[k - 1] = defer[k];
-          __syncwarp();
-          --ndef;
-        }
-        if (lane == 0) defer[ndef] = d.b;
-        __syncwarp();
-        ++ndef;
-      }
-      continue;
-    }
-    const unsigned long long now = globaltimer();
-    const bool stop = *reinterpret_cast<volatile int*>(&P.ctrl->abort) ||
-                      *reinterpret_cast<volatile int*>(&C.abort);
-    if (__any_sync(0xffffffffu, stop)) break;
-    if (now - last_progress > WAIT_LIMIT_NS) {
-      if (lane == 0) give_up(P, C);
-      __syncwarp();
-      break;
-    }
-    if (ndef > 0) {
-      if (now - last_probe > 1500) {
-        last_probe = now;
-        if (t3_ready(P, C, defer[0])) {
-          task_t3<DT>(P, C, defer[0]);
-          if (lane == 0)
-            for (int k = 1; k < ndef; ++k) defer[k - 1] = defer[k];
-          __syncwarp();
-          --ndef;
-          last_progress = globaltimer();
-        }
-      } else {
-        __nanosleep(200);
-      }
-    } else if (!mbar_wait(&C.staged[e], euse & 1u, P, C)) {
-      break;
-    }
-  }
-  for (int k = 0; k < ndef; ++k) task_t3<DT>(P, C, defer[k]);  // the rest (bounded waits)
-}
-
-// --------------------------------------------------------- the kernel
-
-template <int DT, bool GREEDY>
-__global__ void __launch_bounds__(NTHR, 1) sv_kernel(const Params P) {
-  extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char* slots = smem;
-  SmemCtl& C = *reinterpret_cast<SmemCtl*>(smem + size_t(NSLOT) * SLOT);
-  if (threadIdx.x == 0) {
-    C.epoch = __ldcg(&P.ctrl->epoch_counter) + 1u;
-    C.abort = 0;
-    for (int s = 0; s < NSLOT; ++s) {
-      mbar_init(&C.full[s], 1);
-      mbar_init(&C.empty[s], NCW);
-    }
-    for (int e = 0; e < NSTAGE; ++e) {
-      mbar_init(&C.staged[e], NCW);
-      mbar_init(&C.freed[e], 1);
-    }
-  }
-  if (!GREEDY)
-    for (int b = threadIdx.x; b < min(P.B, KF_CAP); b += NTHR) C.kf_tab[b] = LOG2E_F / __ldg(P.temp + b);
-  __syncthreads();
-  const int warp = int(threadIdx.x >> 5);
-  if (warp == 0) {
-    if (threadIdx.x == 0) producer<DT, GREEDY>(P, C, slots);
-  } else if (warp <= NCW) {
-    consumer<DT, GREEDY>(P, C, slots);
-  } else {
-    booking<DT, GREEDY>(P, C);
-  }
-  __syncthreads();
-  // exit: the last CTA out checks and resets the control block
-  if (threadIdx.x == 0) {
-    const unsigned old = atomicAdd(&P.ctrl->exit_count, 1u);
-    if (old == gridDim.x - 1) {
-      __threadfence();
-      const unsigned long long tc = __ldcg(&P.ctrl->task);
-      if (tc != (unsigned long long)P.total + 2ull * gridDim.x) set_status(P, SV_ST_WORKSPACE);
-      P.ctrl->task = 0ull;
-      P.ctrl->exit_count = 0u;
-      P.ctrl->abort = 0;
-      const unsigned e = P.ctrl->epoch_counter;
-      P.ctrl->epoch_counter = (e + 1u) % 0xFFFFFFFFu;
-    }
-  }
+__global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
+  const int b = int(blockIdx.x) * DRAW_WARPS + int(threadIdx.x >> 5);
+  if (b < P.B) draw_one<DT>(P, b);
+  // the last kernel of a sampling call: the workspace is ready for the next one
+  if (blockIdx.x == 0 && threadIdx.x == 0) P.ctrl->state = 0ull;
 }
 
 // ---------------------------------------------------------------- host
 
 struct Tuning {
-  int chunk = 0, lag = 0;
+  int chunk = 0;
 };
 Tuning g_tune;
 
@@ -1634,7 +1305,7 @@ DevCache g_dev[64];
 
 template <int DT, bool G>
 bool prepare_kernel() {
-  return cudaFuncSetAttribute(sv_kernel<DT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(sv_reduce<DT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(SMEM_BYTES)) == cudaSuccess;
 }
 
@@ -1705,73 +1376,45 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
   P.B = B; P.gamma = gamma; P.V = V; P.R = R;
   P.ch1 = ch1; P.nch1 = nch1;
   P.np1 = nch1 * NCW;
+  P.tasks = (long long)B * R * nch1;
   P.ch2 = chmax;
   P.nch2 = (V + chmax - 1) / chmax;
-  // each consumer warp takes a contiguous sub-range of a phase-2 chunk, a
+  // each residual warp takes a contiguous sub-range of a phase-2 chunk, a
   // whole number of 16-byte vectors long (the last one may be shorter)
   P.sub = round_up((chmax + NCW - 1) / NCW, 8);
-  P.n1 = (long long)R * nch1;
-  P.n2 = greedy ? 0 : P.nch2;
-  P.draw = !greedy;
-  // per request: its P1 chunks, one D task, and (sampling) its P2 chunks and one T3 task
-  const long long per_req = P.n1 + 1 + (greedy ? 0 : P.n2 + 1);
-  P.total = (long long)B * per_req;
-  const long long grid = min((long long)sms, P.total);
-  // a request's D, P2 and T3 tasks each come `lag` requests after the stage
-  // before them: enough tasks in between to cover everything in flight
-  // (every CTA's slot ring and claims, 1.5 times)
-  if (g_tune.lag > 0) P.lag = g_tune.lag;
-  else P.lag = int(max(1LL, (3 * grid * (NSLOT + 2) / 2 + per_req - 1) / per_req));
-  {
-    // regions of constant block composition between the block indices where a
-    // stage starts or ends (see decode)
-    const long long Lg = P.lag, Bl = B;
-    auto block_size = [&](long long j) {
-      long long z = 0;
-      if (j < Bl) z += P.n1;
-      if (j >= Lg && j < Bl + Lg) z += 1;
-      if (P.draw && j >= 2 * Lg && j < Bl + 2 * Lg) z += P.n2;
-      if (P.draw && j >= 3 * Lg && j < Bl + 3 * Lg) z += 1;
-      return z;
-    };
-    const long long J = Bl + (P.draw ? 3 : 1) * Lg;
-    long long cuts[9] = {0, Lg, Bl, Bl + Lg, 2 * Lg, Bl + 2 * Lg, 3 * Lg, Bl + 3 * Lg, J};
-    std::sort(cuts, cuts + 9);
-    P.nreg = 0;
-    long long c = 0;
-    for (int q = 0; q < 9; ++q) {
-      const long long ja = cuts[q], jb = (q + 1 < 9) ? cuts[q + 1] : J;
-      if (ja >= J || jb <= ja) continue;
-      const long long sz = block_size(ja);
-      if (sz > 0) {
-        P.rj[P.nreg] = ja;
-        P.rc[P.nreg] = c;
-        P.rsz[P.nreg] = int(sz);
-        ++P.nreg;
-      }
-      c += sz * (min(jb, J) - ja);
-    }
-    P.rj[P.nreg] = J;
-    P.rc[P.nreg] = c;
-    if (c != P.total || P.total >= (1LL << 31)) return SV_ERR_INVALID_ARG;
-  }
   P.out_tokens = out_tokens; P.out_n = out_n; P.out_p = out_p; P.out_Z = out_Z;
   P.status = status;
   unsigned char* w = static_cast<unsigned char*>(ws);
   P.ctrl = reinterpret_cast<Ctrl*>(w + L.ctrl);
-  P.req = reinterpret_cast<ReqCtl*>(w + L.req);
-  P.rec = reinterpret_cast<Record*>(w + L.rec);
   P.part = reinterpret_cast<Partial*>(w + L.part);
-  P.z2 = reinterpret_cast<ZPart*>(w + L.z2);
+  P.rec = reinterpret_cast<Record*>(w + L.rec);
+  P.mass = reinterpret_cast<Mass*>(w + L.mass);
+  if ((long long)B * P.nch2 > 0x7fffffffLL) return SV_ERR_INVALID_ARG;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const dim3 g{unsigned(grid)}, blk{unsigned(NTHR)};
+  const unsigned grid = unsigned(min((long long)sms, P.tasks));
+  const unsigned ndraw = unsigned((B + DRAW_WARPS - 1) / DRAW_WARPS);
+  const unsigned nres = unsigned((long long)B * P.nch2);
   if (dtype == SV_F32) {
-    if (greedy) sv_kernel<SV_F32, true><<<g, blk, SMEM_BYTES, st>>>(P);
-    else sv_kernel<SV_F32, false><<<g, blk, SMEM_BYTES, st>>>(P);
+    if (greedy) {
+      sv_reduce<SV_F32, true><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      sv_decide<SV_F32, true><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, true);
+    } else {
+      sv_reduce<SV_F32, false><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      sv_decide<SV_F32, false><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, false);
+      sv_residual<SV_F32><<<nres, 32 * NCW, 0, st>>>(P);
+      sv_draw<SV_F32><<<ndraw, 32 * DRAW_WARPS, 0, st>>>(P);
+    }
   } else {
-    if (greedy) sv_kernel<SV_BF16, true><<<g, blk, SMEM_BYTES, st>>>(P);
-    else sv_kernel<SV_BF16, false><<<g, blk, SMEM_BYTES, st>>>(P);
+    if (greedy) {
+      sv_reduce<SV_BF16, true><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      sv_decide<SV_BF16, true><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, true);
+    } else {
+      sv_reduce<SV_BF16, false><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      sv_decide<SV_BF16, false><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, false);
+      sv_residual<SV_BF16><<<nres, 32 * NCW, 0, st>>>(P);
+      sv_draw<SV_BF16><<<ndraw, 32 * DRAW_WARPS, 0, st>>>(P);
+    }
   }
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
@@ -1869,21 +1512,18 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
   int rc = noalloc_scratch(&scratch);
   if (rc != SV_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the task counter and the exit counter must start at zero; the launch
-  // epoch after them must survive from call to call
-  if (cudaMemsetAsync(scratch, 0, offsetof(Ctrl, epoch_counter), st) != cudaSuccess ||
-      cudaMemsetAsync(static_cast<unsigned char*>(scratch) + offsetof(Ctrl, abort), 0,
-                      sizeof(int), st) != cudaSuccess)
-    return SV_ERR_CUDA;
+  // the control block starts every call in its ready state (calls that may
+  // overlap are the caller's to serialise)
+  if (cudaMemsetAsync(scratch, 0, sizeof(Ctrl), st) != cudaSuccess) return SV_ERR_CUDA;
   return launch(false, target_logits, draft_logits, draft_tokens, u_accept, u_resample,
                 temperature, B, gamma, V, dtype, out_tokens, out_num_accepted, nullptr, nullptr,
                 scratch, SV_NOALLOC_MAX_WORKSPACE, dev_status, stream);
 }
 
 int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests) {
-  (void)ctas_per_sm;  // the kernel always runs one CTA per SM
+  (void)ctas_per_sm;   // the reduce kernel always runs one CTA per SM
+  (void)lag_requests;  // the stages run as separate kernels: there is no lag
   g_tune.chunk = chunk_elems > 0 ? chunk_elems : 0;
-  g_tune.lag = lag_requests > 0 ? lag_requests : 0;
   return SV_OK;
 }
 
@@ -1898,6 +1538,6 @@ const char* sv_error_string(int code) {
   }
 }
 
-int sv_version(void) { return 200; }
+int sv_version(void) { return 300; }
 
 }  // extern "C"

@@ -225,7 +225,7 @@ def test_poisoned_task_counter_is_detected_and_repaired():
     d = to_dev(inp)
     ws = binding.make_workspace(inp.B, inp.gamma, inp.V, DEV)
     ref = oracle_sampling(inp)
-    ws[0:8].view(torch.int64).fill_(1 << 40)  # beyond every task: nothing runs, nothing waits
+    ws[0:8].view(torch.int64).fill_(1 << 40)  # the control block is not in its ready state
     bad = run_sampling(inp, d, ws)
     assert bad["status"] & binding.SV_ST_WORKSPACE
     compare_sampling(inp, run_sampling(inp, d, ws), ref)
