@@ -58,7 +58,7 @@ constexpr unsigned SUSPEND_HINT_NS = 1000000u;  // a waiting warp sleeps until t
 constexpr int SMS_CAP = 256;           // the chunk heuristic assumes at most this many SMs
 constexpr int MAXR = SV_MAX_GAMMA + 1;
 constexpr int DECIDE_WARPS = 8;        // decide: warps per request
-constexpr int DRAW_WARPS = 4;          // draw: requests per CTA
+constexpr int DRAW_WARPS = 8;          // draw: warps per request
 constexpr float LOG2E_F = 1.4426950408889634f;
 constexpr double LOG2E_D = 1.4426950408889634;
 constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;  // one second
@@ -274,6 +274,9 @@ struct Elem<SV_F32> {
   __device__ static float load(const unsigned char* base, long long idx) {
     return __ldg(reinterpret_cast<const float*>(base) + idx);
   }
+  __device__ static float lds(const unsigned char* base, int idx) {
+    return reinterpret_cast<const float*>(base)[idx];
+  }
   __device__ static void unpack(const uint4& v, float* f) {
     f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
     f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
@@ -306,6 +309,9 @@ struct Elem<SV_BF16> {
   __device__ static float load(const unsigned char* base, long long idx) {
     return __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short*>(base) + idx))
                            << 16);
+  }
+  __device__ static float lds(const unsigned char* base, int idx) {
+    return __uint_as_float(uint32_t(reinterpret_cast<const unsigned short*>(base)[idx]) << 16);
   }
   __device__ static void unpack(const uint4& v, float* f) {
     f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
@@ -420,8 +426,10 @@ struct alignas(16) Desc {
   int head_d, nb_d;           // draft likewise
   float kf;                   // sampling: log2(e) / T of the request
   int pad;
+  Record rec;                 // residual: the request's decision record (bulk-copied)
 };
-// Shared-memory control block of the reduce kernel (after the slots).
+static_assert(offsetof(Desc, rec) % 16 == 0 && sizeof(Record) % 16 == 0, "record copy");
+// Shared-memory control block of the streaming kernels (after the slots).
 struct SmemCtl {
   unsigned long long full[NSLOT], empty[NSLOT];
   Desc desc[NSLOT];
@@ -594,45 +602,55 @@ __device__ void warp_argmax(const unsigned char* sbody, int nb, const unsigned c
 
 // ---------------------------------------------- P2 / P3: residual weights
 
-// Weight of one element of the final draw (fp32, identical in P2 and P3).
-// Residual max(0, P_t - P_d) formed as P_t * (1 - 2^delta) with
-// delta = log2(P_d / P_t), so it keeps its relative precision where the two
-// rows nearly agree (no cancellation); the normaliser is applied as hi + lo.
-// 1 - 2^delta for delta <= 0, to fp32 relative precision: 1 - ex2(delta)
-// where that loses nothing (delta < -1/2), else -expm1(y), y = delta*ln2 in
-// [-0.347, 0], by its Taylor series to y^7 (truncation below 2e-8 relative).
+// Weight of one element of the final draw, up to the row's factor 1/S_t
+// (applied once to the masses): e = 2^((l_t - m_t) * kf), the unnormalised
+// P_t; after a rejection the residual max(0, P_t - P_d) = P_t * (1 - 2^delta)
+// with delta = log2(P_d / P_t) = (l_d - l_t) * kf + c0, which keeps its
+// relative precision where the rows nearly agree (no cancellation).  delta is
+// clamped to <= 0 (weight 0, also for NaN); 1 - 2^delta is 1 - ex2(delta)
+// where that loses nothing (delta < -1/2), else its Taylor series in delta,
+// sum_{n=1..7} -(ln 2)^n / n! * delta^n (truncation below 2e-8 relative).
+// weight() and vec_weights() perform the same fp32 operations per element.
+constexpr float OMC1 = -0.69314718055994531f, OMC2 = -0.24022650695910071f,
+                OMC3 = -0.055504108664821580f, OMC4 = -0.0096181291076284772f,
+                OMC5 = -0.0013333558146428443f, OMC6 = -1.5403530393381609e-4f,
+                OMC7 = -1.5252733804059841e-5f;
 __device__ __forceinline__ float one_minus_exp2(float delta) {
-  const float y = delta * 0.69314718055994531f;
-  float p = 1.f / 5040.f;
-  p = fmaf(p, y, 1.f / 720.f);
-  p = fmaf(p, y, 1.f / 120.f);
-  p = fmaf(p, y, 1.f / 24.f);
-  p = fmaf(p, y, 1.f / 6.f);
-  p = fmaf(p, y, 0.5f);
-  p = fmaf(p, y, 1.f);
-  const float series = -y * p;
-  return delta < -0.5f ? 1.f - ex2(delta) : series;
+  float p = OMC7;
+  p = fmaf(p, delta, OMC6);
+  p = fmaf(p, delta, OMC5);
+  p = fmaf(p, delta, OMC4);
+  p = fmaf(p, delta, OMC3);
+  p = fmaf(p, delta, OMC2);
+  p = fmaf(p, delta, OMC1);
+  const float series = p * delta;
+  const float alt = 1.f - ex2(delta);
+  return delta < -0.5f ? alt : series;
 }
 
 __device__ __forceinline__ float weight(const Record& r, float lt, float ld) {
   const float et = ex2((lt - r.mt) * r.kf);
-  const float pt = fmaf(et, r.ist_hi, et * r.ist_lo);
   if (r.mode == MODE_REJECT) {
-    const float delta = fmaf(ld - lt, r.kf, r.c0_hi) + r.c0_lo;  // log2(P_d / P_t)
-    return (et > 0.f && delta < 0.f) ? pt * one_minus_exp2(delta) : 0.f;
+    const float delta = fminf(fmaf(ld - lt, r.kf, r.c0_hi) + r.c0_lo, 0.f);  // log2(P_d / P_t)
+    return et * one_minus_exp2(delta);
   }
-  return pt;
+  return et;
 }
 
-// Residual (or bonus) weights of one 16-byte vector of target values `t`
-// and draft values `dv`, summed; packed fp32x2 arithmetic, the same formula
-// as weight() element by element.
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Weights of one 16-byte vector of target values `t` and draft values `dv`,
+// summed; the same operations as weight() on packed fp32 pairs.
 template <int DT>
 __device__ __forceinline__ float vec_weights(const Record& r, const uint4& t, const uint4& dv,
                                              bool two) {
   using E = Elem<DT>;
   const unsigned long long mm = pk2(r.mt, r.mt), kk = pk2(r.kf, r.kf);
-  const unsigned long long hh = pk2(r.ist_hi, r.ist_hi), ll = pk2(r.ist_lo, r.ist_lo);
   unsigned long long acc = pk2(0.f, 0.f);
 #pragma unroll
   for (int q = 0; q < E::PAIRS; ++q) {
@@ -640,24 +658,27 @@ __device__ __forceinline__ float vec_weights(const Record& r, const uint4& t, co
     float a, b;
     upk2(mul2(sub2(lt, mm), kk), a, b);
     const unsigned long long et = pk2(ex2(a), ex2(b));
-    unsigned long long pt;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(pt) : "l"(et), "l"(hh), "l"(mul2(et, ll)));
     if (two) {
-      // delta = log2(P_d / P_t) = (l_d - l_t) * kf + c0
-      unsigned long long dl;
       const unsigned long long ch = pk2(r.c0_hi, r.c0_hi), cl = pk2(r.c0_lo, r.c0_lo);
-      asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(dl) : "l"(sub2(E::pair(dv, q), lt)), "l"(kk),
-          "l"(ch));
-      dl = add2(dl, cl);
-      float d0, d1, e0, e1, p0, p1;
-      upk2(dl, d0, d1);
-      upk2(et, e0, e1);
-      upk2(pt, p0, p1);
-      const float w0 = (e0 > 0.f && d0 < 0.f) ? p0 * one_minus_exp2(d0) : 0.f;
-      const float w1 = (e1 > 0.f && d1 < 0.f) ? p1 * one_minus_exp2(d1) : 0.f;
-      acc = add2(acc, pk2(w0, w1));
+      float d0, d1;
+      upk2(add2(fma2(sub2(E::pair(dv, q), lt), kk, ch), cl), d0, d1);
+      d0 = fminf(d0, 0.f);
+      d1 = fminf(d1, 0.f);
+      const unsigned long long dd = pk2(d0, d1);
+      unsigned long long p = pk2(OMC7, OMC7);
+      p = fma2(p, dd, pk2(OMC6, OMC6));
+      p = fma2(p, dd, pk2(OMC5, OMC5));
+      p = fma2(p, dd, pk2(OMC4, OMC4));
+      p = fma2(p, dd, pk2(OMC3, OMC3));
+      p = fma2(p, dd, pk2(OMC2, OMC2));
+      p = fma2(p, dd, pk2(OMC1, OMC1));
+      float s0, s1;
+      upk2(mul2(p, dd), s0, s1);
+      const float f0 = d0 < -0.5f ? 1.f - ex2(d0) : s0;
+      const float f1 = d1 < -0.5f ? 1.f - ex2(d1) : s1;
+      acc = add2(acc, mul2(et, pk2(f0, f1)));
     } else {
-      acc = add2(acc, pt);
+      acc = add2(acc, et);
     }
   }
   float a, b;
@@ -1061,46 +1082,186 @@ __device__ void span_mass(const Record& r, const unsigned char* trow, const unsi
   warp_sum_ff(mh, ml);
 }
 
-// One CTA per (phase-2 chunk c, request b), flattened: NCW warps, warp w
-// publishes the mass of sub-range [c * ch2 + w * sub, +sub) (clipped).
+// Residual producer (one lane): this CTA's contiguous range of phase-2 chunks
+// (chunk t % nch2 of request t / nch2); chunks of invalid requests are
+// skipped.  Each slot gets the chunk of target row k (gamma for the bonus),
+// the draft row k chunk after a rejection, and the request's record.
 template <int DT>
-__global__ void __launch_bounds__(32 * NCW) sv_residual(const Params P) {
+__device__ void producer_res(const Params& P, SmemCtl& C, unsigned char* slots) {
   using E = Elem<DT>;
-  const int c = int(blockIdx.x % unsigned(P.nch2)), b = int(blockIdx.x / unsigned(P.nch2));
-  const int cw = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
-  Record r;
-  {
-    const int4* src = reinterpret_cast<const int4*>(P.rec + b);
-    int4* dst = reinterpret_cast<int4*>(&r);
-    dst[0] = __ldg(src); dst[1] = __ldg(src + 1); dst[2] = __ldg(src + 2);
+  const long long T = (long long)P.B * P.nch2, G = gridDim.x;
+  const long long t0 = T * blockIdx.x / G, t1 = T * (blockIdx.x + 1) / G;
+  int b = int(t0 / P.nch2), c = int(t0 - (long long)b * P.nch2);
+  int2 km = __ldg(reinterpret_cast<const int2*>(P.rec + b));  // (k, mode)
+  int2 km_next = b + 1 < P.B ? __ldg(reinterpret_cast<const int2*>(P.rec + b + 1)) : km;
+  long long seq = 0;
+  for (long long t = t0; t < t1; ++t) {
+    if (km.y == MODE_REJECT || km.y == MODE_BONUS) {
+      const int s = int(seq % NSLOT);
+      const unsigned use = unsigned(seq / NSLOT);
+      ++seq;
+      if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, &C.abort)) return;
+      if (C.abort) break;
+      Desc& d = C.desc[s];
+      const bool two = km.y == MODE_REJECT;
+      const int rowk = two ? km.x : P.gamma;
+      d.end = 0;
+      d.b = b; d.i = rowk; d.c = c;
+      d.e0 = c * P.ch2;
+      d.n = min(P.ch2, P.V - d.e0);
+      const unsigned char* tseg = P.Lt + ((size_t(b) * P.R + rowk) * size_t(P.V) + d.e0) * E::ES;
+      const unsigned char* dseg =
+          two ? P.Ld + ((size_t(b) * P.gamma + km.x) * size_t(P.V) + d.e0) * E::ES : nullptr;
+      split<DT>(tseg, d.n, d.head_t, d.nb_t);
+      d.head_d = d.nb_d = 0;
+      if (dseg) split<DT>(dseg, d.n, d.head_d, d.nb_d);
+      const unsigned bt = unsigned(d.nb_t) * E::ES, bd = unsigned(d.nb_d) * E::ES;
+      mbar_arrive_tx(&C.full[s], bt + bd + unsigned(sizeof(Record)));
+      if (bt) bulk_g2s(slots + size_t(s) * SLOT, tseg + size_t(d.head_t) * E::ES, bt, &C.full[s]);
+      if (bd)
+        bulk_g2s(slots + size_t(s) * SLOT + HALF, dseg + size_t(d.head_d) * E::ES, bd,
+                 &C.full[s]);
+      bulk_g2s(&d.rec, P.rec + b, unsigned(sizeof(Record)), &C.full[s]);
+    }
+    if (++c == P.nch2) {
+      c = 0;
+      ++b;
+      km = km_next;
+      if (b + 1 < P.B) km_next = __ldg(reinterpret_cast<const int2*>(P.rec + b + 1));
+    }
   }
-  if (r.mode != MODE_REJECT && r.mode != MODE_BONUS) return;
-  const int rowk = (r.mode == MODE_BONUS) ? P.gamma : r.k;
-  const unsigned char* trow = P.Lt + (size_t(b) * P.R + rowk) * size_t(P.V) * E::ES;
-  const unsigned char* drow =
-      r.mode == MODE_REJECT ? P.Ld + (size_t(b) * P.gamma + r.k) * size_t(P.V) * E::ES : nullptr;
-  const int lo = c * P.ch2 + cw * P.sub;
-  const int hi = min(lo + P.sub, min(P.V, (c + 1) * P.ch2));
-  float mh = 0.f, ml = 0.f;
-  if (lo < hi) span_mass<DT>(r, trow, drow, lo, hi, mh, ml);
-  if (lane == 0) P.mass[(size_t(b) * P.nch2 + c) * NCW + cw] = Mass{mh, ml};
+  const int s = int(seq % NSLOT);
+  const unsigned use = unsigned(seq / NSLOT);
+  if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, &C.abort)) return;
+  C.desc[s].end = 1;
+  mbar_arrive(&C.full[s]);
+}
+
+// Mass of this warp's contiguous sub-range [cw*sub, (cw+1)*sub) of a
+// phase-2 chunk held in a slot (target body at +0, draft body at +HALF),
+// returned as a float pair (hi, lo) valid in every lane.
+template <int DT, typename Release>
+__device__ float2 warp_slot_mass(const Params& P, const Desc& d, const Record& r,
+                                 const unsigned char* slot, int cw, int lane, Release release) {
+  using E = Elem<DT>;
+  const bool two = (r.mode == MODE_REJECT);
+  const int lo = cw * P.sub;
+  const int hi = min(lo + P.sub, d.n);
+  float acc = 0.f;
+  if (lo >= hi) {
+    release();
+  } else {
+    const unsigned char* trow = P.Lt + ((size_t(d.b) * P.R + d.i) * size_t(P.V) + d.e0) * E::ES;
+    const unsigned char* drow =
+        two ? P.Ld + ((size_t(d.b) * P.gamma + r.k) * size_t(P.V) + d.e0) * E::ES : nullptr;
+    if (d.head_t == 0 && (!two || d.head_d == 0)) {
+      // aligned: whole 16-byte vectors from shared memory, held in registers
+      constexpr int PV = (HALF / 16 + 32 * NCW - 1) / (32 * NCW);
+      const uint4* tv = reinterpret_cast<const uint4*>(slot);
+      const uint4* dv = reinterpret_cast<const uint4*>(slot + HALF);
+      const int j0 = lo / E::VEC, vhi = min(hi, d.nb_t) / E::VEC;
+      uint4 vt[PV], vd[PV];
+#pragma unroll
+      for (int u = 0; u < PV; ++u) {
+        const int j = j0 + lane + 32 * u;
+        vt[u] = j < vhi ? tv[j] : make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD,
+                                             E::NEG_INF_WORD);
+        vd[u] = (two && j < vhi) ? dv[j] : vt[u];
+      }
+      for (int j = j0 + lane + 32 * PV; j < vhi; j += 32)  // only if sub exceeds 32*PV vectors
+        acc += vec_weights<DT>(r, tv[j], two ? dv[j] : tv[j], two);
+      release();
+#pragma unroll
+      for (int u = 0; u < PV; ++u) acc += vec_weights<DT>(r, vt[u], vd[u], two);
+      for (int e = max(lo, d.nb_t) + lane; e < hi; e += 32)
+        acc += weight(r, E::load(trow, e), two ? E::load(drow, e) : 0.f);
+    } else {
+      // unaligned rows: element by element, from shared memory where held
+      for (int e = lo + lane; e < hi; e += 32) {
+        const int et = e - d.head_t, ed = e - d.head_d;
+        const float lt = (et >= 0 && et < d.nb_t) ? E::lds(slot, et) : E::load(trow, e);
+        float ld = 0.f;
+        if (two) ld = (ed >= 0 && ed < d.nb_d) ? E::lds(slot + HALF, ed) : E::load(drow, e);
+        acc += weight(r, lt, ld);
+      }
+      release();
+    }
+  }
+  float2 m = make_float2(acc, 0.f);
+  warp_sum_ff(m.x, m.y);
+  return m;
+}
+
+template <int DT>
+__device__ void consumer_res(const Params& P, SmemCtl& C, const unsigned char* slots) {
+  const int cw = int(threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
+  for (long long seq = 0;; ++seq) {
+    const int s = int(seq % NSLOT);
+    const unsigned use = unsigned(seq / NSLOT);
+    if (!mbar_wait(&C.full[s], use & 1u, P, &C.abort)) return;
+    const Desc d = C.desc[s];
+    if (d.end) return;
+    auto release = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&C.empty[s]);
+    };
+    const float2 m = warp_slot_mass<DT>(P, d, d.rec, slots + size_t(s) * SLOT, cw, lane, release);
+    if (lane == 0) P.mass[(size_t(d.b) * P.nch2 + d.c) * NCW + cw] = Mass{m.x, m.y};
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(NTHR, 1) sv_residual(const Params P) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* slots = smem;
+  SmemCtl& C = *reinterpret_cast<SmemCtl*>(smem + size_t(NSLOT) * SLOT);
+  if (threadIdx.x == 0) {
+    C.abort = 0;
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&C.full[s], 1);
+      mbar_init(&C.empty[s], NCW);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    if (threadIdx.x == 0) producer_res<DT>(P, C, slots);
+  } else {
+    consumer_res<DT>(P, C, slots);
+  }
 }
 
 // ------------------------------------------------------------ draw
 
-// Token k of request b (one warp): Z = the sum of the sub-range masses, the
-// sub-range where the running mass crosses u * Z, scanned in index order.
+// Token k of request b, one CTA of DRAW_WARPS warps:
+//   1. every warp takes a contiguous run of sub-ranges, loads their masses
+//      (published by the residual kernel) and sums them; a block prefix over
+//      the warps gives Z and the warp whose run crosses tau = u * Z;
+//   2. that warp finds the crossing sub-range within its run (lane prefix);
+//   3. the sub-range's elements are split over the warps, each warp sums its
+//      slice's weights; a block prefix finds the crossing slice, whose warp
+//      scans it in index order.
+// When the residual summed to 0 (degenerate), the masses of target row k are
+// recomputed in step 1 instead.  Running sums are float pairs, compared in fp64.
+constexpr int DRAW_RUN = 4;  // sub-ranges per lane in step 1 (run of 128 per warp)
+
 template <int DT>
-__device__ void draw_one(const Params& P, int b) {
+__global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
   using E = Elem<DT>;
-  const int lane = threadIdx.x & 31;
+  __shared__ float2 wsum[DRAW_WARPS];
+  __shared__ double sh_tau, sh_before;
+  __shared__ int sh_q, sh_wsel;
+  const int b = int(blockIdx.x), warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
   Record r;
   {
     const int4* src = reinterpret_cast<const int4*>(P.rec + b);
     int4* dst = reinterpret_cast<int4*>(&r);
     dst[0] = __ldg(src); dst[1] = __ldg(src + 1); dst[2] = __ldg(src + 2);
   }
-  if (r.mode == MODE_INVALID) return;
+  const bool last_cta = blockIdx.x == 0;
+  if (r.mode == MODE_INVALID) {
+    if (last_cta && threadIdx.x == 0) P.ctrl->state = 0ull;
+    return;
+  }
   const int R = P.R, V = P.V;
   const int nq = P.nch2 * NCW;
   const Mass* ms = P.mass + size_t(b) * P.nch2 * NCW;
@@ -1112,181 +1273,222 @@ __device__ void draw_one(const Params& P, int b) {
       two ? P.Ld + (size_t(b) * P.gamma + r.k) * size_t(V) * E::ES : nullptr;
   auto sub_lo = [&](int q) { return (q / NCW) * P.ch2 + (q % NCW) * P.sub; };
   auto sub_hi = [&](int q) { return min(sub_lo(q) + P.sub, min(V, (q / NCW + 1) * P.ch2)); };
-  bool degenerate = false;
-  // sub-range mass: published by the residual kernel, or (degenerate case)
-  // recomputed here for target row k
-  auto zq = [&](int q, float& h, float& l) {
-    if (!degenerate) {
-      const Mass m = ms[q];
-      h = m.hi;
-      l = m.lo;
-    } else {
-      const int lo = sub_lo(q), hi = sub_hi(q);
-      h = l = 0.f;
-      if (lo < hi) span_mass<DT>(r, trow, nullptr, lo, hi, h, l);
-    }
-  };
-  // Z over all sub-ranges, 32 at a time
-  auto total = [&]() {
-    float zh = 0.f, zl = 0.f;
-    for (int q0 = 0; q0 < nq; q0 += 32) {
-      float h = 0.f, l = 0.f;
-      if (q0 + lane < nq) {
-        if (!degenerate) zq(q0 + lane, h, l);
-      }
-      if (degenerate)  // one sub-range at a time, by the whole warp
-        for (int j = 0; j < 32 && q0 + j < nq; ++j) {
-          float hj, lj;
-          zq(q0 + j, hj, lj);
-          if (lane == j) { h = hj; l = lj; }
+  // block-wide exclusive prefix of the warps' pair sums in wsum: the warp
+  // where the running sum crosses tau (the last warp with mass if none), and
+  // the mass before it; written to sh_wsel / sh_before by thread 0
+  auto pick_warp = [&](double tau) {
+    if (threadIdx.x == 0) {
+      double base = 0.0;
+      int sel = -1, last = -1;
+      double before_last = 0.0, before = 0.0;
+      for (int w = 0; w < DRAW_WARPS; ++w) {
+        const double z = ff_val(wsum[w].x, wsum[w].y);
+        if (z > 0.0) {
+          last = w;
+          before_last = base;
+          if (sel < 0 && base + z > tau) { sel = w; before = base; }
         }
-      warp_sum_ff(h, l);
-      ff_add2(zh, zl, h, l);
+        base += z;
+      }
+      if (sel < 0) { sel = last < 0 ? 0 : last; before = before_last; }
+      sh_wsel = sel;
+      sh_before = before;
     }
-    return ff_val(zh, zl);
+    __syncthreads();
   };
-  double Z = total();
+
+  // 1. runs of sub-ranges: warp w takes [w * run, (w + 1) * run)
+  const int run = (nq + DRAW_WARPS - 1) / DRAW_WARPS;
+  const int qa = min(nq, warp * run), qb = min(nq, qa + run);
+  bool degenerate = false;
+  float mh[DRAW_RUN], ml[DRAW_RUN];  // this lane's masses q = qa + lane + 32 j
+  float th = 0.f, tl = 0.f;
+  auto load_masses = [&]() {
+    th = tl = 0.f;
+#pragma unroll
+    for (int j = 0; j < DRAW_RUN; ++j) {
+      const int q = qa + lane + 32 * j;
+      mh[j] = ml[j] = 0.f;
+      if (q < qb) {
+        const Mass m = ms[q];
+        mh[j] = m.hi;
+        ml[j] = m.lo;
+      }
+      ff_add2(th, tl, mh[j], ml[j]);
+    }
+    for (int q = qa + lane + 32 * DRAW_RUN; q < qb; q += 32) {  // runs beyond 32 * DRAW_RUN
+      const Mass m = ms[q];
+      ff_add2(th, tl, m.hi, m.lo);
+    }
+  };
+  auto target_masses = [&]() {  // degenerate case: masses of target row k, recomputed
+    th = tl = 0.f;
+    for (int j = 0; j < DRAW_RUN; ++j) mh[j] = ml[j] = 0.f;
+    for (int q = qa; q < qb; ++q) {
+      float h = 0.f, l = 0.f;
+      if (sub_lo(q) < sub_hi(q)) span_mass<DT>(r, trow, nullptr, sub_lo(q), sub_hi(q), h, l);
+      const int j = (q - qa) >> 5;
+      if (lane == ((q - qa) & 31) && j < DRAW_RUN) { mh[j] = h; ml[j] = l; }
+      if (lane == 0) ff_add2(th, tl, h, l);
+    }
+  };
+  load_masses();
+  float wh = th, wl = tl;
+  warp_sum_ff(wh, wl);
+  if (lane == 0) wsum[warp] = make_float2(wh, wl);
+  __syncthreads();
+  double Z = 0.0;
+  for (int w = 0; w < DRAW_WARPS; ++w) Z += ff_val(wsum[w].x, wsum[w].y);
   if (!(Z > 0.0)) {
     // the residual vanished in fp32: sample target row k instead (reading of
     // the Z = 0 case)
     degenerate = true;
     two = false;
     r.mode = MODE_TARGET;
-    Z = total();
+    __syncthreads();
+    target_masses();
+    wh = th;
+    wl = tl;
+    warp_sum_ff(wh, wl);
+    if (lane == 0) wsum[warp] = make_float2(wh, wl);
+    __syncthreads();
+    Z = 0.0;
+    for (int w = 0; w < DRAW_WARPS; ++w) Z += ff_val(wsum[w].x, wsum[w].y);
   }
   const double tau = double(u) * Z;
-  // the sub-range where the running mass crosses tau
-  double base = 0.0, before = 0.0;
-  int qstar = -1, qlast = 0;
-  double before_last = 0.0;
-  for (int q0 = 0; q0 < nq && qstar < 0; q0 += 32) {
-    float h = 0.f, l = 0.f;
-    if (!degenerate) {
-      if (q0 + lane < nq) zq(q0 + lane, h, l);
-    } else {
-      for (int j = 0; j < 32 && q0 + j < nq; ++j) {
-        float hj, lj;
-        zq(q0 + j, hj, lj);
-        if (lane == j) { h = hj; l = lj; }
-      }
-    }
-    const double z = ff_val(h, l);
-    float sh = h, sl = l;
-    warp_scan_ff(sh, sl, lane);
-    const double incl = ff_val(sh, sl);
-    const unsigned pos = __ballot_sync(0xffffffffu, q0 + lane < nq && z > 0.0);
-    if (pos) {
-      const int l_last = 31 - __clz(pos);
-      qlast = q0 + l_last;
-      before_last = base + __shfl_sync(0xffffffffu, incl - z, l_last);
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, q0 + lane < nq && z > 0.0 && base + incl > tau);
-    if (hit) {
-      const int l0 = __ffs(hit) - 1;
-      qstar = q0 + l0;
-      before = base + __shfl_sync(0xffffffffu, incl - z, l0);
-    }
-    base += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (qstar < 0) {  // rounding: take the last sub-range with mass
-    qstar = qlast;
-    before = before_last;
-  }
-  // scan the sub-range in index order, 32 lanes x runs of consecutive weights
-  const int lo = sub_lo(qstar), hi = sub_hi(qstar);
-  const double tau2 = tau - before;
-  double run = 0.0;
-  int tok = -1, last_pos = -1;
-  auto round = [&](const float* w, int cnt, int e0) {
-    float th = 0.f, tl = 0.f;
-    for (int q = 0; q < cnt; ++q) {
-      ff_add(th, tl, w[q]);
-      if (w[q] > 0.f) last_pos = e0 + q;
-    }
-    const double tot = ff_val(th, tl);
-    warp_scan_ff(th, tl, lane);
-    const double incl = ff_val(th, tl);
-    const unsigned hit = __ballot_sync(0xffffffffu, tot > 0.0 && run + incl > tau2);
-    if (hit) {
-      const int l0 = __ffs(hit) - 1;
-      if (lane == l0) {
-        double acc = run + incl - tot;
-        int v = -1, lp = -1;
-        for (int q = 0; q < cnt; ++q) {
-          acc += double(w[q]);
-          if (w[q] > 0.f) lp = e0 + q;
-          if (acc > tau2) { v = e0 + q; break; }
-        }
-        tok = (v >= 0) ? v : lp;
-      }
-      tok = __shfl_sync(0xffffffffu, tok, l0);
-    }
-    run += __shfl_sync(0xffffffffu, incl, 31);
-  };
-  const unsigned char* tsub = trow + size_t(lo) * E::ES;
-  const unsigned char* dsub = two ? drow + size_t(lo) * E::ES : nullptr;
-  const bool vec_ok = ((reinterpret_cast<uintptr_t>(tsub) & 15u) == 0) &&
-                      (!two || (reinterpret_cast<uintptr_t>(dsub) & 15u) == 0);
-  int done_e = lo;  // elements before done_e have been scanned
-  if (vec_ok) {
-    // whole 16-byte vectors: UMAX per lane loaded at once, then scanned in
-    // rounds of 32 consecutive vectors
-    constexpr int UMAX = 5;
-    const int nv = (hi - lo) / E::VEC;
-    const uint4* tv = reinterpret_cast<const uint4*>(tsub);
-    const uint4* dvp = reinterpret_cast<const uint4*>(two ? dsub : tsub);
-    for (int v0 = 0; v0 < nv && tok < 0; v0 += 32 * UMAX) {
-      uint4 vt[UMAX], vd[UMAX];
-#pragma unroll
-      for (int uu = 0; uu < UMAX; ++uu) {
-        const int j = v0 + 32 * uu + lane;
-        vt[uu] = j < nv ? __ldg(tv + j) : make_uint4(0u, 0u, 0u, 0u);
-        vd[uu] = (two && j < nv) ? __ldg(dvp + j) : vt[uu];
-      }
-#pragma unroll
-      for (int uu = 0; uu < UMAX; ++uu) {
-        if (tok >= 0 || v0 + 32 * uu >= nv) break;
-        const int j = v0 + 32 * uu + lane;
-        float ft[E::VEC], fd[E::VEC], w[E::VEC];
-        E::unpack(vt[uu], ft);
-        E::unpack(vd[uu], fd);
-#pragma unroll
-        for (int q = 0; q < E::VEC; ++q) w[q] = j < nv ? weight(r, ft[q], two ? fd[q] : 0.f) : 0.f;
-        round(w, E::VEC, lo + j * E::VEC);
-      }
-    }
-    done_e = lo + nv * E::VEC;
-  }
-  // the rest (all of it for unaligned rows): rounds of 32 lanes x 8 elements
-  for (int r0 = done_e; r0 < hi && tok < 0; r0 += 256) {
-    const int e0 = r0 + lane * 8;
-    float w[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = e0 + q;
-      w[q] = (e < hi) ? weight(r, E::load(trow, e), two ? E::load(drow, e) : 0.f) : 0.f;
-    }
-    round(w, 8, e0);
-  }
-  if (tok < 0) {  // rounding: the last element with mass in the sub-range
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-      last_pos = max(last_pos, __shfl_xor_sync(0xffffffffu, last_pos, o));
-    tok = last_pos < 0 ? lo : last_pos;
-  }
-  if (lane == 0) {
-    P.out_tokens[size_t(b) * R + r.k] = tok;
-    if (P.out_Z) P.out_Z[b] = float(Z);
-    if (degenerate) set_status(P, SV_ST_DEGENERATE);
-  }
-}
+  pick_warp(tau);
 
-template <int DT>
-__global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
-  const int b = int(blockIdx.x) * DRAW_WARPS + int(threadIdx.x >> 5);
-  if (b < P.B) draw_one<DT>(P, b);
+  // 2. the crossing sub-range within the selected warp's run
+  if (warp == sh_wsel) {
+    const double tau_w = tau - sh_before;
+    double base = 0.0, before = 0.0, before_last = 0.0;
+    int qs = -1, qlast = qa;
+    for (int j = 0; j < DRAW_RUN + (run > 32 * DRAW_RUN ? (run + 31) / 32 : 0) && qs < 0; ++j) {
+      const int q = qa + lane + 32 * j;
+      float h = 0.f, l = 0.f;
+      if (j < DRAW_RUN) {
+#pragma unroll
+        for (int jj = 0; jj < DRAW_RUN; ++jj)
+          if (jj == j) { h = mh[jj]; l = ml[jj]; }
+      } else if (!degenerate) {
+        if (q < qb) {
+          const Mass m = ms[q];
+          h = m.hi;
+          l = m.lo;
+        }
+      } else {  // long runs, degenerate: recompute, one sub-range at a time
+        for (int L = 0; L < 32; ++L) {
+          const int qq = qa + L + 32 * j;
+          float hh = 0.f, hl = 0.f;
+          if (qq < qb && sub_lo(qq) < sub_hi(qq))
+            span_mass<DT>(r, trow, nullptr, sub_lo(qq), sub_hi(qq), hh, hl);
+          if (lane == L) { h = hh; l = hl; }
+        }
+      }
+      if (q >= qb) h = l = 0.f;
+      const double z = ff_val(h, l);
+      float sh = h, sl = l;
+      warp_scan_ff(sh, sl, lane);
+      const double incl = ff_val(sh, sl);
+      const unsigned pos = __ballot_sync(0xffffffffu, q < qb && z > 0.0);
+      if (pos) {
+        const int lp = 31 - __clz(pos);
+        qlast = qa + 32 * j + lp;
+        before_last = base + __shfl_sync(0xffffffffu, incl - z, lp);
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, q < qb && z > 0.0 && base + incl > tau_w);
+      if (hit) {
+        const int l0 = __ffs(hit) - 1;
+        qs = qa + 32 * j + l0;
+        before = base + __shfl_sync(0xffffffffu, incl - z, l0);
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (qs < 0) { qs = qlast; before = before_last; }
+    if (lane == 0) {
+      sh_q = qs;
+      sh_tau = tau_w - before;  // what remains to cross inside the sub-range
+    }
+  }
+  __syncthreads();
+
+  // 3. the sub-range's elements in DRAW_WARPS slices of whole 8-element runs
+  const int q = sh_q;
+  const int lo = sub_lo(q), hi = sub_hi(q);
+  const double tau_q = sh_tau;
+  const int nrun = (hi - lo + 7) / 8;                          // runs of 8 elements
+  const int per_warp = (nrun + DRAW_WARPS - 1) / DRAW_WARPS;   // runs per warp
+  const int ra = min(nrun, warp * per_warp), rb = min(nrun, ra + per_warp);
+  // this lane's runs: ra + lane + 32 j; weights kept for the final scan
+  constexpr int RUNS = 2;  // runs per lane held (slices of up to 64 runs = 512 elements)
+  static_assert((HALF / 2 + NCW - 1) / NCW + 8 <= DRAW_WARPS * 32 * RUNS * 8, "slice size");
+  float w[RUNS][8];
+  float lh = 0.f, ll = 0.f;
+#pragma unroll
+  for (int j = 0; j < RUNS; ++j) {
+    const int rr = ra + lane + 32 * j;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int el = lo + rr * 8 + e;
+      w[j][e] = (rr < rb && el < hi)
+                    ? weight(r, E::load(trow, el), two ? E::load(drow, el) : 0.f)
+                    : 0.f;
+      ff_add(lh, ll, w[j][e]);
+    }
+  }
+  float sh2 = lh, sl2 = ll;
+  warp_sum_ff(sh2, sl2);
+  __syncthreads();  // wsum is reused
+  if (lane == 0) wsum[warp] = make_float2(sh2, sl2);
+  __syncthreads();
+  pick_warp(tau_q);
+  if (warp == sh_wsel) {
+    const double tau_s = tau_q - sh_before;
+    double base = 0.0;
+    int tok = -1, last_pos = -1;
+    for (int j = 0; j < RUNS && tok < 0; ++j) {
+      const int rr = ra + lane + 32 * j;
+      float rh = 0.f, rl = 0.f;
+      for (int e = 0; e < 8; ++e) {
+        ff_add(rh, rl, w[j][e]);
+        if (w[j][e] > 0.f) last_pos = lo + rr * 8 + e;
+      }
+      const double tot = ff_val(rh, rl);
+      float ih = rh, il = rl;
+      warp_scan_ff(ih, il, lane);
+      const double incl = ff_val(ih, il);
+      const unsigned hit = __ballot_sync(0xffffffffu, rr < rb && tot > 0.0 && base + incl > tau_s);
+      if (hit) {
+        const int l0 = __ffs(hit) - 1;
+        if (lane == l0) {
+          double acc = base + incl - tot;
+          int v = -1, lp = -1;
+          for (int e = 0; e < 8; ++e) {
+            acc += double(w[j][e]);
+            if (w[j][e] > 0.f) lp = lo + rr * 8 + e;
+            if (acc > tau_s) { v = lo + rr * 8 + e; break; }
+          }
+          tok = (v >= 0) ? v : lp;
+        }
+        tok = __shfl_sync(0xffffffffu, tok, l0);
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (tok < 0) {  // rounding: the last element with mass in the slice
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+        last_pos = max(last_pos, __shfl_xor_sync(0xffffffffu, last_pos, o));
+      tok = last_pos < 0 ? lo : last_pos;
+    }
+    if (lane == 0) {
+      P.out_tokens[size_t(b) * R + r.k] = tok;
+      // the masses leave out the row's 1/S_t (a common factor)
+      if (P.out_Z) P.out_Z[b] = float(Z * (double(r.ist_hi) + double(r.ist_lo)));
+      if (degenerate) set_status(P, SV_ST_DEGENERATE);
+    }
+  }
   // the last kernel of a sampling call: the workspace is ready for the next one
-  if (blockIdx.x == 0 && threadIdx.x == 0) P.ctrl->state = 0ull;
+  if (last_cta && threadIdx.x == 0) P.ctrl->state = 0ull;
 }
 
 // ---------------------------------------------------------------- host
@@ -1305,6 +1507,9 @@ DevCache g_dev[64];
 
 template <int DT, bool G>
 bool prepare_kernel() {
+  if (!G && cudaFuncSetAttribute(sv_residual<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(SMEM_BYTES)) != cudaSuccess)
+    return false;
   return cudaFuncSetAttribute(sv_reduce<DT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(SMEM_BYTES)) == cudaSuccess;
 }
@@ -1393,8 +1598,7 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const unsigned grid = unsigned(min((long long)sms, P.tasks));
-  const unsigned ndraw = unsigned((B + DRAW_WARPS - 1) / DRAW_WARPS);
-  const unsigned nres = unsigned((long long)B * P.nch2);
+  const unsigned gres = unsigned(min((long long)sms, (long long)B * P.nch2));
   if (dtype == SV_F32) {
     if (greedy) {
       sv_reduce<SV_F32, true><<<grid, NTHR, SMEM_BYTES, st>>>(P);
@@ -1402,8 +1606,8 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
     } else {
       sv_reduce<SV_F32, false><<<grid, NTHR, SMEM_BYTES, st>>>(P);
       sv_decide<SV_F32, false><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, false);
-      sv_residual<SV_F32><<<nres, 32 * NCW, 0, st>>>(P);
-      sv_draw<SV_F32><<<ndraw, 32 * DRAW_WARPS, 0, st>>>(P);
+      sv_residual<SV_F32><<<gres, NTHR, SMEM_BYTES, st>>>(P);
+      sv_draw<SV_F32><<<unsigned(B), 32 * DRAW_WARPS, 0, st>>>(P);
     }
   } else {
     if (greedy) {
@@ -1412,8 +1616,8 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
     } else {
       sv_reduce<SV_BF16, false><<<grid, NTHR, SMEM_BYTES, st>>>(P);
       sv_decide<SV_BF16, false><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, false);
-      sv_residual<SV_BF16><<<nres, 32 * NCW, 0, st>>>(P);
-      sv_draw<SV_BF16><<<ndraw, 32 * DRAW_WARPS, 0, st>>>(P);
+      sv_residual<SV_BF16><<<gres, NTHR, SMEM_BYTES, st>>>(P);
+      sv_draw<SV_BF16><<<unsigned(B), 32 * DRAW_WARPS, 0, st>>>(P);
     }
   }
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
