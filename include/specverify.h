@@ -168,6 +168,16 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
  */
 int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests);
 
+/*
+ * Profiling aid: the next calls record the caller's CUDA events (cudaEvent_t
+ * handles, created on the device the calls run on) on their stream: events[0]
+ * before the first kernel and events[j] after the j-th (sampling runs four
+ * kernels: reduce, decide, residual, draw; greedy runs two), for j < n.
+ * n = 0 turns it off.  n outside [0, 5] or a NULL handle: SV_ERR_INVALID_ARG.
+ * Not thread-safe, like sv_set_tuning().
+ */
+int sv_set_stage_events(void* const* events, int n);
+
 /* Human-readable name of a host return code. */
 const char* sv_error_string(int code);
 

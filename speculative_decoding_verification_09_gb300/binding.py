@@ -21,8 +21,8 @@ SV_ST_TIMEOUT, SV_ST_WORKSPACE, SV_ST_DEGENERATE = 0x8, 0x10, 0x20
 SV_MAX_GAMMA = 32
 
 EXPORTED = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_diag",
-            "spec_verify_greedy", "spec_verify_noalloc", "sv_set_tuning", "sv_error_string",
-            "sv_version")
+            "spec_verify_greedy", "spec_verify_noalloc", "sv_set_tuning",
+            "sv_set_stage_events", "sv_error_string", "sv_version")
 SV_NOALLOC_MAX_WORKSPACE = 16 << 20
 
 _lib = None
@@ -48,10 +48,12 @@ def lib() -> ctypes.CDLL:
         L.spec_verify_greedy.argtypes = [P, P, I, I, I, I, P, P, P, Z, P, P]
         L.spec_verify_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, P, P]
         L.sv_set_tuning.argtypes = [I, I, I]
+        L.sv_set_stage_events.argtypes = [P, I]
         L.sv_error_string.argtypes = [I]
         L.sv_error_string.restype = ctypes.c_char_p
         for name in ("sv_workspace_init", "spec_verify", "spec_verify_diag",
-                     "spec_verify_greedy", "spec_verify_noalloc", "sv_set_tuning", "sv_version"):
+                     "spec_verify_greedy", "spec_verify_noalloc", "sv_set_tuning",
+                     "sv_set_stage_events", "sv_version"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -106,6 +108,13 @@ def make_workspace(B: int, gamma: int, V: int, device) -> torch.Tensor:
 
 def sv_set_tuning(chunk_elems: int = 0, ctas_per_sm: int = 0, lag_requests: int = 0) -> None:
     _check(lib().sv_set_tuning(chunk_elems, ctas_per_sm, lag_requests))
+
+
+def sv_set_stage_events(events) -> None:
+    """Record these torch.cuda.Events (already recorded once, so they exist)
+    around the kernels of the next calls; an empty list turns it off."""
+    handles = (ctypes.c_void_p * max(1, len(events)))(*[e.cuda_event for e in events])
+    _check(lib().sv_set_stage_events(handles if events else None, len(events)))
 
 
 def _shapes(target_logits: torch.Tensor):

@@ -461,43 +461,60 @@ __device__ __forceinline__ float vec_expsum(const uint4& v, unsigned long long m
   return a + b;
 }
 
-// This warp's (max, sum 2^((l-max)*kf)) over its share of one row chunk: the
-// aligned body in shared memory plus, for consumer warp 0, the few unaligned
-// head/tail elements read from global memory.  Target and draft chunks are
-// reduced together, every lane's vectors in registers; each lane sums
-// relative to its own maximum and the lanes' sums are rescaled to the warp's.
-template <int DT, typename Release>
-__device__ void warp_ms2(const unsigned char* st, const unsigned char* sd, const Desc& d,
-                         const unsigned char* gt, const unsigned char* gd, bool has_d, float kf,
-                         int cw, int lane, float4& out, Release release) {
+// A consumer warp's share of one slot: body vector j of a row chunk belongs
+// to consumer thread j mod (NCW*32); the vectors are loaded from shared
+// memory into registers (MAXV per row per thread), plus the chunk fields the
+// reduction needs.  Target and draft shares are loaded together.
+struct Share {
+  uint4 t[MAXV], d[MAXV];
+  int b, i, c, e0, n, head_t, nb_t, head_d, nb_d;
+  float kf;
+};
+template <int DT>
+__device__ __forceinline__ void load_share(const Desc& d, const unsigned char* slot, bool has_d,
+                                           int cw, int lane, Share& sh) {
   using E = Elem<DT>;
   constexpr int NCT = NCW * 32;
   const int tid = cw * 32 + lane;
   const int nvt = d.nb_t / E::VEC, nvd = has_d ? d.nb_d / E::VEC : 0;
   const uint4 neg = make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD);
-  uint4 vt[MAXV], vd[MAXV];
 #pragma unroll
   for (int u = 0; u < MAXV; ++u) {
     const int j = tid + u * NCT;
-    vt[u] = j < nvt ? reinterpret_cast<const uint4*>(st)[j] : neg;
-    vd[u] = j < nvd ? reinterpret_cast<const uint4*>(sd)[j] : neg;
+    sh.t[u] = j < nvt ? reinterpret_cast<const uint4*>(slot)[j] : neg;
+    sh.d[u] = j < nvd ? reinterpret_cast<const uint4*>(slot + HALF)[j] : neg;
   }
-  release();  // the chunk is in registers: the slot can be refilled
+  sh.b = d.b; sh.i = d.i; sh.c = d.c; sh.e0 = d.e0; sh.n = d.n;
+  sh.head_t = d.head_t; sh.nb_t = d.nb_t; sh.head_d = d.head_d; sh.nb_d = d.nb_d;
+  sh.kf = d.kf;
+}
+
+// This warp's (max, sum 2^((l-max)*kf)) over its share of one row chunk: the
+// body vectors in `sh` plus, for consumer warp 0, the few unaligned head/tail
+// elements read from global memory.  Each lane sums relative to its own
+// maximum; the lanes' sums are rescaled to the warp's.
+template <int DT>
+__device__ float4 reduce_share_ms(const Params& P, const Share& sh, bool has_d, int cw, int lane) {
+  using E = Elem<DT>;
+  const float kf = sh.kf;
   float ht = -INFINITY, tt = -INFINITY, hd = -INFINITY, td = -INFINITY;
   if (cw == 0) {
-    if (lane < d.head_t) ht = E::load(gt, lane);
-    if (lane < d.n - d.head_t - d.nb_t) tt = E::load(gt, d.head_t + d.nb_t + lane);
+    const unsigned char* gt = P.Lt + ((size_t(sh.b) * P.R + sh.i) * size_t(P.V) + sh.e0) * E::ES;
+    if (lane < sh.head_t) ht = E::load(gt, lane);
+    if (lane < sh.n - sh.head_t - sh.nb_t) tt = E::load(gt, sh.head_t + sh.nb_t + lane);
     if (has_d) {
-      if (lane < d.head_d) hd = E::load(gd, lane);
-      if (lane < d.n - d.head_d - d.nb_d) td = E::load(gd, d.head_d + d.nb_d + lane);
+      const unsigned char* gd =
+          P.Ld + ((size_t(sh.b) * P.gamma + sh.i) * size_t(P.V) + sh.e0) * E::ES;
+      if (lane < sh.head_d) hd = E::load(gd, lane);
+      if (lane < sh.n - sh.head_d - sh.nb_d) td = E::load(gd, sh.head_d + sh.nb_d + lane);
     }
   }
   // lane maxima: balanced trees over the vectors
   uint32_t wt[MAXV], wd[MAXV];
 #pragma unroll
   for (int u = 0; u < MAXV; ++u) {
-    wt[u] = E::vmax_acc(E::MAX_INIT, vt[u]);
-    wd[u] = E::vmax_acc(E::MAX_INIT, vd[u]);
+    wt[u] = E::vmax_acc(E::MAX_INIT, sh.t[u]);
+    wd[u] = E::vmax_acc(E::MAX_INIT, sh.d[u]);
   }
 #pragma unroll
   for (int w = 1; w < MAXV; w *= 2)
@@ -515,8 +532,8 @@ __device__ void warp_ms2(const unsigned char* st, const unsigned char* sd, const
   float s_t = 0.f, s_d = 0.f;
 #pragma unroll
   for (int u = 0; u < MAXV; ++u) {
-    if (lt) s_t += vec_expsum<DT>(vt[u], mmt, kk);
-    if (ld) s_d += vec_expsum<DT>(vd[u], mmd, kk);
+    if (lt) s_t += vec_expsum<DT>(sh.t[u], mmt, kk);
+    if (ld) s_d += vec_expsum<DT>(sh.d[u], mmd, kk);
   }
   if (lt) s_t += ex2((ht - mt) * kf) + ex2((tt - mt) * kf);
   if (ld) s_d += ex2((hd - md) * kf) + ex2((td - md) * kf);
@@ -533,39 +550,28 @@ __device__ void warp_ms2(const unsigned char* st, const unsigned char* sd, const
     s_t += __shfl_xor_sync(0xffffffffu, s_t, o);
     s_d += __shfl_xor_sync(0xffffffffu, s_d, o);
   }
-  out = make_float4(Mt, s_t, Md, s_d);
+  return make_float4(Mt, s_t, Md, s_d);
 }
 
 // This warp's (largest value, lowest index among its occurrences, NaN seen)
-// over its share of one row chunk; indices are within the row.
-template <int DT, typename Release>
-__device__ void warp_argmax(const unsigned char* sbody, int nb, const unsigned char* gseg,
-                            int head, int n, int e0, int cw, int lane, float& best_out,
-                            int& bi_out, int& nan_out, Release release) {
+// over its share of one target row chunk; indices are within the row.
+template <int DT>
+__device__ float4 reduce_share_argmax(const Params& P, const Share& sh, int cw, int lane) {
   using E = Elem<DT>;
-  const int nv = nb / E::VEC;
-  const int tid = cw * 32 + lane;
   constexpr int NCT = NCW * 32;
-  const uint4* sv = reinterpret_cast<const uint4*>(sbody);
+  const int tid = cw * 32 + lane;
+  const unsigned char* gseg = P.Lt + ((size_t(sh.b) * P.R + sh.i) * size_t(P.V) + sh.e0) * E::ES;
   float best = -INFINITY;
   int bi = INT_MAX, nan = 0;
-  if (cw == 0 && lane < head) {
+  if (cw == 0 && lane < sh.head_t) {
     const float l = E::load(gseg, lane);
     if (l != l) nan = 1;
-    else if (l > best) { best = l; bi = e0 + lane; }
+    else if (l > best) { best = l; bi = sh.e0 + lane; }
   }
-  uint4 vr[MAXV];
 #pragma unroll
   for (int u = 0; u < MAXV; ++u) {
     const int j = tid + u * NCT;
-    vr[u] = j < nv ? sv[j] : make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD,
-                                        E::NEG_INF_WORD);
-  }
-  release();
-#pragma unroll
-  for (int u = 0; u < MAXV; ++u) {
-    const int j = tid + u * NCT;
-    const uint4 v = vr[u];
+    const uint4 v = sh.t[u];
     const float vm = E::vmax(v);
     if (vm != vm) {
       nan = 1;
@@ -577,15 +583,15 @@ __device__ void warp_argmax(const unsigned char* sbody, int nb, const unsigned c
       for (int e = E::VEC - 1; e >= 0; --e)
         if (f[e] == vm) first = e;
       best = vm;
-      bi = e0 + head + j * E::VEC + first;
+      bi = sh.e0 + sh.head_t + j * E::VEC + first;
     }
   }
   if (cw == 0) {
-    const int t0 = head + nb;
-    if (lane < n - t0) {
+    const int t0 = sh.head_t + sh.nb_t;
+    if (lane < sh.n - t0) {
       const float l = E::load(gseg, t0 + lane);
       if (l != l) nan = 1;
-      else if (l > best) { best = l; bi = e0 + t0 + lane; }
+      else if (l > best) { best = l; bi = sh.e0 + t0 + lane; }
     }
   }
 #pragma unroll
@@ -595,12 +601,8 @@ __device__ void warp_argmax(const unsigned char* sbody, int nb, const unsigned c
     const int n2 = __shfl_xor_sync(0xffffffffu, nan, o);
     am_merge(best, bi, nan, b2, i2, n2);
   }
-  best_out = best;
-  bi_out = bi;
-  nan_out = nan;
+  return make_float4(best, __int_as_float(bi), __int_as_float(nan), 0.f);
 }
-
-// ---------------------------------------------- P2 / P3: residual weights
 
 // Weight of one element of the final draw, up to the row's factor 1/S_t
 // (applied once to the masses): e = 2^((l_t - m_t) * kf), the unnormalised
@@ -759,41 +761,37 @@ __device__ void producer(const Params& P, SmemCtl& C, unsigned char* slots) {
   }
 }
 
-// Consumers: every warp reduces its share of each slot from registers (the
-// slot is handed back as soon as the share is loaded) and publishes its own
-// partial.
+// Consumers: every warp loads its share of a slot into registers and hands
+// the slot back at once (so the producer can refill it while the share is
+// reduced), then publishes its own partial.
 template <int DT, bool GREEDY>
 __device__ void consumer(const Params& P, SmemCtl& C, const unsigned char* slots) {
-  using E = Elem<DT>;
   const int cw = int(threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
-  for (long long seq = 0;; ++seq) {
+  // wait for slot `seq`, load this warp's share and release the slot; false
+  // at the end marker or when the CTA gave up
+  auto acquire = [&](long long seq, Share& sh) {
     const int s = int(seq % NSLOT);
     const unsigned use = unsigned(seq / NSLOT);
-    if (!mbar_wait(&C.full[s], use & 1u, P, &C.abort)) return;
-    const Desc d = C.desc[s];
-    const unsigned char* slot = slots + size_t(s) * SLOT;
-    auto release = [&]() {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&C.empty[s]);
-    };
-    if (d.end) return;
-    const unsigned char* tseg = P.Lt + ((size_t(d.b) * P.R + d.i) * size_t(P.V) + d.e0) * E::ES;
-    float4 out;
-    if (GREEDY) {
-      float best;
-      int bi, nan;
-      warp_argmax<DT>(slot, d.nb_t, tseg, d.head_t, d.n, d.e0, cw, lane, best, bi, nan, release);
-      out = make_float4(best, __int_as_float(bi), __int_as_float(nan), 0.f);
-    } else {
-      const bool has_d = d.i < P.gamma;
-      const unsigned char* dseg =
-          has_d ? P.Ld + ((size_t(d.b) * P.gamma + d.i) * size_t(P.V) + d.e0) * E::ES : nullptr;
-      warp_ms2<DT>(slot, slot + HALF, d, tseg, dseg, has_d, d.kf, cw, lane, out, release);
-    }
+    if (!mbar_wait(&C.full[s], use & 1u, P, &C.abort)) return false;
+    const Desc& d = C.desc[s];
+    if (d.end) return false;
+    load_share<DT>(d, slots + size_t(s) * SLOT, !GREEDY && d.i < P.gamma, cw, lane, sh);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&C.empty[s]);
+    return true;
+  };
+  auto process = [&](const Share& sh) {
+    const float4 out = GREEDY ? reduce_share_argmax<DT>(P, sh, cw, lane)
+                              : reduce_share_ms<DT>(P, sh, sh.i < P.gamma, cw, lane);
     if (lane == 0) {
-      Partial* dst = P.part + ((size_t(d.b) * P.R + d.i) * P.nch1 + d.c) * NCW + cw;
+      Partial* dst = P.part + ((size_t(sh.b) * P.R + sh.i) * P.nch1 + sh.c) * NCW + cw;
       *reinterpret_cast<float4*>(dst) = out;
     }
+  };
+  Share sh;
+  for (long long seq = 0;; ++seq) {
+    if (!acquire(seq, sh)) return;
+    process(sh);
   }
 }
 
@@ -1495,6 +1493,8 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
 
 struct Tuning {
   int chunk = 0;
+  cudaEvent_t stage_ev[5] = {};  // profiling: events recorded around the kernels
+  int stage_n = 0;
 };
 Tuning g_tune;
 
@@ -1599,25 +1599,43 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const unsigned grid = unsigned(min((long long)sms, P.tasks));
   const unsigned gres = unsigned(min((long long)sms, (long long)B * P.nch2));
+  // profiling aid: event j after the j-th kernel (event 0 before the first)
+  const Tuning& tu = g_tune;
+  auto mark = [&](int j) {
+    if (j < tu.stage_n) cudaEventRecord(tu.stage_ev[j], st);
+  };
+  mark(0);
   if (dtype == SV_F32) {
     if (greedy) {
       sv_reduce<SV_F32, true><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      mark(1);
       sv_decide<SV_F32, true><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, true);
+      mark(2);
     } else {
       sv_reduce<SV_F32, false><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      mark(1);
       sv_decide<SV_F32, false><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, false);
+      mark(2);
       sv_residual<SV_F32><<<gres, NTHR, SMEM_BYTES, st>>>(P);
+      mark(3);
       sv_draw<SV_F32><<<unsigned(B), 32 * DRAW_WARPS, 0, st>>>(P);
+      mark(4);
     }
   } else {
     if (greedy) {
       sv_reduce<SV_BF16, true><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      mark(1);
       sv_decide<SV_BF16, true><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, true);
+      mark(2);
     } else {
       sv_reduce<SV_BF16, false><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      mark(1);
       sv_decide<SV_BF16, false><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, false);
+      mark(2);
       sv_residual<SV_BF16><<<gres, NTHR, SMEM_BYTES, st>>>(P);
+      mark(3);
       sv_draw<SV_BF16><<<unsigned(B), 32 * DRAW_WARPS, 0, st>>>(P);
+      mark(4);
     }
   }
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
@@ -1728,6 +1746,16 @@ int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests) {
   (void)ctas_per_sm;   // the reduce kernel always runs one CTA per SM
   (void)lag_requests;  // the stages run as separate kernels: there is no lag
   g_tune.chunk = chunk_elems > 0 ? chunk_elems : 0;
+  return SV_OK;
+}
+
+int sv_set_stage_events(void* const* events, int n) {
+  if (n < 0 || n > 5 || (n > 0 && !events)) return SV_ERR_INVALID_ARG;
+  for (int j = 0; j < n; ++j) {
+    if (!events[j]) return SV_ERR_INVALID_ARG;
+    g_tune.stage_ev[j] = static_cast<cudaEvent_t>(events[j]);
+  }
+  g_tune.stage_n = n;
   return SV_OK;
 }
 

@@ -90,3 +90,13 @@ def test_no_gpu_fails_loudly(L):
         pytest.skip("a GPU is present")
     # valid-looking arguments reach the device query, which must fail, not fall back
     assert _call(L) == binding.SV_ERR_CUDA
+
+
+def test_stage_events_validation(L):
+    arr = (ctypes.c_void_p * 6)(*([FAKE] * 6))
+    assert L.sv_set_stage_events(arr, 6) == binding.SV_ERR_INVALID_ARG   # at most five
+    assert L.sv_set_stage_events(arr, -1) == binding.SV_ERR_INVALID_ARG
+    assert L.sv_set_stage_events(None, 2) == binding.SV_ERR_INVALID_ARG
+    nul = (ctypes.c_void_p * 2)(FAKE, None)
+    assert L.sv_set_stage_events(nul, 2) == binding.SV_ERR_INVALID_ARG   # a NULL handle
+    assert L.sv_set_stage_events(None, 0) == binding.SV_OK               # off
