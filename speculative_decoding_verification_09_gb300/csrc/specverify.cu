@@ -44,16 +44,32 @@ namespace {
 
 // ------------------------------------------------------------ constants
 
-// reduce: 15 warps, the producer (warp 0) and NCW consumer warps.  Warp w runs
-// on SM sub-partition w % 4, so sub-partitions 1..3 hold four consumer warps
-// and sub-partition 0 three besides the producer.
+// Streaming kernels: 15 warps, the producer (warp 0) and NCW consumer warps in
+// NGRP groups that take the ring's slots in turn (slot sequence number mod
+// NGRP), so the groups' phases (loading, exponentials, reductions) need not
+// coincide.  Warp w runs on SM sub-partition w % 4; both groups have warps on
+// every sub-partition.
 constexpr int NCW = 14;
 constexpr int NTHR = 32 * (NCW + 1);
-constexpr int NSLOT = 3;               // shared-memory ring depth
-constexpr int HALF = 32768;            // bytes of one row chunk in a slot
-constexpr int SLOT = 2 * HALF;         // target chunk + draft chunk
+// Ring geometry of a streaming kernel: NG consumer groups of GW warps, NS
+// slots (NS / NG per group), HALF bytes per row chunk (a slot holds a target
+// and a draft chunk).
+template <int NG_, int NS_, int HALF_>
+struct Geo {
+  static constexpr int NG = NG_;
+  static constexpr int GW = NCW / NG_;
+  static constexpr int NS = NS_;
+  static constexpr int HALF = HALF_;
+  static constexpr int SLOT = 2 * HALF_;
+  // body vectors of a row chunk per consumer thread: vector j belongs to
+  // thread j mod (GW * 32) of the group
+  static constexpr int MAXV = (HALF_ / 16 + GW * 32 - 1) / (GW * 32);
+  static_assert(NCW % NG_ == 0 && NS_ % NG_ == 0, "groups");
+};
+using GeoReduce = Geo<2, 6, 16384>;    // phase 1: two groups of 7 warps, 6 slots of 32 KB
+using GeoResidual = Geo<1, 3, 32768>;  // phase 2: one group of 14 warps, 3 slots of 64 KB
 constexpr int CH1_MIN = 1024;          // smallest phase-1 chunk (elements)
-constexpr int CH2_F32 = HALF / 4;      // phase-2 chunk for fp32 (the workspace bound)
+constexpr int CH2_F32 = GeoResidual::HALF / 4;  // phase-2 chunk for fp32 (the workspace bound)
 constexpr unsigned SUSPEND_HINT_NS = 1000000u;  // a waiting warp sleeps until the phase completes
 constexpr int SMS_CAP = 256;           // the chunk heuristic assumes at most this many SMs
 constexpr int MAXR = SV_MAX_GAMMA + 1;
@@ -108,15 +124,15 @@ Layout make_layout(int B, int gamma, int V) {
   // the chunk heuristic below never uses more chunks than this (it assumes
   // at most SMS_CAP SMs)
   const long long units = (long long)B * (long long)R;
-  const long long by_bytes = (V + CH2_F32 - 1) / CH2_F32;
+  const long long by_bytes = (V + GeoReduce::HALF / 4 - 1) / (GeoReduce::HALF / 4);
   const long long by_tasks = units > 0 ? (8LL * SMS_CAP + units - 1) / units : 1;
   L.nch1_max = int(min((long long)(V + CH1_MIN - 1) / CH1_MIN, max(by_bytes, by_tasks)));
   L.nch2_max = (V + CH2_F32 - 1) / CH2_F32;
   L.ctrl = 0;
   L.part = align256(sizeof(Ctrl));
-  L.rec = L.part + align256(size_t(B) * R * L.nch1_max * NCW * sizeof(Partial));
+  L.rec = L.part + align256(size_t(B) * R * L.nch1_max * GeoReduce::GW * sizeof(Partial));
   L.mass = L.rec + align256(size_t(B) * sizeof(Record));
-  L.total = L.mass + align256(size_t(B) * L.nch2_max * NCW * sizeof(Mass));
+  L.total = L.mass + align256(size_t(B) * L.nch2_max * GeoResidual::GW * sizeof(Mass));
   return L;
 }
 
@@ -430,19 +446,36 @@ struct alignas(16) Desc {
 };
 static_assert(offsetof(Desc, rec) % 16 == 0 && sizeof(Record) % 16 == 0, "record copy");
 // Shared-memory control block of the streaming kernels (after the slots).
+template <class G>
 struct SmemCtl {
-  unsigned long long full[NSLOT], empty[NSLOT];
-  Desc desc[NSLOT];
+  unsigned long long full[G::NS], empty[G::NS];
+  Desc desc[G::NS];
   int abort;
 };
-constexpr size_t SMEM_BYTES = size_t(NSLOT) * SLOT + sizeof(SmemCtl);
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+template <class G>
+constexpr size_t smem_bytes() {
+  return size_t(G::NS) * G::SLOT + sizeof(SmemCtl<G>);
+}
+static_assert(smem_bytes<GeoReduce>() <= 227 * 1024 && smem_bytes<GeoResidual>() <= 227 * 1024,
+              "shared memory budget");
 
 
 // ------------------------------------------------ phase 1: consumer reductions
 
-constexpr int MAXV = (HALF / 16 + NCW * 32 - 1) / (NCW * 32);
-static_assert(MAXV * 16 * NCW * 32 >= HALF, "chunk split");
+// Group of consumer warp w (1..NCW) and its index in the group.  With two
+// groups: group 0 is warps 1-3 and 8-11, group 1 warps 4-7 and 12-14, so
+// both have warps on every SM sub-partition.
+template <class G>
+__device__ __forceinline__ void consumer_role(int w, int& grp, int& wg) {
+  if (G::NG == 1) {
+    grp = 0;
+    wg = w - 1;
+  } else {
+    static_assert(G::NG <= 2, "role map");
+    grp = (w >> 2) & 1;
+    wg = grp == 0 ? (w < 4 ? w - 1 : w - 5) : (w < 8 ? w - 4 : w - 8);
+  }
+}
 
 // sum over pairs of 2^((f - m) * kf), with packed fp32x2 arithmetic
 template <int DT>
@@ -462,20 +495,22 @@ __device__ __forceinline__ float vec_expsum(const uint4& v, unsigned long long m
 }
 
 // A consumer warp's share of one slot: body vector j of a row chunk belongs
-// to consumer thread j mod (NCW*32); the vectors are loaded from shared
+// to thread j mod (GW*32) of the group; the vectors are loaded from shared
 // memory into registers (MAXV per row per thread), plus the chunk fields the
 // reduction needs.  Target and draft shares are loaded together.
+template <int MAXV>
 struct Share {
   uint4 t[MAXV], d[MAXV];
   int b, i, c, e0, n, head_t, nb_t, head_d, nb_d;
   float kf;
 };
-template <int DT>
+template <int DT, class G>
 __device__ __forceinline__ void load_share(const Desc& d, const unsigned char* slot, bool has_d,
-                                           int cw, int lane, Share& sh) {
+                                           int wg, int lane, Share<G::MAXV>& sh) {
   using E = Elem<DT>;
-  constexpr int NCT = NCW * 32;
-  const int tid = cw * 32 + lane;
+  constexpr int MAXV = G::MAXV, HALF = G::HALF;
+  constexpr int NCT = G::GW * 32;
+  const int tid = wg * 32 + lane;
   const int nvt = d.nb_t / E::VEC, nvd = has_d ? d.nb_d / E::VEC : 0;
   const uint4 neg = make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD);
 #pragma unroll
@@ -493,12 +528,13 @@ __device__ __forceinline__ void load_share(const Desc& d, const unsigned char* s
 // body vectors in `sh` plus, for consumer warp 0, the few unaligned head/tail
 // elements read from global memory.  Each lane sums relative to its own
 // maximum; the lanes' sums are rescaled to the warp's.
-template <int DT>
-__device__ float4 reduce_share_ms(const Params& P, const Share& sh, bool has_d, int cw, int lane) {
+template <int DT, int MAXV>
+__device__ float4 reduce_share_ms(const Params& P, const Share<MAXV>& sh, bool has_d, int wg,
+                                  int lane) {
   using E = Elem<DT>;
   const float kf = sh.kf;
   float ht = -INFINITY, tt = -INFINITY, hd = -INFINITY, td = -INFINITY;
-  if (cw == 0) {
+  if (wg == 0) {
     const unsigned char* gt = P.Lt + ((size_t(sh.b) * P.R + sh.i) * size_t(P.V) + sh.e0) * E::ES;
     if (lane < sh.head_t) ht = E::load(gt, lane);
     if (lane < sh.n - sh.head_t - sh.nb_t) tt = E::load(gt, sh.head_t + sh.nb_t + lane);
@@ -555,15 +591,16 @@ __device__ float4 reduce_share_ms(const Params& P, const Share& sh, bool has_d, 
 
 // This warp's (largest value, lowest index among its occurrences, NaN seen)
 // over its share of one target row chunk; indices are within the row.
-template <int DT>
-__device__ float4 reduce_share_argmax(const Params& P, const Share& sh, int cw, int lane) {
+template <int DT, class G>
+__device__ float4 reduce_share_argmax(const Params& P, const Share<G::MAXV>& sh, int wg, int lane) {
   using E = Elem<DT>;
-  constexpr int NCT = NCW * 32;
-  const int tid = cw * 32 + lane;
+  constexpr int MAXV = G::MAXV;
+  constexpr int NCT = G::GW * 32;
+  const int tid = wg * 32 + lane;
   const unsigned char* gseg = P.Lt + ((size_t(sh.b) * P.R + sh.i) * size_t(P.V) + sh.e0) * E::ES;
   float best = -INFINITY;
   int bi = INT_MAX, nan = 0;
-  if (cw == 0 && lane < sh.head_t) {
+  if (wg == 0 && lane < sh.head_t) {
     const float l = E::load(gseg, lane);
     if (l != l) nan = 1;
     else if (l > best) { best = l; bi = sh.e0 + lane; }
@@ -586,7 +623,7 @@ __device__ float4 reduce_share_argmax(const Params& P, const Share& sh, int cw, 
       bi = sh.e0 + sh.head_t + j * E::VEC + first;
     }
   }
-  if (cw == 0) {
+  if (wg == 0) {
     const int t0 = sh.head_t + sh.nb_t;
     if (lane < sh.n - t0) {
       const float l = E::load(gseg, t0 + lane);
@@ -700,13 +737,27 @@ __device__ __forceinline__ void split(const unsigned char* p, int n, int& head, 
   nb = ((n - head) / E::VEC) * E::VEC;
 }
 
+// The end marker for every consumer group, in slots seq .. seq + NGRP - 1.
+template <class G>
+__device__ void end_markers(const Params& P, SmemCtl<G>& C, long long seq) {
+  for (int g = 0; g < G::NG; ++g, ++seq) {
+    const int s = int(seq % G::NS);
+    const unsigned use = unsigned(seq / G::NS);
+    if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, &C.abort)) return;
+    C.desc[s].end = 1;
+    mbar_arrive(&C.full[s]);
+  }
+}
+
 // Producer (one lane): this CTA's contiguous range of chunks, in order, into
 // the slot ring.  Chunk t is chunk t % nch1 of row t / nch1 (row = b * R + i).
 template <int DT, bool GREEDY>
-__device__ void producer(const Params& P, SmemCtl& C, unsigned char* slots) {
+__device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* slots) {
   using E = Elem<DT>;
-  const long long G = gridDim.x;
-  const long long t0 = P.tasks * blockIdx.x / G, t1 = P.tasks * (blockIdx.x + 1) / G;
+  using G = GeoReduce;
+  constexpr int NS = G::NS, SLOT = G::SLOT, HALF = G::HALF;
+  const long long nb = gridDim.x;
+  const long long t0 = P.tasks * blockIdx.x / nb, t1 = P.tasks * (blockIdx.x + 1) / nb;
   const long long row0 = t0 / P.nch1;
   int c = int(t0 - row0 * P.nch1);
   int b = int(row0 / P.R), i = int(row0 - (long long)b * P.R);
@@ -716,15 +767,14 @@ __device__ void producer(const Params& P, SmemCtl& C, unsigned char* slots) {
   const unsigned char* drow =
       (!GREEDY && i < P.gamma) ? P.Ld + (size_t(b) * P.gamma + i) * size_t(P.V) * E::ES : nullptr;
   for (long long t = t0, seq = 0; t <= t1; ++t, ++seq) {
-    const int s = int(seq % NSLOT);
-    const unsigned use = unsigned(seq / NSLOT);
-    if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, &C.abort)) return;
-    Desc& d = C.desc[s];
+    const int s = int(seq % NS);
+    const unsigned use = unsigned(seq / NS);
     if (t == t1 || C.abort) {
-      d.end = 1;
-      mbar_arrive(&C.full[s]);
+      end_markers(P, C, seq);
       return;
     }
+    if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, &C.abort)) return;
+    Desc& d = C.desc[s];
     d.end = 0;
     d.b = b; d.i = i; d.c = c;
     d.e0 = c * P.ch1;
@@ -765,31 +815,35 @@ __device__ void producer(const Params& P, SmemCtl& C, unsigned char* slots) {
 // the slot back at once (so the producer can refill it while the share is
 // reduced), then publishes its own partial.
 template <int DT, bool GREEDY>
-__device__ void consumer(const Params& P, SmemCtl& C, const unsigned char* slots) {
-  const int cw = int(threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
+__device__ void consumer(const Params& P, SmemCtl<GeoReduce>& C, const unsigned char* slots) {
+  using G = GeoReduce;
+  constexpr int NS = G::NS, SLOT = G::SLOT, GW = G::GW;
+  const int lane = threadIdx.x & 31;
+  int grp, wg;
+  consumer_role<G>(int(threadIdx.x >> 5), grp, wg);
   // wait for slot `seq`, load this warp's share and release the slot; false
   // at the end marker or when the CTA gave up
-  auto acquire = [&](long long seq, Share& sh) {
-    const int s = int(seq % NSLOT);
-    const unsigned use = unsigned(seq / NSLOT);
+  auto acquire = [&](long long seq, Share<G::MAXV>& sh) {
+    const int s = int(seq % NS);
+    const unsigned use = unsigned(seq / NS);
     if (!mbar_wait(&C.full[s], use & 1u, P, &C.abort)) return false;
     const Desc& d = C.desc[s];
     if (d.end) return false;
-    load_share<DT>(d, slots + size_t(s) * SLOT, !GREEDY && d.i < P.gamma, cw, lane, sh);
+    load_share<DT, G>(d, slots + size_t(s) * SLOT, !GREEDY && d.i < P.gamma, wg, lane, sh);
     __syncwarp();
     if (lane == 0) mbar_arrive(&C.empty[s]);
     return true;
   };
-  auto process = [&](const Share& sh) {
-    const float4 out = GREEDY ? reduce_share_argmax<DT>(P, sh, cw, lane)
-                              : reduce_share_ms<DT>(P, sh, sh.i < P.gamma, cw, lane);
+  auto process = [&](const Share<G::MAXV>& sh) {
+    const float4 out = GREEDY ? reduce_share_argmax<DT, G>(P, sh, wg, lane)
+                              : reduce_share_ms<DT, G::MAXV>(P, sh, sh.i < P.gamma, wg, lane);
     if (lane == 0) {
-      Partial* dst = P.part + ((size_t(sh.b) * P.R + sh.i) * P.nch1 + sh.c) * NCW + cw;
+      Partial* dst = P.part + ((size_t(sh.b) * P.R + sh.i) * P.nch1 + sh.c) * GW + wg;
       *reinterpret_cast<float4*>(dst) = out;
     }
   };
-  Share sh;
-  for (long long seq = 0;; ++seq) {
+  Share<G::MAXV> sh;
+  for (long long seq = grp;; seq += G::NG) {
     if (!acquire(seq, sh)) return;
     process(sh);
   }
@@ -797,14 +851,15 @@ __device__ void consumer(const Params& P, SmemCtl& C, const unsigned char* slots
 
 template <int DT, bool GREEDY>
 __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
+  using G = GeoReduce;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* slots = smem;
-  SmemCtl& C = *reinterpret_cast<SmemCtl*>(smem + size_t(NSLOT) * SLOT);
+  SmemCtl<G>& C = *reinterpret_cast<SmemCtl<G>*>(smem + size_t(G::NS) * G::SLOT);
   if (threadIdx.x == 0) {
     C.abort = 0;
-    for (int s = 0; s < NSLOT; ++s) {
+    for (int s = 0; s < G::NS; ++s) {
       mbar_init(&C.full[s], 1);
-      mbar_init(&C.empty[s], NCW);
+      mbar_init(&C.empty[s], G::GW);
     }
     // the workspace is in its ready state between calls; mark this call
     if (blockIdx.x == 0) {
@@ -1054,7 +1109,7 @@ __device__ void span_mass(const Record& r, const unsigned char* trow, const unsi
   const unsigned char* t0 = trow + size_t(lo) * E::ES;
   const unsigned char* d0 = two ? drow + size_t(lo) * E::ES : t0;
   if (((reinterpret_cast<uintptr_t>(t0) | reinterpret_cast<uintptr_t>(d0)) & 15u) == 0) {
-    constexpr int PV = (HALF / 16 + 32 * NCW - 1) / (32 * NCW);
+    constexpr int PV = 4;  // vectors per lane in flight
     const int nv = (hi - lo) / E::VEC;
     const uint4* tv = reinterpret_cast<const uint4*>(t0);
     const uint4* dv = reinterpret_cast<const uint4*>(d0);
@@ -1085,18 +1140,20 @@ __device__ void span_mass(const Record& r, const unsigned char* trow, const unsi
 // skipped.  Each slot gets the chunk of target row k (gamma for the bonus),
 // the draft row k chunk after a rejection, and the request's record.
 template <int DT>
-__device__ void producer_res(const Params& P, SmemCtl& C, unsigned char* slots) {
+__device__ void producer_res(const Params& P, SmemCtl<GeoResidual>& C, unsigned char* slots) {
   using E = Elem<DT>;
-  const long long T = (long long)P.B * P.nch2, G = gridDim.x;
-  const long long t0 = T * blockIdx.x / G, t1 = T * (blockIdx.x + 1) / G;
+  using G = GeoResidual;
+  constexpr int NS = G::NS, SLOT = G::SLOT, HALF = G::HALF;
+  const long long T = (long long)P.B * P.nch2, nb = gridDim.x;
+  const long long t0 = T * blockIdx.x / nb, t1 = T * (blockIdx.x + 1) / nb;
   int b = int(t0 / P.nch2), c = int(t0 - (long long)b * P.nch2);
   int2 km = __ldg(reinterpret_cast<const int2*>(P.rec + b));  // (k, mode)
   int2 km_next = b + 1 < P.B ? __ldg(reinterpret_cast<const int2*>(P.rec + b + 1)) : km;
   long long seq = 0;
   for (long long t = t0; t < t1; ++t) {
     if (km.y == MODE_REJECT || km.y == MODE_BONUS) {
-      const int s = int(seq % NSLOT);
-      const unsigned use = unsigned(seq / NSLOT);
+      const int s = int(seq % NS);
+      const unsigned use = unsigned(seq / NS);
       ++seq;
       if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, &C.abort)) return;
       if (C.abort) break;
@@ -1128,11 +1185,7 @@ __device__ void producer_res(const Params& P, SmemCtl& C, unsigned char* slots) 
       if (b + 1 < P.B) km_next = __ldg(reinterpret_cast<const int2*>(P.rec + b + 1));
     }
   }
-  const int s = int(seq % NSLOT);
-  const unsigned use = unsigned(seq / NSLOT);
-  if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, &C.abort)) return;
-  C.desc[s].end = 1;
-  mbar_arrive(&C.full[s]);
+  end_markers(P, C, seq);
 }
 
 // Mass of this warp's contiguous sub-range [cw*sub, (cw+1)*sub) of a
@@ -1140,10 +1193,12 @@ __device__ void producer_res(const Params& P, SmemCtl& C, unsigned char* slots) 
 // returned as a float pair (hi, lo) valid in every lane.
 template <int DT, typename Release>
 __device__ float2 warp_slot_mass(const Params& P, const Desc& d, const Record& r,
-                                 const unsigned char* slot, int cw, int lane, Release release) {
+                                 const unsigned char* slot, int wg, int lane, Release release) {
   using E = Elem<DT>;
+  using G = GeoResidual;
+  constexpr int HALF = G::HALF;
   const bool two = (r.mode == MODE_REJECT);
-  const int lo = cw * P.sub;
+  const int lo = wg * P.sub;
   const int hi = min(lo + P.sub, d.n);
   float acc = 0.f;
   if (lo >= hi) {
@@ -1154,7 +1209,7 @@ __device__ float2 warp_slot_mass(const Params& P, const Desc& d, const Record& r
         two ? P.Ld + ((size_t(d.b) * P.gamma + r.k) * size_t(P.V) + d.e0) * E::ES : nullptr;
     if (d.head_t == 0 && (!two || d.head_d == 0)) {
       // aligned: whole 16-byte vectors from shared memory, held in registers
-      constexpr int PV = (HALF / 16 + 32 * NCW - 1) / (32 * NCW);
+      constexpr int PV = G::MAXV;  // a sub-range has at most 32 * PV vectors
       const uint4* tv = reinterpret_cast<const uint4*>(slot);
       const uint4* dv = reinterpret_cast<const uint4*>(slot + HALF);
       const int j0 = lo / E::VEC, vhi = min(hi, d.nb_t) / E::VEC;
@@ -1191,11 +1246,16 @@ __device__ float2 warp_slot_mass(const Params& P, const Desc& d, const Record& r
 }
 
 template <int DT>
-__device__ void consumer_res(const Params& P, SmemCtl& C, const unsigned char* slots) {
-  const int cw = int(threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
-  for (long long seq = 0;; ++seq) {
-    const int s = int(seq % NSLOT);
-    const unsigned use = unsigned(seq / NSLOT);
+__device__ void consumer_res(const Params& P, SmemCtl<GeoResidual>& C,
+                             const unsigned char* slots) {
+  using G = GeoResidual;
+  constexpr int NS = G::NS, SLOT = G::SLOT, GW = G::GW;
+  const int lane = threadIdx.x & 31;
+  int grp, wg;
+  consumer_role<G>(int(threadIdx.x >> 5), grp, wg);
+  for (long long seq = grp;; seq += G::NG) {
+    const int s = int(seq % NS);
+    const unsigned use = unsigned(seq / NS);
     if (!mbar_wait(&C.full[s], use & 1u, P, &C.abort)) return;
     const Desc d = C.desc[s];
     if (d.end) return;
@@ -1203,21 +1263,22 @@ __device__ void consumer_res(const Params& P, SmemCtl& C, const unsigned char* s
       __syncwarp();
       if (lane == 0) mbar_arrive(&C.empty[s]);
     };
-    const float2 m = warp_slot_mass<DT>(P, d, d.rec, slots + size_t(s) * SLOT, cw, lane, release);
-    if (lane == 0) P.mass[(size_t(d.b) * P.nch2 + d.c) * NCW + cw] = Mass{m.x, m.y};
+    const float2 m = warp_slot_mass<DT>(P, d, d.rec, slots + size_t(s) * SLOT, wg, lane, release);
+    if (lane == 0) P.mass[(size_t(d.b) * P.nch2 + d.c) * GW + wg] = Mass{m.x, m.y};
   }
 }
 
 template <int DT>
 __global__ void __launch_bounds__(NTHR, 1) sv_residual(const Params P) {
+  using G = GeoResidual;
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* slots = smem;
-  SmemCtl& C = *reinterpret_cast<SmemCtl*>(smem + size_t(NSLOT) * SLOT);
+  SmemCtl<G>& C = *reinterpret_cast<SmemCtl<G>*>(smem + size_t(G::NS) * G::SLOT);
   if (threadIdx.x == 0) {
     C.abort = 0;
-    for (int s = 0; s < NSLOT; ++s) {
+    for (int s = 0; s < G::NS; ++s) {
       mbar_init(&C.full[s], 1);
-      mbar_init(&C.empty[s], NCW);
+      mbar_init(&C.empty[s], G::GW);
     }
   }
   __syncthreads();
@@ -1261,16 +1322,17 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
     return;
   }
   const int R = P.R, V = P.V;
-  const int nq = P.nch2 * NCW;
-  const Mass* ms = P.mass + size_t(b) * P.nch2 * NCW;
+  constexpr int GW = GeoResidual::GW;
+  const int nq = P.nch2 * GW;
+  const Mass* ms = P.mass + size_t(b) * P.nch2 * GW;
   const float u = __ldg(P.u_res + size_t(b) * R + r.k);
   const int rowk = (r.mode == MODE_BONUS) ? P.gamma : r.k;
   const unsigned char* trow = P.Lt + (size_t(b) * R + rowk) * size_t(V) * E::ES;
   bool two = (r.mode == MODE_REJECT);
   const unsigned char* drow =
       two ? P.Ld + (size_t(b) * P.gamma + r.k) * size_t(V) * E::ES : nullptr;
-  auto sub_lo = [&](int q) { return (q / NCW) * P.ch2 + (q % NCW) * P.sub; };
-  auto sub_hi = [&](int q) { return min(sub_lo(q) + P.sub, min(V, (q / NCW + 1) * P.ch2)); };
+  auto sub_lo = [&](int q) { return (q / GW) * P.ch2 + (q % GW) * P.sub; };
+  auto sub_hi = [&](int q) { return min(sub_lo(q) + P.sub, min(V, (q / GW + 1) * P.ch2)); };
   // block-wide exclusive prefix of the warps' pair sums in wsum: the warp
   // where the running sum crosses tau (the last warp with mass if none), and
   // the mass before it; written to sh_wsel / sh_before by thread 0
@@ -1419,7 +1481,8 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
   const int ra = min(nrun, warp * per_warp), rb = min(nrun, ra + per_warp);
   // this lane's runs: ra + lane + 32 j; weights kept for the final scan
   constexpr int RUNS = 2;  // runs per lane held (slices of up to 64 runs = 512 elements)
-  static_assert((HALF / 2 + NCW - 1) / NCW + 8 <= DRAW_WARPS * 32 * RUNS * 8, "slice size");
+  static_assert((GeoResidual::HALF / 2 + GW - 1) / GW + 8 <= DRAW_WARPS * 32 * RUNS * 8,
+                "slice size");
   float w[RUNS][8];
   float lh = 0.f, ll = 0.f;
 #pragma unroll
@@ -1508,10 +1571,10 @@ DevCache g_dev[64];
 template <int DT, bool G>
 bool prepare_kernel() {
   if (!G && cudaFuncSetAttribute(sv_residual<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(SMEM_BYTES)) != cudaSuccess)
+                                 int(smem_bytes<GeoResidual>())) != cudaSuccess)
     return false;
   return cudaFuncSetAttribute(sv_reduce<DT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(SMEM_BYTES)) == cudaSuccess;
+                              int(smem_bytes<GeoReduce>())) == cudaSuccess;
 }
 
 int device_info(int& sms) {
@@ -1555,7 +1618,8 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
   if (rc != SV_OK) return rc;
   const int R = gamma + 1;
   const long long units = (long long)B * R;
-  const int chmax = HALF / ES;  // a row chunk must fit half a slot
+  const int chmax = GeoReduce::HALF / ES;     // a phase-1 chunk fits half a slot
+  const int chmax2 = GeoResidual::HALF / ES;  // phase 2 likewise
 
   // phase-1 chunk: at most half a slot, at least CH1_MIN (or the whole row),
   // and small enough that every SM gets several tasks
@@ -1580,13 +1644,13 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
   P.x = x; P.u_acc = u_acc; P.u_res = u_res; P.temp = temp;
   P.B = B; P.gamma = gamma; P.V = V; P.R = R;
   P.ch1 = ch1; P.nch1 = nch1;
-  P.np1 = nch1 * NCW;
+  P.np1 = nch1 * GeoReduce::GW;
   P.tasks = (long long)B * R * nch1;
-  P.ch2 = chmax;
-  P.nch2 = (V + chmax - 1) / chmax;
+  P.ch2 = chmax2;
+  P.nch2 = (V + chmax2 - 1) / chmax2;
   // each residual warp takes a contiguous sub-range of a phase-2 chunk, a
   // whole number of 16-byte vectors long (the last one may be shorter)
-  P.sub = round_up((chmax + NCW - 1) / NCW, 8);
+  P.sub = round_up((chmax2 + GeoResidual::GW - 1) / GeoResidual::GW, 8);
   P.out_tokens = out_tokens; P.out_n = out_n; P.out_p = out_p; P.out_Z = out_Z;
   P.status = status;
   unsigned char* w = static_cast<unsigned char*>(ws);
@@ -1607,32 +1671,32 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
   mark(0);
   if (dtype == SV_F32) {
     if (greedy) {
-      sv_reduce<SV_F32, true><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      sv_reduce<SV_F32, true><<<grid, NTHR, smem_bytes<GeoReduce>(), st>>>(P);
       mark(1);
       sv_decide<SV_F32, true><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, true);
       mark(2);
     } else {
-      sv_reduce<SV_F32, false><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      sv_reduce<SV_F32, false><<<grid, NTHR, smem_bytes<GeoReduce>(), st>>>(P);
       mark(1);
       sv_decide<SV_F32, false><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, false);
       mark(2);
-      sv_residual<SV_F32><<<gres, NTHR, SMEM_BYTES, st>>>(P);
+      sv_residual<SV_F32><<<gres, NTHR, smem_bytes<GeoResidual>(), st>>>(P);
       mark(3);
       sv_draw<SV_F32><<<unsigned(B), 32 * DRAW_WARPS, 0, st>>>(P);
       mark(4);
     }
   } else {
     if (greedy) {
-      sv_reduce<SV_BF16, true><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      sv_reduce<SV_BF16, true><<<grid, NTHR, smem_bytes<GeoReduce>(), st>>>(P);
       mark(1);
       sv_decide<SV_BF16, true><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, true);
       mark(2);
     } else {
-      sv_reduce<SV_BF16, false><<<grid, NTHR, SMEM_BYTES, st>>>(P);
+      sv_reduce<SV_BF16, false><<<grid, NTHR, smem_bytes<GeoReduce>(), st>>>(P);
       mark(1);
       sv_decide<SV_BF16, false><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, false);
       mark(2);
-      sv_residual<SV_BF16><<<gres, NTHR, SMEM_BYTES, st>>>(P);
+      sv_residual<SV_BF16><<<gres, NTHR, smem_bytes<GeoResidual>(), st>>>(P);
       mark(3);
       sv_draw<SV_BF16><<<unsigned(B), 32 * DRAW_WARPS, 0, st>>>(P);
       mark(4);
