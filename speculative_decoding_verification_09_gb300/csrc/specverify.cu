@@ -929,18 +929,46 @@ __device__ void row_argmax(const Partial* pp, int np, float& best, int& bi, int&
   }
 }
 
+// The draw's normalisers of every row i (one warp, lane i), whichever row
+// turns out to be the first rejection: 1/S_t and, for i < gamma,
+// c0 = (m_t - m_d) * kf + log2(S_t / S_d), each as an unevaluated float pair.
+struct Cand {
+  float ist_hi, ist_lo, c0_hi, c0_lo;
+};
+__device__ void record_candidates(const Params& P, int b, const RowStat* rows, Cand* cand) {
+  const int g = P.gamma, R = P.R;
+  const int lane = threadIdx.x & 31;
+  const float kf = LOG2E_F / __ldg(P.temp + b);
+  for (int i = lane; i < R; i += 32) {
+    const RowStat& rk = rows[i];
+    Cand c{0.f, 0.f, 0.f, 0.f};
+    if (rk.bad == 0) {
+      const double ist = 1.0 / rk.St;
+      c.ist_hi = float(ist);
+      c.ist_lo = float(ist - double(c.ist_hi));
+      if (i < g) {
+        // log2(P_d[v] / P_t[v]) = (l_d[v] - l_t[v]) * kf + (m_t - m_d) * kf + log2(S_t / S_d)
+        const double c0 = (double(rk.mt) - double(rk.md)) * double(kf) + log2(rk.St / rk.Sd);
+        c.c0_hi = float(c0);
+        c.c0_lo = float(c0 - double(c.c0_hi));
+      }
+    }
+    cand[i] = c;
+  }
+}
+
 // Sampling decision of request b (warp 0 of the CTA, rows in `rows`): lane
 // i < gamma tests position i, accept iff u <= min(1, P_t / P_d) with
 // P_t / P_d = 2^((l_t - m_t) * k - (l_d - m_d) * k) * S_d / S_t in fp64;
-// then the first rejection k, the outputs but token k, and the record.
+// then the first rejection k and the outputs but token k.  Returns the
+// record's mode and k (in lane 0).
 template <int DT>
-__device__ void decide_sample(const Params& P, int b, const RowStat* rows, float lt, float ld,
+__device__ int2 decide_sample(const Params& P, int b, const RowStat* rows, float lt, float ld,
                               float u, bool tok_ok, int xi) {
   const int g = P.gamma, R = P.R;
   const int lane = threadIdx.x & 31;
   const float T = __ldg(P.temp + b);
   const bool t_ok = isfinite(T) && T >= 0x1p-126f;
-  const float kf = LOG2E_F / T;
   const double k64 = LOG2E_D / double(T);
   int bad = 0, acc = 1;
   float pt = NAN, pd = NAN;
@@ -968,8 +996,9 @@ __device__ void decide_sample(const Params& P, int b, const RowStat* rows, float
   const bool valid = (bad == 0);
   const unsigned rej = __ballot_sync(0xffffffffu, lane < g && !acc);
   const int k = rej ? __ffs(rej) - 1 : g;
+  // lane i < gamma holds x_i (no shuffle: lanes i >= R skip this loop)
   for (int i = lane; i < R; i += 32) {
-    const int tok = __shfl_sync(0xffffffffu, xi, i & 31);
+    const int tok = i < g ? xi : -1;
     if (!valid || i != k) P.out_tokens[size_t(b) * R + i] = (valid && i < k) ? tok : -1;
   }
   if (P.out_p && lane < g) {
@@ -980,29 +1009,33 @@ __device__ void decide_sample(const Params& P, int b, const RowStat* rows, float
     P.out_n[b] = valid ? k : 0;
     if (!valid && P.out_Z) P.out_Z[b] = NAN;
     set_status(P, bad);
-    Record r;
-    r.k = k;
-    r.mode = !valid ? MODE_INVALID : (k < g ? MODE_REJECT : MODE_BONUS);
-    r.kf = kf;
-    r.mt = 0.f;
-    r.ist_hi = r.ist_lo = r.c0_hi = r.c0_lo = 0.f;
-    r.pad[0] = r.pad[1] = r.pad[2] = r.pad[3] = 0;
-    if (valid) {
-      const RowStat& rk = rows[k];
-      r.mt = rk.mt;
-      const double ist = 1.0 / rk.St;
-      r.ist_hi = float(ist);
-      r.ist_lo = float(ist - double(r.ist_hi));
-      // log2(P_d[v] / P_t[v]) = (l_d[v] - l_t[v]) * kf + (m_t - m_d) * kf + log2(S_t / S_d)
-      const double c0 =
-          k < g ? (double(rk.mt) - double(rk.md)) * double(kf) + log2(rk.St / rk.Sd) : 0.0;
-      r.c0_hi = float(c0);
-      r.c0_lo = float(c0 - double(r.c0_hi));
-    }
-    int4* d = reinterpret_cast<int4*>(P.rec + b);
-    const int4* src = reinterpret_cast<const int4*>(&r);
-    d[0] = src[0]; d[1] = src[1]; d[2] = src[2];
   }
+  return make_int2(!valid ? MODE_INVALID : (k < g ? MODE_REJECT : MODE_BONUS), k);
+}
+
+// The decision record of request b (one thread): the draw's row k and its
+// normalisers, read by the residual and draw kernels.
+__device__ void write_record(const Params& P, int b, int mode, int k, const RowStat* rows,
+                             const Cand* cand) {
+  Record r;
+  r.k = k;
+  r.mode = mode;
+  r.kf = LOG2E_F / __ldg(P.temp + b);
+  r.mt = 0.f;
+  r.ist_hi = r.ist_lo = r.c0_hi = r.c0_lo = 0.f;
+  r.pad[0] = r.pad[1] = r.pad[2] = r.pad[3] = 0;
+  if (mode != MODE_INVALID) {
+    r.mt = rows[k].mt;
+    r.ist_hi = cand[k].ist_hi;
+    r.ist_lo = cand[k].ist_lo;
+    if (mode == MODE_REJECT) {
+      r.c0_hi = cand[k].c0_hi;
+      r.c0_lo = cand[k].c0_lo;
+    }
+  }
+  int4* d = reinterpret_cast<int4*>(P.rec + b);
+  const int4* src = reinterpret_cast<const int4*>(&r);
+  d[0] = src[0]; d[1] = src[1]; d[2] = src[2];
 }
 
 // Greedy decision of request b (warp 0, rows in `rows`).
@@ -1042,6 +1075,8 @@ template <int DT, bool GREEDY>
 __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, bool last) {
   using E = Elem<DT>;
   __shared__ RowStat rows[MAXR];
+  __shared__ Cand cand[MAXR];
+  __shared__ int2 mode_k;
   const int b = blockIdx.x, warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int g = P.gamma, R = P.R, V = P.V;
   float lt = 0.f, ld = 0.f, u = 0.f;
@@ -1084,9 +1119,17 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
     }
   }
   __syncthreads();
-  if (warp == 0) {
-    if (GREEDY) decide_greedy(P, b, rows);
-    else decide_sample<DT>(P, b, rows, lt, ld, u, tok_ok, xi);
+  if (GREEDY) {
+    if (warp == 0) decide_greedy(P, b, rows);
+  } else {
+    // the record's normalisers for every row, beside the acceptance tests
+    if (warp == 1) record_candidates(P, b, rows, cand);
+    if (warp == 0) {
+      const int2 mk = decide_sample<DT>(P, b, rows, lt, ld, u, tok_ok, xi);
+      if (lane == 0) mode_k = mk;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) write_record(P, b, mode_k.x, mode_k.y, rows, cand);
   }
   // greedy verification ends here: the workspace is ready for the next call
   if (last && b == 0 && threadIdx.x == 0) P.ctrl->state = 0ull;
@@ -1291,6 +1334,38 @@ __global__ void __launch_bounds__(NTHR, 1) sv_residual(const Params P) {
 
 // ------------------------------------------------------------ draw
 
+// Float pairs (hi, lo), hi + lo the value: comparisons and the product with a
+// float, in fp32 arithmetic (the fp64 units are slow on this part).
+struct FF {
+  float h, l;
+};
+__device__ __forceinline__ FF ff(float h, float l = 0.f) { return FF{h, l}; }
+__device__ __forceinline__ FF operator+(FF a, FF b) {
+  ff_add2(a.h, a.l, b.h, b.l);
+  return a;
+}
+__device__ __forceinline__ FF operator-(FF a, FF b) {
+  ff_add2(a.h, a.l, -b.h, -b.l);
+  return a;
+}
+__device__ __forceinline__ bool ff_gt(FF a, FF b) {  // a > b
+  const FF d = a - b;
+  return d.h > 0.f || (d.h == 0.f && d.l > 0.f);
+}
+__device__ __forceinline__ bool ff_pos(FF a) { return a.h > 0.f || (a.h == 0.f && a.l > 0.f); }
+__device__ __forceinline__ FF ff_mul(float u, FF z) {  // u * z
+  const float p = u * z.h;
+  const float e = fmaf(u, z.h, -p);  // the product's rounding error, exactly
+  const float t = e + u * z.l;
+  FF r;
+  r.h = p + t;
+  r.l = t - (r.h - p);
+  return r;
+}
+__device__ __forceinline__ FF ff_shfl(FF a, int src) {
+  return FF{__shfl_sync(0xffffffffu, a.h, src), __shfl_sync(0xffffffffu, a.l, src)};
+}
+
 // Token k of request b, one CTA of DRAW_WARPS warps:
 //   1. every warp takes a contiguous run of sub-ranges, loads their masses
 //      (published by the residual kernel) and sums them; a block prefix over
@@ -1300,14 +1375,15 @@ __global__ void __launch_bounds__(NTHR, 1) sv_residual(const Params P) {
 //      slice's weights; a block prefix finds the crossing slice, whose warp
 //      scans it in index order.
 // When the residual summed to 0 (degenerate), the masses of target row k are
-// recomputed in step 1 instead.  Running sums are float pairs, compared in fp64.
+// recomputed in step 1 instead.  Running sums and tau are float pairs.
 constexpr int DRAW_RUN = 4;  // sub-ranges per lane in step 1 (run of 128 per warp)
 
 template <int DT>
 __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
   using E = Elem<DT>;
-  __shared__ float2 wsum[DRAW_WARPS];
-  __shared__ double sh_tau, sh_before;
+  constexpr int GW = GeoResidual::GW;
+  __shared__ FF wsum[DRAW_WARPS];
+  __shared__ FF sh_rest, sh_before;
   __shared__ int sh_q, sh_wsel;
   const int b = int(blockIdx.x), warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
   Record r;
@@ -1322,7 +1398,6 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
     return;
   }
   const int R = P.R, V = P.V;
-  constexpr int GW = GeoResidual::GW;
   const int nq = P.nch2 * GW;
   const Mass* ms = P.mass + size_t(b) * P.nch2 * GW;
   const float u = __ldg(P.u_res + size_t(b) * R + r.k);
@@ -1333,22 +1408,21 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
       two ? P.Ld + (size_t(b) * P.gamma + r.k) * size_t(V) * E::ES : nullptr;
   auto sub_lo = [&](int q) { return (q / GW) * P.ch2 + (q % GW) * P.sub; };
   auto sub_hi = [&](int q) { return min(sub_lo(q) + P.sub, min(V, (q / GW + 1) * P.ch2)); };
-  // block-wide exclusive prefix of the warps' pair sums in wsum: the warp
-  // where the running sum crosses tau (the last warp with mass if none), and
-  // the mass before it; written to sh_wsel / sh_before by thread 0
-  auto pick_warp = [&](double tau) {
+  // block-wide prefix of the warps' sums in wsum: the warp where the running
+  // sum crosses tau (the last warp with mass if none) and the mass before it,
+  // into sh_wsel / sh_before (thread 0)
+  auto pick_warp = [&](FF tau) {
     if (threadIdx.x == 0) {
-      double base = 0.0;
+      FF base = ff(0.f), before = ff(0.f), before_last = ff(0.f);
       int sel = -1, last = -1;
-      double before_last = 0.0, before = 0.0;
       for (int w = 0; w < DRAW_WARPS; ++w) {
-        const double z = ff_val(wsum[w].x, wsum[w].y);
-        if (z > 0.0) {
+        const FF z = wsum[w];
+        if (ff_pos(z)) {
           last = w;
           before_last = base;
-          if (sel < 0 && base + z > tau) { sel = w; before = base; }
+          if (sel < 0 && ff_gt(base + z, tau)) { sel = w; before = base; }
         }
-        base += z;
+        base = base + z;
       }
       if (sel < 0) { sel = last < 0 ? 0 : last; before = before_last; }
       sh_wsel = sel;
@@ -1361,45 +1435,48 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
   const int run = (nq + DRAW_WARPS - 1) / DRAW_WARPS;
   const int qa = min(nq, warp * run), qb = min(nq, qa + run);
   bool degenerate = false;
-  float mh[DRAW_RUN], ml[DRAW_RUN];  // this lane's masses q = qa + lane + 32 j
-  float th = 0.f, tl = 0.f;
+  FF mq[DRAW_RUN];  // this lane's masses q = qa + lane + 32 j
+  FF tot = ff(0.f);
   auto load_masses = [&]() {
-    th = tl = 0.f;
+    tot = ff(0.f);
 #pragma unroll
     for (int j = 0; j < DRAW_RUN; ++j) {
       const int q = qa + lane + 32 * j;
-      mh[j] = ml[j] = 0.f;
+      mq[j] = ff(0.f);
       if (q < qb) {
         const Mass m = ms[q];
-        mh[j] = m.hi;
-        ml[j] = m.lo;
+        mq[j] = ff(m.hi, m.lo);
       }
-      ff_add2(th, tl, mh[j], ml[j]);
+      tot = tot + mq[j];
     }
     for (int q = qa + lane + 32 * DRAW_RUN; q < qb; q += 32) {  // runs beyond 32 * DRAW_RUN
       const Mass m = ms[q];
-      ff_add2(th, tl, m.hi, m.lo);
+      tot = tot + ff(m.hi, m.lo);
     }
   };
   auto target_masses = [&]() {  // degenerate case: masses of target row k, recomputed
-    th = tl = 0.f;
-    for (int j = 0; j < DRAW_RUN; ++j) mh[j] = ml[j] = 0.f;
+    tot = ff(0.f);
+    for (int j = 0; j < DRAW_RUN; ++j) mq[j] = ff(0.f);
     for (int q = qa; q < qb; ++q) {
       float h = 0.f, l = 0.f;
       if (sub_lo(q) < sub_hi(q)) span_mass<DT>(r, trow, nullptr, sub_lo(q), sub_hi(q), h, l);
       const int j = (q - qa) >> 5;
-      if (lane == ((q - qa) & 31) && j < DRAW_RUN) { mh[j] = h; ml[j] = l; }
-      if (lane == 0) ff_add2(th, tl, h, l);
+      if (lane == ((q - qa) & 31) && j < DRAW_RUN) mq[j] = ff(h, l);
+      if (lane == 0) tot = tot + ff(h, l);
     }
   };
+  auto block_total = [&]() {
+    FF w = tot;
+    warp_sum_ff(w.h, w.l);
+    if (lane == 0) wsum[warp] = w;
+    __syncthreads();
+    FF z = ff(0.f);
+    for (int k = 0; k < DRAW_WARPS; ++k) z = z + wsum[k];
+    return z;
+  };
   load_masses();
-  float wh = th, wl = tl;
-  warp_sum_ff(wh, wl);
-  if (lane == 0) wsum[warp] = make_float2(wh, wl);
-  __syncthreads();
-  double Z = 0.0;
-  for (int w = 0; w < DRAW_WARPS; ++w) Z += ff_val(wsum[w].x, wsum[w].y);
-  if (!(Z > 0.0)) {
+  FF Z = block_total();
+  if (!ff_pos(Z)) {
     // the residual vanished in fp32: sample target row k instead (reading of
     // the Z = 0 case)
     degenerate = true;
@@ -1407,34 +1484,28 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
     r.mode = MODE_TARGET;
     __syncthreads();
     target_masses();
-    wh = th;
-    wl = tl;
-    warp_sum_ff(wh, wl);
-    if (lane == 0) wsum[warp] = make_float2(wh, wl);
-    __syncthreads();
-    Z = 0.0;
-    for (int w = 0; w < DRAW_WARPS; ++w) Z += ff_val(wsum[w].x, wsum[w].y);
+    Z = block_total();
   }
-  const double tau = double(u) * Z;
+  const FF tau = ff_mul(u, Z);
   pick_warp(tau);
 
   // 2. the crossing sub-range within the selected warp's run
   if (warp == sh_wsel) {
-    const double tau_w = tau - sh_before;
-    double base = 0.0, before = 0.0, before_last = 0.0;
+    const FF tau_w = tau - sh_before;
+    FF base = ff(0.f), before = ff(0.f), before_last = ff(0.f);
     int qs = -1, qlast = qa;
-    for (int j = 0; j < DRAW_RUN + (run > 32 * DRAW_RUN ? (run + 31) / 32 : 0) && qs < 0; ++j) {
+    const int nj = run > 32 * DRAW_RUN ? (run + 31) / 32 : DRAW_RUN;
+    for (int j = 0; j < nj && qs < 0; ++j) {
       const int q = qa + lane + 32 * j;
-      float h = 0.f, l = 0.f;
+      FF z = ff(0.f);
       if (j < DRAW_RUN) {
 #pragma unroll
         for (int jj = 0; jj < DRAW_RUN; ++jj)
-          if (jj == j) { h = mh[jj]; l = ml[jj]; }
+          if (jj == j) z = mq[jj];
       } else if (!degenerate) {
         if (q < qb) {
           const Mass m = ms[q];
-          h = m.hi;
-          l = m.lo;
+          z = ff(m.hi, m.lo);
         }
       } else {  // long runs, degenerate: recompute, one sub-range at a time
         for (int L = 0; L < 32; ++L) {
@@ -1442,32 +1513,31 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
           float hh = 0.f, hl = 0.f;
           if (qq < qb && sub_lo(qq) < sub_hi(qq))
             span_mass<DT>(r, trow, nullptr, sub_lo(qq), sub_hi(qq), hh, hl);
-          if (lane == L) { h = hh; l = hl; }
+          if (lane == L) z = ff(hh, hl);
         }
       }
-      if (q >= qb) h = l = 0.f;
-      const double z = ff_val(h, l);
-      float sh = h, sl = l;
-      warp_scan_ff(sh, sl, lane);
-      const double incl = ff_val(sh, sl);
-      const unsigned pos = __ballot_sync(0xffffffffu, q < qb && z > 0.0);
+      if (q >= qb) z = ff(0.f);
+      FF incl = z;
+      warp_scan_ff(incl.h, incl.l, lane);
+      const bool posz = q < qb && ff_pos(z);
+      const unsigned pos = __ballot_sync(0xffffffffu, posz);
       if (pos) {
         const int lp = 31 - __clz(pos);
         qlast = qa + 32 * j + lp;
-        before_last = base + __shfl_sync(0xffffffffu, incl - z, lp);
+        before_last = base + ff_shfl(incl - z, lp);
       }
-      const unsigned hit = __ballot_sync(0xffffffffu, q < qb && z > 0.0 && base + incl > tau_w);
+      const unsigned hit = __ballot_sync(0xffffffffu, posz && ff_gt(base + incl, tau_w));
       if (hit) {
         const int l0 = __ffs(hit) - 1;
         qs = qa + 32 * j + l0;
-        before = base + __shfl_sync(0xffffffffu, incl - z, l0);
+        before = base + ff_shfl(incl - z, l0);
       }
-      base += __shfl_sync(0xffffffffu, incl, 31);
+      base = base + ff_shfl(incl, 31);
     }
     if (qs < 0) { qs = qlast; before = before_last; }
     if (lane == 0) {
       sh_q = qs;
-      sh_tau = tau_w - before;  // what remains to cross inside the sub-range
+      sh_rest = tau_w - before;  // what remains to cross inside the sub-range
     }
   }
   __syncthreads();
@@ -1475,16 +1545,15 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
   // 3. the sub-range's elements in DRAW_WARPS slices of whole 8-element runs
   const int q = sh_q;
   const int lo = sub_lo(q), hi = sub_hi(q);
-  const double tau_q = sh_tau;
+  const FF tau_q = sh_rest;
   const int nrun = (hi - lo + 7) / 8;                          // runs of 8 elements
   const int per_warp = (nrun + DRAW_WARPS - 1) / DRAW_WARPS;   // runs per warp
   const int ra = min(nrun, warp * per_warp), rb = min(nrun, ra + per_warp);
-  // this lane's runs: ra + lane + 32 j; weights kept for the final scan
   constexpr int RUNS = 2;  // runs per lane held (slices of up to 64 runs = 512 elements)
   static_assert((GeoResidual::HALF / 2 + GW - 1) / GW + 8 <= DRAW_WARPS * 32 * RUNS * 8,
                 "slice size");
   float w[RUNS][8];
-  float lh = 0.f, ll = 0.f;
+  tot = ff(0.f);
 #pragma unroll
   for (int j = 0; j < RUNS; ++j) {
     const int rr = ra + lane + 32 * j;
@@ -1494,46 +1563,42 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
       w[j][e] = (rr < rb && el < hi)
                     ? weight(r, E::load(trow, el), two ? E::load(drow, el) : 0.f)
                     : 0.f;
-      ff_add(lh, ll, w[j][e]);
+      ff_add(tot.h, tot.l, w[j][e]);
     }
   }
-  float sh2 = lh, sl2 = ll;
-  warp_sum_ff(sh2, sl2);
   __syncthreads();  // wsum is reused
-  if (lane == 0) wsum[warp] = make_float2(sh2, sl2);
-  __syncthreads();
+  block_total();
   pick_warp(tau_q);
   if (warp == sh_wsel) {
-    const double tau_s = tau_q - sh_before;
-    double base = 0.0;
+    const FF tau_s = tau_q - sh_before;
+    FF base = ff(0.f);
     int tok = -1, last_pos = -1;
     for (int j = 0; j < RUNS && tok < 0; ++j) {
       const int rr = ra + lane + 32 * j;
-      float rh = 0.f, rl = 0.f;
+      FF rs = ff(0.f);
       for (int e = 0; e < 8; ++e) {
-        ff_add(rh, rl, w[j][e]);
+        ff_add(rs.h, rs.l, w[j][e]);
         if (w[j][e] > 0.f) last_pos = lo + rr * 8 + e;
       }
-      const double tot = ff_val(rh, rl);
-      float ih = rh, il = rl;
-      warp_scan_ff(ih, il, lane);
-      const double incl = ff_val(ih, il);
-      const unsigned hit = __ballot_sync(0xffffffffu, rr < rb && tot > 0.0 && base + incl > tau_s);
+      FF incl = rs;
+      warp_scan_ff(incl.h, incl.l, lane);
+      const unsigned hit =
+          __ballot_sync(0xffffffffu, rr < rb && ff_pos(rs) && ff_gt(base + incl, tau_s));
       if (hit) {
         const int l0 = __ffs(hit) - 1;
         if (lane == l0) {
-          double acc = base + incl - tot;
+          FF acc = base + (incl - rs);
           int v = -1, lp = -1;
           for (int e = 0; e < 8; ++e) {
-            acc += double(w[j][e]);
+            ff_add(acc.h, acc.l, w[j][e]);
             if (w[j][e] > 0.f) lp = lo + rr * 8 + e;
-            if (acc > tau_s) { v = lo + rr * 8 + e; break; }
+            if (ff_gt(acc, tau_s)) { v = lo + rr * 8 + e; break; }
           }
           tok = (v >= 0) ? v : lp;
         }
         tok = __shfl_sync(0xffffffffu, tok, l0);
       }
-      base += __shfl_sync(0xffffffffu, incl, 31);
+      base = base + ff_shfl(incl, 31);
     }
     if (tok < 0) {  // rounding: the last element with mass in the slice
 #pragma unroll
@@ -1544,7 +1609,8 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
     if (lane == 0) {
       P.out_tokens[size_t(b) * R + r.k] = tok;
       // the masses leave out the row's 1/S_t (a common factor)
-      if (P.out_Z) P.out_Z[b] = float(Z * (double(r.ist_hi) + double(r.ist_lo)));
+      if (P.out_Z) P.out_Z[b] = float((double(Z.h) + double(Z.l)) *
+                                      (double(r.ist_hi) + double(r.ist_lo)));
       if (degenerate) set_status(P, SV_ST_DEGENERATE);
     }
   }
