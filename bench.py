@@ -191,11 +191,13 @@ def run_ours(args) -> None:
     cid = WORKLOADS[args.workload]
     cfg = synth.CONFIGS[cid]
     B, g, V = cfg["B"], cfg["gamma"], cfg["V"]
+    if args.batch:  # a smaller batch of the same workload (profiling captures)
+        B = args.batch
     greedy = cfg["kind"] == "greedy"
     stream = torch.cuda.current_stream(dev)
 
     # input sets: host copies (pinned, for the end-to-end leg) and device copies
-    host_sets = [synth.make_inputs(cid, set_index=1000 * rank + s) for s in range(args.sets)]
+    host_sets = [synth.make_inputs(cid, set_index=1000 * rank + s, B=B) for s in range(args.sets)]
     logit_bytes = host_sets[0].Lt.nbytes if greedy else host_sets[0].logit_bytes
 
     def dev_tensors(inp):
@@ -325,10 +327,15 @@ def run_ours(args) -> None:
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         n_req = min(B, args.cpu_requests)
-        v, dt = oracle_positions_per_s(host_sets[0], n_req, cores)
+        # repeat the bounded sample until about cpu_seconds of work were timed
+        passes, dt = 0, 0.0
+        while passes == 0 or dt < args.cpu_seconds:
+            dt += oracle_positions_per_s(host_sets[0], n_req, cores)[1]
+            passes += 1
+        v = passes * n_req * g / dt
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"first {n_req} of {B} requests of {cfg['name']} (set 0), fp64, "
-                         f"{cores} threads, {dt:.2f} s wall"}
+                         f"{cores} threads, {passes} passes, {dt:.1f} s wall"}
 
     if rank != 0:
         return
@@ -365,10 +372,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c4")
     ap.add_argument("--sets", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="requests per step (0 = the workload's own); for profiling captures")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-requests", type=int, default=256)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="approximate seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-requests", type=int, default=32)
     ap.add_argument("--chunk", type=int, default=0, help="phase-1 chunk elements (0 = auto)")
     ap.add_argument("--lag", type=int, default=0, help="accepted and ignored (no lag)")
