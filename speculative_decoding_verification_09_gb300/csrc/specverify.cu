@@ -64,9 +64,12 @@ struct Geo {
   // body vectors of a row chunk per consumer thread: vector j belongs to
   // thread j mod (GW * 32) of the group
   static constexpr int MAXV = (HALF_ / 16 + GW * 32 - 1) / (GW * 32);
+  // Every use of a slot must be consumed by the same group: a group waits
+  // for use u of a slot only after consuming use u - 1, which is what makes
+  // the mbarrier's phase parity unambiguous.
   static_assert(NCW % NG_ == 0 && NS_ % NG_ == 0, "groups");
 };
-using GeoReduce = Geo<2, 6, 16384>;    // phase 1: two groups of 7 warps, 6 slots of 32 KB
+using GeoReduce = Geo<2, 8, 14336>;    // phase 1: two groups of 7 warps, 8 slots of 28 KB
 using GeoResidual = Geo<1, 3, 32768>;  // phase 2: one group of 14 warps, 3 slots of 64 KB
 constexpr int CH1_MIN = 1024;          // smallest phase-1 chunk (elements)
 constexpr int CH2_F32 = GeoResidual::HALF / 4;  // phase-2 chunk for fp32 (the workspace bound)
@@ -647,16 +650,17 @@ __device__ float4 reduce_share_argmax(const Params& P, const Share<G::MAXV>& sh,
 // with delta = log2(P_d / P_t) = (l_d - l_t) * kf + c0, which keeps its
 // relative precision where the rows nearly agree (no cancellation).  delta is
 // clamped to <= 0 (weight 0, also for NaN); 1 - 2^delta is 1 - ex2(delta)
-// where that loses nothing (delta < -1/2), else its Taylor series in delta,
-// sum_{n=1..7} -(ln 2)^n / n! * delta^n (truncation below 2e-8 relative).
-// weight() and vec_weights() perform the same fp32 operations per element.
+// where that loses little (delta < -1/2: ex2's relative error 2^-22 grows by
+// at most 2^delta / (1 - 2^delta) < 2.5), else its Taylor series in delta,
+// sum_{n=1..6} -(ln 2)^n / n! * delta^n (truncation below 4e-7 relative).
+// The exponent (l_t - m_t) * kf is formed as one fma with -m_t * kf rounded
+// once per row: a common factor of all the row's weights.  weight() and
+// vec_weights() perform the same fp32 operations per element.
 constexpr float OMC1 = -0.69314718055994531f, OMC2 = -0.24022650695910071f,
                 OMC3 = -0.055504108664821580f, OMC4 = -0.0096181291076284772f,
-                OMC5 = -0.0013333558146428443f, OMC6 = -1.5403530393381609e-4f,
-                OMC7 = -1.5252733804059841e-5f;
+                OMC5 = -0.0013333558146428443f, OMC6 = -1.5403530393381609e-4f;
 __device__ __forceinline__ float one_minus_exp2(float delta) {
-  float p = OMC7;
-  p = fmaf(p, delta, OMC6);
+  float p = OMC6;
   p = fmaf(p, delta, OMC5);
   p = fmaf(p, delta, OMC4);
   p = fmaf(p, delta, OMC3);
@@ -668,7 +672,7 @@ __device__ __forceinline__ float one_minus_exp2(float delta) {
 }
 
 __device__ __forceinline__ float weight(const Record& r, float lt, float ld) {
-  const float et = ex2((lt - r.mt) * r.kf);
+  const float et = ex2(fmaf(lt, r.kf, -(r.mt * r.kf)));
   if (r.mode == MODE_REJECT) {
     const float delta = fminf(fmaf(ld - lt, r.kf, r.c0_hi) + r.c0_lo, 0.f);  // log2(P_d / P_t)
     return et * one_minus_exp2(delta);
@@ -689,13 +693,14 @@ template <int DT>
 __device__ __forceinline__ float vec_weights(const Record& r, const uint4& t, const uint4& dv,
                                              bool two) {
   using E = Elem<DT>;
-  const unsigned long long mm = pk2(r.mt, r.mt), kk = pk2(r.kf, r.kf);
+  const float c1 = -(r.mt * r.kf);
+  const unsigned long long cc = pk2(c1, c1), kk = pk2(r.kf, r.kf);
   unsigned long long acc = pk2(0.f, 0.f);
 #pragma unroll
   for (int q = 0; q < E::PAIRS; ++q) {
     const unsigned long long lt = E::pair(t, q);
     float a, b;
-    upk2(mul2(sub2(lt, mm), kk), a, b);
+    upk2(fma2(lt, kk, cc), a, b);
     const unsigned long long et = pk2(ex2(a), ex2(b));
     if (two) {
       const unsigned long long ch = pk2(r.c0_hi, r.c0_hi), cl = pk2(r.c0_lo, r.c0_lo);
@@ -704,8 +709,7 @@ __device__ __forceinline__ float vec_weights(const Record& r, const uint4& t, co
       d0 = fminf(d0, 0.f);
       d1 = fminf(d1, 0.f);
       const unsigned long long dd = pk2(d0, d1);
-      unsigned long long p = pk2(OMC7, OMC7);
-      p = fma2(p, dd, pk2(OMC6, OMC6));
+      unsigned long long p = pk2(OMC6, OMC6);
       p = fma2(p, dd, pk2(OMC5, OMC5));
       p = fma2(p, dd, pk2(OMC4, OMC4));
       p = fma2(p, dd, pk2(OMC3, OMC3));
