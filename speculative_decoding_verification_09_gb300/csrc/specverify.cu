@@ -69,7 +69,7 @@ struct Geo {
   // the mbarrier's phase parity unambiguous.
   static_assert(NCW % NG_ == 0 && NS_ % NG_ == 0, "groups");
 };
-using GeoReduce = Geo<2, 8, 14336>;    // phase 1: two groups of 7 warps, 8 slots of 28 KB
+using GeoReduce = Geo<2, 4, 24576>;    // phase 1: two groups of 7 warps, 4 slots of 48 KB
 using GeoResidual = Geo<1, 3, 32768>;  // phase 2: one group of 14 warps, 3 slots of 64 KB
 constexpr int CH1_MIN = 1024;          // smallest phase-1 chunk (elements)
 constexpr int CH2_F32 = GeoResidual::HALF / 4;  // phase-2 chunk for fp32 (the workspace bound)
