@@ -261,6 +261,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
       : "memory");
 }
 
+// Programmatic dependent launch: the next kernel of the call may be launched
+// (and run what does not read this kernel's outputs) before this one ends;
+// it waits for this kernel's completion, with its memory visible, before
+// reading any of it.
+__device__ __forceinline__ void allow_next_kernel() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_previous_kernel() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(const Params& P, int bits) {
   if (bits && P.status) atomicOr(P.status, bits);
 }
@@ -856,6 +867,9 @@ __device__ void consumer(const Params& P, SmemCtl<GeoReduce>& C, const unsigned 
 template <int DT, bool GREEDY>
 __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
   using G = GeoReduce;
+  // every CTA of this grid is resident from the start (one per SM), so the
+  // decide kernel's CTAs may take the SMs' spare room at once
+  allow_next_kernel();
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* slots = smem;
   SmemCtl<G>& C = *reinterpret_cast<SmemCtl<G>*>(smem + size_t(G::NS) * G::SLOT);
@@ -1096,6 +1110,9 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
     }
   }
   const float kf = GREEDY ? 0.f : LOG2E_F / __ldg(P.temp + b);
+  // the loads above read only the call's inputs; the partials come from the
+  // reduce kernel
+  wait_previous_kernel();
   for (int i = warp; i < R; i += DECIDE_WARPS) {
     const Partial* pp = P.part + (size_t(b) * R + i) * size_t(P.np1);
     if (GREEDY) {
@@ -1137,6 +1154,9 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
   }
   // greedy verification ends here: the workspace is ready for the next call
   if (last && b == 0 && threadIdx.x == 0) P.ctrl->state = 0ull;
+  // only now: the residual kernel's CTAs need whole SMs, which this grid's
+  // CTAs still waiting to be placed must not lose to them
+  allow_next_kernel();
 }
 
 // ------------------------------------------------------------ residual
@@ -1182,22 +1202,27 @@ __device__ void span_mass(const Record& r, const unsigned char* trow, const unsi
   warp_sum_ff(mh, ml);
 }
 
-// Residual producer (one lane): this CTA's contiguous range of phase-2 chunks
-// (chunk t % nch2 of request t / nch2); chunks of invalid requests are
-// skipped.  Each slot gets the chunk of target row k (gamma for the bonus),
-// the draft row k chunk after a rejection, and the request's record.
+// Residual producer (one lane): phase-2 chunks t = x, x + G, x + 2G, ... (CTA
+// x of G; chunk t % nch2 of request t / nch2), interleaved so that every CTA
+// gets a similar mix of rejections (a target and a draft chunk) and bonus
+// draws (a target chunk); chunks of invalid requests are skipped.  Each slot
+// gets the chunk of target row k (gamma for the bonus), the draft row k chunk
+// after a rejection, and the request's record.  The next chunk's (k, mode)
+// is loaded one chunk ahead.
 template <int DT>
 __device__ void producer_res(const Params& P, SmemCtl<GeoResidual>& C, unsigned char* slots) {
   using E = Elem<DT>;
   using G = GeoResidual;
   constexpr int NS = G::NS, SLOT = G::SLOT, HALF = G::HALF;
-  const long long T = (long long)P.B * P.nch2, nb = gridDim.x;
-  const long long t0 = T * blockIdx.x / nb, t1 = T * (blockIdx.x + 1) / nb;
-  int b = int(t0 / P.nch2), c = int(t0 - (long long)b * P.nch2);
-  int2 km = __ldg(reinterpret_cast<const int2*>(P.rec + b));  // (k, mode)
-  int2 km_next = b + 1 < P.B ? __ldg(reinterpret_cast<const int2*>(P.rec + b + 1)) : km;
+  const long long T = (long long)P.B * P.nch2, stride = gridDim.x;
+  long long t = blockIdx.x;
+  auto km_of = [&](long long tt) {
+    return tt < T ? __ldg(reinterpret_cast<const int2*>(P.rec + tt / P.nch2)) : make_int2(0, 0);
+  };
+  int2 km = km_of(t), km_next = km_of(t + stride);
   long long seq = 0;
-  for (long long t = t0; t < t1; ++t) {
+  for (; t < T; t += stride) {
+    const int b = int(t / P.nch2), c = int(t - (long long)b * P.nch2);
     if (km.y == MODE_REJECT || km.y == MODE_BONUS) {
       const int s = int(seq % NS);
       const unsigned use = unsigned(seq / NS);
@@ -1225,12 +1250,8 @@ __device__ void producer_res(const Params& P, SmemCtl<GeoResidual>& C, unsigned 
                  &C.full[s]);
       bulk_g2s(&d.rec, P.rec + b, unsigned(sizeof(Record)), &C.full[s]);
     }
-    if (++c == P.nch2) {
-      c = 0;
-      ++b;
-      km = km_next;
-      if (b + 1 < P.B) km_next = __ldg(reinterpret_cast<const int2*>(P.rec + b + 1));
-    }
+    km = km_next;
+    km_next = km_of(t + 2 * stride);
   }
   end_markers(P, C, seq);
 }
@@ -1318,6 +1339,7 @@ __device__ void consumer_res(const Params& P, SmemCtl<GeoResidual>& C,
 template <int DT>
 __global__ void __launch_bounds__(NTHR, 1) sv_residual(const Params P) {
   using G = GeoResidual;
+  allow_next_kernel();  // one CTA per SM: every CTA of this grid is resident
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* slots = smem;
   SmemCtl<G>& C = *reinterpret_cast<SmemCtl<G>*>(smem + size_t(G::NS) * G::SLOT);
@@ -1329,6 +1351,7 @@ __global__ void __launch_bounds__(NTHR, 1) sv_residual(const Params P) {
     }
   }
   __syncthreads();
+  wait_previous_kernel();  // the decision records
   if (threadIdx.x < 32) {
     if (threadIdx.x == 0) producer_res<DT>(P, C, slots);
   } else {
@@ -1390,6 +1413,7 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
   __shared__ FF sh_rest, sh_before;
   __shared__ int sh_q, sh_wsel;
   const int b = int(blockIdx.x), warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
+  wait_previous_kernel();  // the masses (and, before them, the records)
   Record r;
   {
     const int4* src = reinterpret_cast<const int4*>(P.rec + b);
@@ -1666,6 +1690,25 @@ int device_info(int& sms) {
 
 int round_up(long long x, int m) { return int(((x + m - 1) / m) * m); }
 
+// Launch a kernel that follows another of the same call with programmatic
+// stream serialisation: it may start before its predecessor ends and waits
+// for it on the device (wait_previous_kernel).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                         cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const float* u_acc,
            const float* u_res, const float* temp, int B, int gamma, int V, int dtype,
            int32_t* out_tokens, int32_t* out_n, float* out_p, float* out_Z, void* ws,
@@ -1739,40 +1782,36 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
     if (j < tu.stage_n) cudaEventRecord(tu.stage_ev[j], st);
   };
   mark(0);
+  cudaError_t e = cudaSuccess;
+  auto run = [&](auto reduce_k, auto decide_k, auto residual_k, auto draw_k) {
+    reduce_k<<<grid, NTHR, smem_bytes<GeoReduce>(), st>>>(P);
+    e = cudaGetLastError();
+    mark(1);
+    if (e == cudaSuccess)
+      e = launch_after(decide_k, unsigned(B), 32 * DECIDE_WARPS, 0, st, P, greedy);
+    mark(2);
+    if (greedy) return;
+    if (e == cudaSuccess) e = launch_after(residual_k, gres, NTHR, smem_bytes<GeoResidual>(), st, P);
+    mark(3);
+    if (e == cudaSuccess) e = launch_after(draw_k, unsigned(B), 32 * DRAW_WARPS, 0, st, P);
+    mark(4);
+  };
   if (dtype == SV_F32) {
-    if (greedy) {
-      sv_reduce<SV_F32, true><<<grid, NTHR, smem_bytes<GeoReduce>(), st>>>(P);
-      mark(1);
-      sv_decide<SV_F32, true><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, true);
-      mark(2);
-    } else {
-      sv_reduce<SV_F32, false><<<grid, NTHR, smem_bytes<GeoReduce>(), st>>>(P);
-      mark(1);
-      sv_decide<SV_F32, false><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, false);
-      mark(2);
-      sv_residual<SV_F32><<<gres, NTHR, smem_bytes<GeoResidual>(), st>>>(P);
-      mark(3);
-      sv_draw<SV_F32><<<unsigned(B), 32 * DRAW_WARPS, 0, st>>>(P);
-      mark(4);
-    }
+    if (greedy)
+      run(sv_reduce<SV_F32, true>, sv_decide<SV_F32, true>, sv_residual<SV_F32>, sv_draw<SV_F32>);
+    else
+      run(sv_reduce<SV_F32, false>, sv_decide<SV_F32, false>, sv_residual<SV_F32>,
+          sv_draw<SV_F32>);
   } else {
-    if (greedy) {
-      sv_reduce<SV_BF16, true><<<grid, NTHR, smem_bytes<GeoReduce>(), st>>>(P);
-      mark(1);
-      sv_decide<SV_BF16, true><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, true);
-      mark(2);
-    } else {
-      sv_reduce<SV_BF16, false><<<grid, NTHR, smem_bytes<GeoReduce>(), st>>>(P);
-      mark(1);
-      sv_decide<SV_BF16, false><<<unsigned(B), 32 * DECIDE_WARPS, 0, st>>>(P, false);
-      mark(2);
-      sv_residual<SV_BF16><<<gres, NTHR, smem_bytes<GeoResidual>(), st>>>(P);
-      mark(3);
-      sv_draw<SV_BF16><<<unsigned(B), 32 * DRAW_WARPS, 0, st>>>(P);
-      mark(4);
-    }
+    if (greedy)
+      run(sv_reduce<SV_BF16, true>, sv_decide<SV_BF16, true>, sv_residual<SV_BF16>,
+          sv_draw<SV_BF16>);
+    else
+      run(sv_reduce<SV_BF16, false>, sv_decide<SV_BF16, false>, sv_residual<SV_BF16>,
+          sv_draw<SV_BF16>);
   }
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
 }
 
 }  // namespace
