@@ -70,7 +70,7 @@ struct Geo {
   static_assert(NCW % NG_ == 0 && NS_ % NG_ == 0, "groups");
 };
 using GeoReduce = Geo<2, 4, 24576>;    // phase 1: two groups of 7 warps, 4 slots of 48 KB
-using GeoResidual = Geo<1, 3, 32768>;  // phase 2: one group of 14 warps, 3 slots of 64 KB
+using GeoResidual = Geo<1, 2, 49152>;  // phase 2: one group of 14 warps, 2 slots of 96 KB
 constexpr int CH1_MIN = 1024;          // smallest phase-1 chunk (elements)
 constexpr int CH2_F32 = GeoResidual::HALF / 4;  // phase-2 chunk for fp32 (the workspace bound)
 constexpr unsigned SUSPEND_HINT_NS = 1000000u;  // a waiting warp sleeps until the phase completes
@@ -1413,6 +1413,10 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
   __shared__ FF sh_rest, sh_before;
   __shared__ int sh_q, sh_wsel;
   const int b = int(blockIdx.x), warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int R = P.R, V = P.V;
+  // every uniform of the request (only entry k is used): an input, loaded
+  // before the wait
+  const float u_lane = lane < R ? __ldg(P.u_res + size_t(b) * R + lane) : 0.f;
   wait_previous_kernel();  // the masses (and, before them, the records)
   Record r;
   {
@@ -1421,14 +1425,26 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
     dst[0] = __ldg(src); dst[1] = __ldg(src + 1); dst[2] = __ldg(src + 2);
   }
   const bool last_cta = blockIdx.x == 0;
+  const int nq = P.nch2 * GW;
+  const Mass* ms = P.mass + size_t(b) * P.nch2 * GW;
+  // 1a. the masses of this warp's run, loaded beside the record
+  const int run = (nq + DRAW_WARPS - 1) / DRAW_WARPS;
+  const int qa = min(nq, warp * run), qb = min(nq, qa + run);
+  FF mq[DRAW_RUN];  // this lane's masses q = qa + lane + 32 j
+#pragma unroll
+  for (int j = 0; j < DRAW_RUN; ++j) {
+    const int q = qa + lane + 32 * j;
+    mq[j] = ff(0.f);
+    if (q < qb) {
+      const Mass m = ms[q];
+      mq[j] = ff(m.hi, m.lo);
+    }
+  }
   if (r.mode == MODE_INVALID) {
     if (last_cta && threadIdx.x == 0) P.ctrl->state = 0ull;
     return;
   }
-  const int R = P.R, V = P.V;
-  const int nq = P.nch2 * GW;
-  const Mass* ms = P.mass + size_t(b) * P.nch2 * GW;
-  const float u = __ldg(P.u_res + size_t(b) * R + r.k);
+  const float u = __shfl_sync(0xffffffffu, u_lane, r.k & 31) ;
   const int rowk = (r.mode == MODE_BONUS) ? P.gamma : r.k;
   const unsigned char* trow = P.Lt + (size_t(b) * R + rowk) * size_t(V) * E::ES;
   bool two = (r.mode == MODE_REJECT);
@@ -1460,23 +1476,12 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
   };
 
   // 1. runs of sub-ranges: warp w takes [w * run, (w + 1) * run)
-  const int run = (nq + DRAW_WARPS - 1) / DRAW_WARPS;
-  const int qa = min(nq, warp * run), qb = min(nq, qa + run);
   bool degenerate = false;
-  FF mq[DRAW_RUN];  // this lane's masses q = qa + lane + 32 j
   FF tot = ff(0.f);
-  auto load_masses = [&]() {
+  auto load_masses = [&]() {  // the rest of the run, and the run's sum
     tot = ff(0.f);
 #pragma unroll
-    for (int j = 0; j < DRAW_RUN; ++j) {
-      const int q = qa + lane + 32 * j;
-      mq[j] = ff(0.f);
-      if (q < qb) {
-        const Mass m = ms[q];
-        mq[j] = ff(m.hi, m.lo);
-      }
-      tot = tot + mq[j];
-    }
+    for (int j = 0; j < DRAW_RUN; ++j) tot = tot + mq[j];
     for (int q = qa + lane + 32 * DRAW_RUN; q < qb; q += 32) {  // runs beyond 32 * DRAW_RUN
       const Mass m = ms[q];
       tot = tot + ff(m.hi, m.lo);
