@@ -421,5 +421,109 @@ int svo_greedy(int dtype, const void* Lt, const int32_t* x, int B, int gamma, in
   return 0;
 }
 
+/* ---------------------------------------------------------------- draft side
+ * Draft-token sampling, the step before verification.  [SD-overview] 考点2
+ * and 第三章: the token x that verification tests is one the draft model
+ * SAMPLED from its own distribution P_draft.  Here each draft row is sampled
+ * from its tempered softmax (reading R7 for the temperature) by the same
+ * index-order inverse CDF as the bonus token (reading R5), and the row's
+ * normaliser is reported with it, so that verification can reuse it:
+ *   m = the largest stored logit of the row,
+ *   S = sum_v exp((l_v - m) / T),  P_draft[v] = exp((l_v - m) / T) / S.
+ * Rows with NaN / +inf / only -inf, or a bad temperature, are invalid
+ * (reading R8): token -1, m = S = NaN. */
+typedef struct {
+  int dtype;
+  const void* L;
+  const float *u, *temp;
+  int B, n, V;
+  int32_t* out_tokens;
+  double *out_m, *out_S, *out_dist;
+  int32_t* out_flags;
+  double near_eps;
+  int r0, r1; /* rows b * n + i in [r0, r1) */
+} draft_job;
+
+static void* draft_worker(void* arg) {
+  const draft_job* J = (const draft_job*)arg;
+  const int V = J->V;
+  double* P = (double*)malloc((size_t)V * sizeof(double));
+  for (int r = J->r0; r < J->r1; ++r) {
+    const int b = r / J->n;
+    const size_t off = (size_t)r * V;
+    J->out_tokens[r] = -1;
+    J->out_m[r] = J->out_S[r] = NAN;
+    if (J->out_dist) J->out_dist[r] = INFINITY;
+    if (!P) { J->out_flags[r] = -1; continue; }
+    const double T = (double)J->temp[b];
+    if (!(isfinite(T) && T >= 0x1p-126)) { /* reading R7 */
+      J->out_flags[r] = SVO_INVALID_TEMP;
+      continue;
+    }
+#if SVO_MUTANT == 11
+    const double Ts = 1.0; /* planted: the draft sample ignores the temperature */
+#else
+    const double Ts = T;
+#endif
+    if (!softmax_row(J->L, J->dtype, off, V, Ts, P)) {
+      J->out_flags[r] = SVO_INVALID_NONFINITE;
+      continue;
+    }
+    /* the normaliser, from its definition */
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+      const double l = load_logit(J->L, J->dtype, off + (size_t)v);
+      if (l > m) m = l;
+    }
+    double S = 0.0;
+    for (int v = 0; v < V; ++v) S += exp((load_logit(J->L, J->dtype, off + (size_t)v) - m) / T);
+    double Z = 0.0;
+    for (int v = 0; v < V; ++v) Z += P[v];
+    int near = 0;
+    double dist = INFINITY;
+    J->out_tokens[r] = inverse_cdf(P, V, Z, (double)J->u[r], J->near_eps, &near, &dist);
+    J->out_m[r] = m;
+    J->out_S[r] = S;
+    if (J->out_dist) J->out_dist[r] = dist;
+    J->out_flags[r] = near ? SVO_NEAR_SAMPLE : 0;
+  }
+  free(P);
+  return NULL;
+}
+
+/* Draft-sampling oracle.  L [B][n][V] (fp32 or bf16 bits), u [B][n] in
+ * [0, 1), temp [B].  Outputs [B][n]: out_tokens, out_m, out_S, out_flags
+ * (SVO_* bits), out_dist optional (distance of u to the nearer CDF edge of
+ * the chosen token).  Returns 0, or -1 on a bad argument. */
+int svo_draft_sample(int dtype, const void* L, const float* u, const float* temp, int B, int n,
+                     int V, int32_t* out_tokens, double* out_m, double* out_S,
+                     double* out_dist, int32_t* out_flags, double near_eps, int nthreads) {
+  if (B < 0 || n < 0 || V < 1 || (dtype != SVO_F32 && dtype != SVO_BF16)) return -1;
+  const int rows = B * n;
+  if (rows == 0) return 0;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > rows) nthreads = rows;
+  draft_job* jobs = (draft_job*)calloc((size_t)nthreads, sizeof(draft_job));
+  pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  for (int t = 0; t < nthreads; ++t) {
+    draft_job* J = &jobs[t];
+    J->dtype = dtype; J->L = L; J->u = u; J->temp = temp;
+    J->B = B; J->n = n; J->V = V;
+    J->out_tokens = out_tokens; J->out_m = out_m; J->out_S = out_S; J->out_dist = out_dist;
+    J->out_flags = out_flags;
+    J->near_eps = near_eps;
+    J->r0 = (int)((long long)rows * t / nthreads);
+    J->r1 = (int)((long long)rows * (t + 1) / nthreads);
+  }
+  for (int t = 1; t < nthreads; ++t) pthread_create(&th[t], NULL, draft_worker, &jobs[t]);
+  draft_worker(&jobs[0]);
+  for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
+  free(jobs);
+  free(th);
+  for (int r = 0; r < rows; ++r)
+    if (out_flags[r] < 0) return -2;
+  return 0;
+}
+
 /* Build-identity hook for the mutation tests. */
 int svo_mutant_id(void) { return SVO_MUTANT; }

@@ -398,3 +398,233 @@ ALL_PINS = [pin_worked_example, pin_numpy_operator_vectors, pin_expected_tokens,
             pin_losslessness_chisq, pin_brute_force_tiny, pin_accept_boundary,
             pin_inverse_cdf_strict, pin_softmax_textbook, pin_degenerate_shapes,
             pin_invalid_inputs, pin_greedy]
+
+
+# ------------------------------------------------------- draft-row sampling
+
+def _bf16_bits(a):
+    """fp32 values -> bf16 bit patterns (truncation; the test's rows are
+    built from these exact values)."""
+    return (np.ascontiguousarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _bf16_wide(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def pin_draft_sample_grid(lib):
+    """考点2: the draft token is a sample of P_draft.  Brute force at V=5 over
+    a u grid, fp32 and bf16 rows, T = 0.6: away from CDF edges the token is
+    np.searchsorted(cumsum(P), u * sum(P), 'right') with P the textbook
+    softmax(l / T); token frequencies are P within 1/n; m is the largest
+    stored logit and S = sum exp((l - m) / T)."""
+    rng = np.random.default_rng(21)
+    V, n = 5, 10000
+    T = float(np.float32(0.6))
+    ug = _midgrid(n)
+    for dt in (F32, BF16):
+        l32 = rng.normal(0, 1.3, size=V).astype(np.float32)
+        if dt == BF16:
+            stored = _bf16_bits(l32)
+            wide = _bf16_wide(stored)
+        else:
+            stored = l32
+            wide = l32.astype(np.float64)
+        L = np.ascontiguousarray(np.broadcast_to(stored, (n // 10, 10, V)))
+        out = oracle.draft_sample(L, ug.reshape(n // 10, 10), np.full(n // 10, T, np.float32),
+                                  dt, lib=lib)
+        P = softmax(wide / T)
+        cum = np.cumsum(P)
+        u64 = ug.astype(np.float64)
+        want = np.searchsorted(cum, u64 * cum[-1], side="right")
+        nearb = np.min(np.abs(cum[None, :] / cum[-1] - u64[:, None]), 1) < 1e-6
+        got = out["tokens"].reshape(-1)
+        assert np.array_equal(got[~nearb], want[~nearb])
+        freq = np.bincount(got, minlength=V) / n
+        assert np.all(np.abs(freq - P) <= 1.0 / n + 1e-12)
+        m = wide.max()
+        assert np.all(out["m"] == m)
+        assert np.allclose(out["S"], np.exp((wide - m) / T).sum(), rtol=1e-13, atol=0)
+        assert np.all(out["flags"] & oracle.INVALID_ANY == 0)
+    # ln p logits at T = 1: S = 1 / max p, m = ln max p + c
+    p = rng.dirichlet(np.ones(7))
+    c = 3.0
+    L = (np.log(p) + c).astype(np.float32).reshape(1, 1, 7)
+    out = oracle.draft_sample(L, np.array([[0.5]], np.float32), np.ones(1, np.float32), F32,
+                              lib=lib)
+    wide = L.astype(np.float64).reshape(-1)
+    assert out["m"][0, 0] == wide.max()
+    assert abs(out["S"][0, 0] - np.exp(wide - wide.max()).sum()) < 1e-13 * out["S"][0, 0]
+    assert abs(out["S"][0, 0] * p.max() - 1.0) < 1e-6  # fp32 rounding of ln p + c
+
+
+def pin_draft_then_verify_lossless(lib, trials=400_000):
+    """考点2 identity with the draft tokens drawn by the draft-sampling oracle
+    (T = 1.4): the token emitted at position 0 follows P_target[0], and the
+    drafts follow P_draft.  Chi-square, 7 degrees of freedom, rejected above
+    24.32 (p = 0.001)."""
+    rng = np.random.default_rng(77)
+    V, gamma = 8, 2
+    T = float(np.float32(1.4))
+    lt = rng.normal(0, 1.5, size=(gamma + 1, V)).astype(np.float32)
+    ld = rng.normal(0, 1.5, size=(gamma, V)).astype(np.float32)
+    Pt = softmax(lt.astype(np.float64) / T, axis=1)
+    Pd = softmax(ld.astype(np.float64) / T, axis=1)
+    Ld = np.ascontiguousarray(np.broadcast_to(ld, (trials, gamma, V)))
+    temp = np.full(trials, T, np.float32)
+    ds = oracle.draft_sample(Ld, rng.random((trials, gamma), dtype=np.float32), temp, F32,
+                             lib=lib)
+    x = ds["tokens"]
+    for i in range(gamma):
+        obs = np.bincount(x[:, i], minlength=V)
+        chi2 = float(((obs - Pd[i] * trials) ** 2 / (Pd[i] * trials)).sum())
+        assert chi2 < 24.32, ("draft", i, chi2)
+    Lt = np.ascontiguousarray(np.broadcast_to(lt, (trials, gamma + 1, V)))
+    out = oracle.verify(Lt, Ld, x, rng.random((trials, gamma), dtype=np.float32),
+                        rng.random((trials, gamma + 1), dtype=np.float32), temp, F32, lib=lib)
+    obs = np.bincount(out["tokens"][:, 0], minlength=V)
+    chi2 = float(((obs - Pt[0] * trials) ** 2 / (Pt[0] * trials)).sum())
+    assert chi2 < 24.32, ("emitted", chi2)
+
+
+def pin_draft_sample_invalid(lib):
+    """Readings R7/R8 on the draft side: a NaN or +inf logit, an all -inf row
+    or a bad temperature gives token -1 and NaN statistics for that row only;
+    a row with some -inf entries is legal and never emits them."""
+    rng = np.random.default_rng(31)
+    B, n, V = 4, 3, 9
+    L = rng.normal(0, 1, size=(B, n, V)).astype(np.float32)
+    L[0, 1, 4] = np.nan
+    L[0, 2, 0] = np.inf
+    L[1, 0, :] = -np.inf
+    L[2, :, 1::2] = -np.inf
+    T = np.array([1.0, 1.0, 0.9, 0.0], np.float32)
+    u = rng.random((B, n), dtype=np.float32)
+    out = oracle.draft_sample(L, u, T, F32, lib=lib)
+    bad = np.zeros((B, n), bool)
+    bad[0, 1] = bad[0, 2] = bad[1, 0] = True
+    bad[3, :] = True
+    assert np.all(out["tokens"][bad] == -1) and np.all(np.isnan(out["S"][bad]))
+    assert np.all(out["flags"][0, 1:] & oracle.INVALID_NONFINITE)
+    assert out["flags"][1, 0] & oracle.INVALID_NONFINITE
+    assert np.all(out["flags"][3] & oracle.INVALID_TEMP)
+    assert np.all(out["tokens"][~bad] >= 0)
+    assert np.all(out["tokens"][2] % 2 == 0)
+
+
+# ---------------------------------------------------- sink + ring KV cache
+
+def pin_kv_slot_closed_form(lib):
+    """Deferred-speculation page, "环形上下文与注意力沉淀机制": Slot(pos) is
+    pos inside the S sink slots; past them, W consecutive positions fill the
+    W ring slots S .. S+W-1 once each, and a position W later reuses the
+    slot."""
+    for S in (0, 1, 4):
+        for W in (1, 3, 8):
+            for p in range(S):
+                assert oracle.kv_slot(p, S, W, lib=lib) == p
+            assert oracle.kv_slot(S, S, W, lib=lib) == S
+            for p0 in range(S, S + 3 * W):
+                slots = sorted(oracle.kv_slot(p, S, W, lib=lib) for p in range(p0, p0 + W))
+                assert slots == list(range(S, S + W))
+                assert oracle.kv_slot(p0 + W, S, W, lib=lib) == oracle.kv_slot(p0, S, W, lib=lib)
+
+
+def pin_kv_commit_content(lib):
+    """The cache after a run of verification steps holds exactly what a plain
+    model of a sink + sliding window holds: the first S positions, then the
+    last W committed ones (a deque of length W), oldest first, read through
+    the valid-slot list.  Each step commits k + 1 staged entries (the last
+    emitted token and k accepted drafts, reading K1); entries of rejected
+    drafts are never visible.  Every KV row carries a tag of its position."""
+    from collections import deque
+    rng = np.random.default_rng(41)
+    B, LH, gamma, S, W = 3, 2, 3, 4, 6
+    R = gamma + 1
+    C = S + W
+    kp = np.full((B, LH, C, 2), -99, np.int32)
+    vp = kp.copy()
+    pos = np.zeros(B, np.int32)
+    models = [([], deque(maxlen=W)) for _ in range(B)]
+    for step in range(12):
+        k = rng.integers(-1, R, size=B).astype(np.int32)  # -1: a dropped request
+        kn = np.empty((B, LH, R, 2), np.int32)
+        for b in range(B):
+            for j in range(R):
+                tag = pos[b] + j if (k[b] >= 0 and j <= k[b]) else -1000 - j
+                kn[b, :, j, 0] = tag
+                kn[b, :, j, 1] = np.arange(LH) + 100 * b
+        vn = kn.copy()
+        vn[..., 0] = -vn[..., 0] - 1
+        out = oracle.kv_commit(kp, vp, kn, vn, k, pos, S, W, lib=lib)
+        kp, vp = out["k_pool"], out["v_pool"]
+        for b in range(B):
+            for j in range(int(k[b]) + 1):
+                sinks, ring = models[b]
+                p = int(pos[b]) + j
+                (sinks if p < S else ring).append(p)
+        pos = pos + np.maximum(k + 1, 0)
+        assert np.array_equal(out["pos"], pos)
+        assert np.all(out["flags"] == 0)
+        vs = oracle.kv_valid_slots(pos, S, W, lib=lib)
+        for b in range(B):
+            sinks, ring = models[b]
+            want = sinks + list(ring)
+            n = int(vs["len"][b])
+            assert n == len(want) == min(int(pos[b]), C)
+            sl = vs["slots"][b, :n]
+            assert len(set(sl.tolist())) == n and np.all(vs["slots"][b, n:] == -1)
+            for lh in range(LH):
+                assert np.array_equal(kp[b, lh, sl, 0], want)
+                assert np.array_equal(vp[b, lh, sl, 0], [-t - 1 for t in want])
+                assert np.all(kp[b, lh, sl, 1] == lh + 100 * b)
+    # k past the staged entries is invalid and writes nothing
+    out = oracle.kv_commit(kp, vp, kn, vn, np.array([R, 0, 0], np.int32), pos, S, W, lib=lib)
+    assert out["flags"][0] == oracle.KV_INVALID and out["pos"][0] == pos[0]
+    assert np.array_equal(out["k_pool"][0], kp[0])
+
+
+# ------------------------------------------------ draft KV window block table
+
+def pin_window_block_table(lib):
+    """Draft KV sliding-window page: the unit-test example of "block table 的
+    裁剪方式" ([10, 60, 200, 64] -> [10, 60, 72, 64] at W = 64, K = 3, block 16),
+    the bounds of "窗口数学" (block-aligned start, windowed length <= W + b - 1,
+    the window reaching back to seq + K - W; the clone's width is the page's
+    W / b + 1, widened to ceil((W + b - 1) / b) where that is larger, reading
+    K4), and what
+    the clone is for: every position p in [start, seq) maps through the clone
+    to the block the full table gives it, and columns past `needed` are 0."""
+    g = _golden("draft_window_example.json")
+    blk = g["block_size"]
+    table = np.arange(4 * 16, dtype=np.int32).reshape(4, 16) + 1000
+    out = oracle.window_block_table(g["seq_lens"], table, g["W"], blk, g["K"], lib=lib)
+    assert list(out["seq"]) == g["windowed_seq_lens"]
+    rng = np.random.default_rng(51)
+    for W, blk, K in ((64, 16, 3), (100, 16, 0), (7, 4, 2), (32, 32, 5), (5, 1, 1)):
+        B, full = 40, rng.integers(1, 30)
+        seq = rng.integers(0, min(full * blk + 1, 1 << 20), size=B).astype(np.int32)
+        seq[:3] = [0, 1, full * blk]
+        table = rng.integers(1, 1 << 30, size=(B, full)).astype(np.int32)
+        out = oracle.window_block_table(seq, table, W, blk, K, lib=lib)
+        mc = max(W // blk + 1, -(-(W + blk - 1) // blk))
+        assert out["table"].shape == (B, mc)
+        for b in range(B):
+            s_ = int(seq[b])
+            start = int(out["start_block"][b]) * blk
+            lo = max(s_ + K - W, 0)
+            assert start % blk == 0 and start <= lo < start + blk
+            assert int(out["seq"][b]) == s_ - start
+            assert s_ - start <= W + blk - 1 or start == 0
+            need = int(out["needed"][b])
+            assert need == -(-(s_ - start) // blk) <= mc
+            for p in range(start, s_):
+                assert out["table"][b, (p - start) // blk] == table[b, p // blk]
+            assert np.all(out["table"][b, need:] == 0)
+    bad = oracle.window_block_table([-1, 5], np.ones((2, 3), np.int32), 8, 4, 0, lib=lib)
+    assert bad["flags"][0] == oracle.KV_INVALID and bad["seq"][0] == 0
+    assert np.all(bad["table"][0] == 0) and bad["flags"][1] == 0
+
+
+ALL_PINS += [pin_draft_sample_grid, pin_draft_then_verify_lossless, pin_draft_sample_invalid,
+             pin_kv_slot_closed_form, pin_kv_commit_content, pin_window_block_table]

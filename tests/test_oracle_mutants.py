@@ -5,7 +5,10 @@ plausible mistake: the residual over raw logits (as the C++ scheduler snippet
 of the deferred-speculation page has it), a strict accept test, no bonus
 token, no temperature on the draft row, '>=' in the inverse CDF, resampling
 from the wrong row, swapped residual operands, no max shift in the softmax, a
-dropped softmax term, and a greedy tie broken to the last index.
+dropped softmax term, a greedy tie broken to the last index, a draft sample
+without the temperature, a ring slot without the sink offset, a KV commit
+that drops the last emitted token's entry, a draft window start not aligned
+to a block, and a block-table clone not zeroed past `needed`.
 """
 import pytest
 
@@ -23,6 +26,11 @@ MUTANTS = {
     8: "softmax without the max shift",
     9: "softmax sum drops the last term",
     10: "greedy tie goes to the last index",
+    11: "draft sample ignores the temperature",
+    12: "ring slot without the sink offset",
+    13: "KV commit drops the last emitted token's entry",
+    14: "draft window start not block-aligned",
+    15: "block-table clone not zeroed past needed",
 }
 
 
