@@ -174,6 +174,60 @@ def run_reference(args) -> None:
     }))
 
 
+def measure_draft_side(binding, torch, dev, stream, sets, host_sets, B, g, V, ws, out_tok, out_n,
+                       status, steps, warmup, peak) -> dict:
+    """The steps beside verification on the same workload, each timed alone
+    over `steps` calls (input sets rotating, CUDA events on the stream):
+    sv_draft_sample over the B * gamma draft rows, and spec_verify_cached
+    with the normalisers it produced (the draft rows are then not streamed)."""
+    es = synth.ELEM_BYTES[host_sets[0].dtype]
+    u = [torch.from_numpy(synth.draft_uniforms(B, g, 7000 + i)).to(dev) for i in range(len(sets))]
+    tok = [torch.empty(B, g, dtype=torch.int32, device=dev) for _ in sets]
+    stats = [torch.empty(B, g, 2, dtype=torch.float32, device=dev) for _ in sets]
+    dws = binding.make_draft_workspace(B, g, V, dev)
+
+    def draft(i):
+        binding.sv_draft_sample(sets[i]["Ld"], u[i], sets[i]["temp"], tok[i], stats[i], dws,
+                                dev_status=status, stream=stream)
+
+    def cached(i):
+        t = sets[i]
+        binding.spec_verify_cached(t["Lt"], t["Ld"], tok[i], stats[i], t["u_acc"], t["u_res"],
+                                   t["temp"], out_tok, out_n, ws, dev_status=status,
+                                   stream=stream)
+
+    def timed(fn):
+        for i in range(warmup):
+            fn(i % len(sets))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for i in range(steps):
+            fn(i % len(sets))
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / steps
+
+    for i in range(len(sets)):  # every set's draft tokens and normalisers exist before timing
+        draft(i)
+    d_ms = timed(draft)
+    c_ms = timed(cached)
+    d_bytes = B * g * V * es
+    c_bytes = B * (g + 1) * V * es
+    return {
+        "sv_draft_sample": {
+            "ms_per_call": d_ms, "rows_per_s": B * g / (d_ms / 1e3),
+            "logit_bytes": d_bytes, "call_gbs": d_bytes / (d_ms / 1e3) / 1e9,
+            "frac_of_peak": d_bytes / (d_ms / 1e3) / 1e9 / peak, "kernels": 2},
+        "spec_verify_cached": {
+            "ms_per_call": c_ms, "positions_per_s": B * g / (c_ms / 1e3),
+            "streamed_logit_bytes": c_bytes, "call_gbs": c_bytes / (c_ms / 1e3) / 1e9,
+            "kernels": 4},
+        "timing": f"{steps} calls each after {warmup} warm-up calls, CUDA events around the "
+                  "loop, input sets rotating; not part of the headline value",
+    }
+
+
 def run_ours(args) -> None:
     import torch
 
@@ -277,6 +331,10 @@ def run_ours(args) -> None:
                 for j, nm in enumerate(kernel_names)}
     clk = clocks.stop() if not args.no_clocks else None
     total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    peak, peak_kind = read_peaks()
+    draft_side = None if (greedy or args.no_draft_side) else measure_draft_side(
+        binding, torch, dev, stream, sets, host_sets, B, g, V, ws, out_tok, out_n, status,
+        args.steps, args.warmup, peak)
     per_launch = [a.elapsed_time(b) for a, b in ev]
     if pg:
         tt = torch.tensor([total_ms], device=dev)
@@ -287,7 +345,6 @@ def run_ours(args) -> None:
     positions = B * g * ws_n * args.steps
     value = positions / (total_ms / 1e3)
     launch_ms = float(np.mean(per_launch))
-    peak, peak_kind = read_peaks()
     # the dominant kernel is the streaming reduce: it reads every logit once
     achieved = logit_bytes / (reduce_ms / 1e3) / 1e9
 
@@ -362,6 +419,7 @@ def run_ours(args) -> None:
                                "right after the timed loop (same inputs)"},
         "stages_ms_extra_calls": stage_ms, "call_ms": launch_ms,
         "call_equivalent_gbs": logit_bytes / (launch_ms / 1e3) / 1e9,
+        "draft_side": draft_side,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_kern * args.steps, "clocks": clk,
         "status": st, "wall_s_timed": t_wall,
         "tuning": {"chunk": args.chunk},
@@ -384,6 +442,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-draft-side", action="store_true",
+                    help="skip timing sv_draft_sample and spec_verify_cached")
     ap.add_argument("--cpu-requests", type=int, default=256)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="approximate seconds of oracle work for cpu_baseline")

@@ -126,6 +126,56 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
                        int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
                        int32_t* dev_status, void* stream);
 
+/*
+ * Draft-side sampling: the step before verification.  The token x_i that
+ * verification tests is one the draft model sampled from its own distribution
+ * (Speculative Decoding overview page, 考点2 and the NumPy operator of
+ * 第三章).  For every request b and row i < n of
+ *   draft_logits [B][n][V]  dtype (one or more draft positions per request):
+ *     P = softmax(draft_logits[b][i] / T_b)
+ *     token = smallest v with sum_{j<=v} P_j > u_draft[b][i]   (index-order inverse CDF,
+ *             the rule of the bonus token)
+ *     m = max_v draft_logits[b][i][v] (the stored value), S = sum_v exp((l_v - m) / T_b)
+ *   written to out_tokens[b * ncols + col + i] (int32) and
+ *   out_stats[(b * ncols + col + i) * 2 + {0, 1}] = (m, S) (float).
+ * col/ncols let a draft loop write position i of a [B][gamma] token array
+ * one draft step at a time (n = 1, col = i, ncols = gamma) or all positions
+ * at once (n = gamma, col = 0, ncols = gamma).  out_stats so written is the
+ * draft_stats input of spec_verify_cached.
+ *   u_draft [B][n] float in [0, 1); temperature [B] as for spec_verify.
+ *   Requires 1 <= n <= SV_MAX_GAMMA, 0 <= col, col + n <= ncols.
+ *   workspace: sv_draft_workspace_bytes(B, n, V) bytes, prepared as for
+ *   spec_verify (the same workspace may serve both, if large enough for each,
+ *   on one stream).
+ *   A row with NaN / +inf, only -inf, or a bad temperature gets token -1 and
+ *   stats (NaN, NaN); SV_ST_NONFINITE or SV_ST_BAD_TEMP is OR-ed into
+ *   *dev_status.
+ */
+size_t sv_draft_workspace_bytes(int B, int n, int V);
+int sv_draft_sample(const void* draft_logits, const float* u_draft, const float* temperature,
+                    int B, int n, int V, int dtype, int col, int ncols, int32_t* out_tokens,
+                    float* out_stats, void* workspace, size_t workspace_bytes,
+                    int32_t* dev_status, void* stream);
+
+/*
+ * spec_verify with the draft rows' normalisers given: draft_stats
+ * [B][gamma][2] float (8-byte aligned), (m, S) of every draft row as
+ * sv_draft_sample reports them.  The result is spec_verify's; the draft rows
+ * are then read only where needed (the logit of x_i, and row k after a
+ * rejection), so the streaming pass reads (gamma + 1) * V logits per request
+ * instead of (2 * gamma + 1) * V.  Stats that are not finite (or S <= 0)
+ * invalidate the request like a non-finite logit (SV_ST_NONFINITE).  The
+ * stats must belong to these draft rows at this temperature; the library
+ * cannot check that.  out_p and out_Z as for spec_verify_diag (either may be
+ * NULL); gamma == 0 needs no draft_stats.
+ */
+int spec_verify_cached(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, const float* draft_stats,
+                       const float* u_accept, const float* u_resample, const float* temperature,
+                       int B, int gamma, int V, int dtype, int32_t* out_tokens,
+                       int32_t* out_num_accepted, float* out_p, float* out_Z, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, void* stream);
+
 /* Size of the built-in scratch of spec_verify_noalloc: 16 MiB.  Every GPU that
  * loads this library holds this much device memory until the process exits. */
 #define SV_NOALLOC_MAX_WORKSPACE (16u << 20)
@@ -181,7 +231,7 @@ int sv_set_stage_events(void* const* events, int n);
 /* Human-readable name of a host return code. */
 const char* sv_error_string(int code);
 
-/* Library version, major * 10000 + minor * 100 + patch. */
+/* Library version, major * 100 + minor. */
 int sv_version(void);
 
 #ifdef __cplusplus

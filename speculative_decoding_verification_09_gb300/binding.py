@@ -21,7 +21,8 @@ SV_ST_TIMEOUT, SV_ST_WORKSPACE, SV_ST_DEGENERATE = 0x8, 0x10, 0x20
 SV_MAX_GAMMA = 32
 
 EXPORTED = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_diag",
-            "spec_verify_greedy", "spec_verify_noalloc", "sv_set_tuning",
+            "spec_verify_greedy", "spec_verify_noalloc", "spec_verify_cached",
+            "sv_draft_workspace_bytes", "sv_draft_sample", "sv_set_tuning",
             "sv_set_stage_events", "sv_error_string", "sv_version")
 SV_NOALLOC_MAX_WORKSPACE = 16 << 20
 
@@ -47,13 +48,17 @@ def lib() -> ctypes.CDLL:
         L.spec_verify_diag.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, Z, P, P]
         L.spec_verify_greedy.argtypes = [P, P, I, I, I, I, P, P, P, Z, P, P]
         L.spec_verify_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, P, P]
+        L.spec_verify_cached.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, Z, P, P]
+        L.sv_draft_workspace_bytes.argtypes = [I, I, I]
+        L.sv_draft_workspace_bytes.restype = Z
+        L.sv_draft_sample.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, Z, P, P]
         L.sv_set_tuning.argtypes = [I, I, I]
         L.sv_set_stage_events.argtypes = [P, I]
         L.sv_error_string.argtypes = [I]
         L.sv_error_string.restype = ctypes.c_char_p
         for name in ("sv_workspace_init", "spec_verify", "spec_verify_diag",
-                     "spec_verify_greedy", "spec_verify_noalloc", "sv_set_tuning",
-                     "sv_set_stage_events", "sv_version"):
+                     "spec_verify_greedy", "spec_verify_noalloc", "spec_verify_cached",
+                     "sv_draft_sample", "sv_set_tuning", "sv_set_stage_events", "sv_version"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -190,4 +195,60 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, u_accept, u_r
         _dev(temperature, torch.float32, "temperature"), B, g, V, dt,
         _dev(out_tokens, torch.int32, "out_tokens"),
         _dev(out_num_accepted, torch.int32, "out_num_accepted"),
+        _dev(dev_status, torch.int32, "dev_status"), _stream(stream, target_logits.device)))
+
+
+def sv_draft_workspace_bytes(B: int, n: int, V: int) -> int:
+    return int(lib().sv_draft_workspace_bytes(B, n, V))
+
+
+def make_draft_workspace(B: int, n: int, V: int, device) -> torch.Tensor:
+    """Allocate and zero a workspace for sv_draft_sample."""
+    ws = torch.empty(max(256, sv_draft_workspace_bytes(B, n, V)), dtype=torch.uint8,
+                     device=device)
+    sv_workspace_init(ws)
+    return ws
+
+
+def sv_draft_sample(draft_logits, u_draft, temperature, out_tokens, out_stats, workspace,
+                    col: int = 0, dev_status=None, stream=None) -> None:
+    """Sample one token per draft row of draft_logits [B][n][V] and report the
+    rows' normalisers: out_tokens [B][ncols] int32 and out_stats [B][ncols][2]
+    float32 get columns col .. col + n - 1 (ncols = out_tokens.shape[1])."""
+    if draft_logits.dim() != 3:
+        raise SpecVerifyError("draft_logits must be [B][n][V]")
+    B, n, V = draft_logits.shape
+    if out_tokens.dim() != 2 or out_tokens.shape[0] != B:
+        raise SpecVerifyError("out_tokens must be [B][ncols]")
+    ncols = out_tokens.shape[1]
+    if tuple(out_stats.shape) != (B, ncols, 2):
+        raise SpecVerifyError("out_stats must be [B][ncols][2]")
+    _check(lib().sv_draft_sample(
+        _dev(draft_logits, None, "draft_logits"), _dev(u_draft, torch.float32, "u_draft"),
+        _dev(temperature, torch.float32, "temperature"), B, n, V, _dtype_code(draft_logits),
+        col, ncols, _dev(out_tokens, torch.int32, "out_tokens"),
+        _dev(out_stats, torch.float32, "out_stats"), _dev(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _dev(dev_status, torch.int32, "dev_status"), _stream(stream, draft_logits.device)))
+
+
+def spec_verify_cached(target_logits, draft_logits, draft_tokens, draft_stats, u_accept,
+                       u_resample, temperature, out_tokens, out_num_accepted, workspace,
+                       out_p=None, out_Z=None, dev_status=None, stream=None) -> None:
+    """spec_verify with the draft rows' normalisers draft_stats [B][gamma][2]
+    (as sv_draft_sample writes them): the draft rows are not streamed."""
+    B, g, V = _shapes(target_logits)
+    dt = _dtype_code(target_logits)
+    if draft_logits is not None and draft_logits.dtype != target_logits.dtype:
+        raise SpecVerifyError("draft_logits must have the dtype of target_logits")
+    _check(lib().spec_verify_cached(
+        _dev(target_logits, None, "target_logits"), _dev(draft_logits, None, "draft_logits"),
+        _dev(draft_tokens, torch.int32, "draft_tokens"),
+        _dev(draft_stats, torch.float32, "draft_stats"), _dev(u_accept, torch.float32, "u_accept"),
+        _dev(u_resample, torch.float32, "u_resample"),
+        _dev(temperature, torch.float32, "temperature"), B, g, V, dt,
+        _dev(out_tokens, torch.int32, "out_tokens"),
+        _dev(out_num_accepted, torch.int32, "out_num_accepted"),
+        _dev(out_p, torch.float32, "out_p"), _dev(out_Z, torch.float32, "out_Z"),
+        _dev(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _dev(dev_status, torch.int32, "dev_status"), _stream(stream, target_logits.device)))

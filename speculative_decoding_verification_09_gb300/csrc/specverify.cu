@@ -64,6 +64,8 @@ struct Geo {
   // body vectors of a row chunk per consumer thread: vector j belongs to
   // thread j mod (GW * 32) of the group
   static constexpr int MAXV = (HALF_ / 16 + GW * 32 - 1) / (GW * 32);
+  // a warp's contiguous run of a segment's vectors fits its registers
+  static_assert(32 * MAXV >= (HALF_ / 16 + GW - 1) / GW, "warp run");
   // Every use of a slot must be consumed by the same group: a group waits
   // for use u of a slot only after consuming use u - 1, which is what makes
   // the mbarrier's phase parity unambiguous.
@@ -149,6 +151,9 @@ struct Params {
   const float* u_res;
   const float* temp;
   int B, gamma, V, R;
+  int gs;                     // draft rows streamed by the reduce per request: gamma, or 0
+                              // when the draft rows' normalisers are given (dstats)
+  const float* dstats;        // cached draft normalisers [B][gamma][2] (m, S), or null
   int ch1, nch1, ch2, nch2, sub;
   int np1;                    // phase-1 partials per row: one per (chunk, consumer warp)
   long long tasks;            // phase-1 chunks, B * R * nch1
@@ -156,6 +161,8 @@ struct Params {
   int32_t* out_n;
   float* out_p;
   float* out_Z;
+  float* out_stats;           // draft sampling: row normalisers (m, S)
+  int col, ncols;             // draft sampling: row i of request b goes to column col + i of ncols
   int32_t* status;
   Ctrl* ctrl;
   Partial* part;
@@ -307,6 +314,9 @@ struct Elem<SV_F32> {
   __device__ static float lds(const unsigned char* base, int idx) {
     return reinterpret_cast<const float*>(base)[idx];
   }
+  __device__ static void sts(unsigned char* base, int idx, float v) {
+    reinterpret_cast<float*>(base)[idx] = v;
+  }
   __device__ static void unpack(const uint4& v, float* f) {
     f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
     f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
@@ -342,6 +352,9 @@ struct Elem<SV_BF16> {
   }
   __device__ static float lds(const unsigned char* base, int idx) {
     return __uint_as_float(uint32_t(reinterpret_cast<const unsigned short*>(base)[idx]) << 16);
+  }
+  __device__ static void sts(unsigned char* base, int idx, float v) {  // v holds a bf16 value
+    reinterpret_cast<unsigned short*>(base)[idx] = (unsigned short)(__float_as_uint(v) >> 16);
   }
   __device__ static void unpack(const uint4& v, float* f) {
     f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
@@ -453,9 +466,13 @@ struct alignas(16) Desc {
   int b, i, c;                // request, row position, chunk
   int e0, n;                  // element range of the chunk within the row
   int head_t, nb_t;           // target: leading single elements, aligned body elements in smem
-  int head_d, nb_d;           // draft likewise
+  int head_d, nb_d;           // draft likewise (or the second chunk of a pair)
   float kf;                   // sampling: log2(e) / T of the request
-  int pad;
+  float kf2;                  // pair: log2(e) / T of the second chunk's request
+  int pair;                   // reduce without draft rows: the slot's second half holds
+                              // the next target chunk (not a draft chunk)
+  int n2;                     // pair: elements of the second chunk
+  int pad[2];
   Record rec;                 // residual: the request's decision record (bulk-copied)
 };
 static_assert(offsetof(Desc, rec) % 16 == 0 && sizeof(Record) % 16 == 0, "record copy");
@@ -508,55 +525,105 @@ __device__ __forceinline__ float vec_expsum(const uint4& v, unsigned long long m
   return a + b;
 }
 
-// A consumer warp's share of one slot: body vector j of a row chunk belongs
-// to thread j mod (GW*32) of the group; the vectors are loaded from shared
-// memory into registers (MAXV per row per thread), plus the chunk fields the
-// reduction needs.  Target and draft shares are loaded together.
+// A consumer warp's share of one slot, in one of two maps of a segment's nv
+// body vectors to the group's threads:
+//   interleaved (CONTIG false): vector j to thread j mod (GW * 32); warp 0
+//     also takes the unaligned head and tail elements;
+//   contiguous (CONTIG true): warp wg takes the run [wg * pw, (wg + 1) * pw)
+//     with pw = ceil(nv / GW) (lane l its vectors l, l + 32, ...), so every
+//     warp's partial is the sum over a contiguous span of the row, which the
+//     draft sampler searches directly; warp 0 takes the head, warp GW - 1
+//     the tail.
+// The vectors are loaded from shared memory into registers (MAXV per segment
+// per thread), plus the chunk fields the reduction needs.  Both segments
+// (target and draft, or a pair of target chunks) are loaded together.
 template <int MAXV>
 struct Share {
   uint4 t[MAXV], d[MAXV];
   int b, i, c, e0, n, head_t, nb_t, head_d, nb_d;
-  float kf;
+  float kf, kf2;
+  int pair, n2;
 };
-template <int DT, class G>
+template <int DT, class G, bool CONTIG>
 __device__ __forceinline__ void load_share(const Desc& d, const unsigned char* slot, bool has_d,
                                            int wg, int lane, Share<G::MAXV>& sh) {
   using E = Elem<DT>;
-  constexpr int MAXV = G::MAXV, HALF = G::HALF;
-  constexpr int NCT = G::GW * 32;
-  const int tid = wg * 32 + lane;
+  constexpr int MAXV = G::MAXV, HALF = G::HALF, GW = G::GW;
   const int nvt = d.nb_t / E::VEC, nvd = has_d ? d.nb_d / E::VEC : 0;
   const uint4 neg = make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD);
+  if (CONTIG) {
+    const int pwt = (nvt + GW - 1) / GW, pwd = (nvd + GW - 1) / GW;
+    const int jt0 = wg * pwt, jt1 = min(nvt, jt0 + pwt);
+    const int jd0 = wg * pwd, jd1 = min(nvd, jd0 + pwd);
 #pragma unroll
-  for (int u = 0; u < MAXV; ++u) {
-    const int j = tid + u * NCT;
-    sh.t[u] = j < nvt ? reinterpret_cast<const uint4*>(slot)[j] : neg;
-    sh.d[u] = j < nvd ? reinterpret_cast<const uint4*>(slot + HALF)[j] : neg;
+    for (int u = 0; u < MAXV; ++u) {
+      const int jt = jt0 + lane + 32 * u, jd = jd0 + lane + 32 * u;
+      sh.t[u] = jt < jt1 ? reinterpret_cast<const uint4*>(slot)[jt] : neg;
+      sh.d[u] = jd < jd1 ? reinterpret_cast<const uint4*>(slot + HALF)[jd] : neg;
+    }
+  } else {
+    const int tid = wg * 32 + lane;
+#pragma unroll
+    for (int u = 0; u < MAXV; ++u) {
+      const int j = tid + u * GW * 32;
+      sh.t[u] = j < nvt ? reinterpret_cast<const uint4*>(slot)[j] : neg;
+      sh.d[u] = j < nvd ? reinterpret_cast<const uint4*>(slot + HALF)[j] : neg;
+    }
   }
   sh.b = d.b; sh.i = d.i; sh.c = d.c; sh.e0 = d.e0; sh.n = d.n;
   sh.head_t = d.head_t; sh.nb_t = d.nb_t; sh.head_d = d.head_d; sh.nb_d = d.nb_d;
   sh.kf = d.kf;
+  if (CONTIG) {
+    sh.kf2 = d.kf2;
+    sh.pair = d.pair;
+    sh.n2 = d.n2;
+  }
 }
 
-// This warp's (max, sum 2^((l-max)*kf)) over its share of one row chunk: the
-// body vectors in `sh` plus, for consumer warp 0, the few unaligned head/tail
-// elements read from global memory.  Each lane sums relative to its own
-// maximum; the lanes' sums are rescaled to the warp's.
-template <int DT, int MAXV>
-__device__ float4 reduce_share_ms(const Params& P, const Share<MAXV>& sh, bool has_d, int wg,
-                                  int lane) {
+// The chunk after chunk c of row (b, i) in the reduce's task order.
+__device__ __forceinline__ void next_chunk(const Params& P, int& b, int& i, int& c) {
+  if (++c == P.nch1) {
+    c = 0;
+    if (++i == P.R) { i = 0; ++b; }
+  }
+}
+
+// This warp's (max, sum 2^((l-max)*kf)) over its share of the slot's two
+// segments: the target chunk (b, i, c), and the second segment: the draft
+// chunk of the same span (PAIRS false, rows i < gs), or the next target
+// chunk (PAIRS true, when the slot holds a pair), with its own element count
+// and temperature.  The body vectors are in `sh`; consumer warp 0 also takes
+// the few unaligned head elements, and the tail elements go to warp GW - 1
+// (contiguous map, PAIRS) or warp 0 (interleaved map), from global memory.
+// Each lane sums relative to its own maximum; the lanes' sums are rescaled to
+// the warp's.
+template <int DT, int MAXV, int GW, bool PAIRS>
+__device__ float4 reduce_share_ms(const Params& P, const Share<MAXV>& sh, int wg, int lane) {
   using E = Elem<DT>;
-  const float kf = sh.kf;
+  const bool has_d = PAIRS ? sh.pair != 0 : sh.i < P.gs;
+  const float kf_t = sh.kf, kf_d = PAIRS ? sh.kf2 : sh.kf;
   float ht = -INFINITY, tt = -INFINITY, hd = -INFINITY, td = -INFINITY;
-  if (wg == 0) {
-    const unsigned char* gt = P.Lt + ((size_t(sh.b) * P.R + sh.i) * size_t(P.V) + sh.e0) * E::ES;
-    if (lane < sh.head_t) ht = E::load(gt, lane);
-    if (lane < sh.n - sh.head_t - sh.nb_t) tt = E::load(gt, sh.head_t + sh.nb_t + lane);
+  if (wg == 0 || wg == (PAIRS ? GW - 1 : 0)) {
+    const int n_t = sh.n, n_d = PAIRS ? sh.n2 : sh.n;
+    const unsigned char* gt =
+        P.Lt + ((size_t(sh.b) * P.R + sh.i) * size_t(P.V) + sh.e0) * E::ES;
+    const unsigned char* gd = nullptr;
     if (has_d) {
-      const unsigned char* gd =
-          P.Ld + ((size_t(sh.b) * P.gamma + sh.i) * size_t(P.V) + sh.e0) * E::ES;
-      if (lane < sh.head_d) hd = E::load(gd, lane);
-      if (lane < sh.n - sh.head_d - sh.nb_d) td = E::load(gd, sh.head_d + sh.nb_d + lane);
+      if (PAIRS) {
+        int b2 = sh.b, i2 = sh.i, c2 = sh.c;
+        next_chunk(P, b2, i2, c2);
+        gd = P.Lt + ((size_t(b2) * P.R + i2) * size_t(P.V) + size_t(c2) * P.ch1) * E::ES;
+      } else {
+        gd = P.Ld + ((size_t(sh.b) * P.gamma + sh.i) * size_t(P.V) + sh.e0) * E::ES;
+      }
+    }
+    if (wg == 0) {
+      if (lane < sh.head_t) ht = E::load(gt, lane);
+      if (has_d && lane < sh.head_d) hd = E::load(gd, lane);
+    }
+    if (wg == (PAIRS ? GW - 1 : 0)) {
+      if (lane < n_t - sh.head_t - sh.nb_t) tt = E::load(gt, sh.head_t + sh.nb_t + lane);
+      if (has_d && lane < n_d - sh.head_d - sh.nb_d) td = E::load(gd, sh.head_d + sh.nb_d + lane);
     }
   }
   // lane maxima: balanced trees over the vectors
@@ -577,22 +644,22 @@ __device__ float4 reduce_share_ms(const Params& P, const Share<MAXV>& sh, bool h
   const float md = fmax_nan(E::vmax_final(wd[0]), fmax_nan(hd, td));
   // a NaN max makes the sum NaN; an all -inf share sums to 0
   const bool lt = mt > -INFINITY, ld = md > -INFINITY;
-  const unsigned long long kk = pk2(kf, kf);
+  const unsigned long long kkt = pk2(kf_t, kf_t), kkd = pk2(kf_d, kf_d);
   const unsigned long long mmt = pk2(mt, mt), mmd = pk2(md, md);
   float s_t = 0.f, s_d = 0.f;
 #pragma unroll
   for (int u = 0; u < MAXV; ++u) {
-    if (lt) s_t += vec_expsum<DT>(sh.t[u], mmt, kk);
-    if (ld) s_d += vec_expsum<DT>(sh.d[u], mmd, kk);
+    if (lt) s_t += vec_expsum<DT>(sh.t[u], mmt, kkt);
+    if (ld) s_d += vec_expsum<DT>(sh.d[u], mmd, kkd);
   }
-  if (lt) s_t += ex2((ht - mt) * kf) + ex2((tt - mt) * kf);
-  if (ld) s_d += ex2((hd - md) * kf) + ex2((td - md) * kf);
+  if (lt) s_t += ex2((ht - mt) * kf_t) + ex2((tt - mt) * kf_t);
+  if (ld) s_d += ex2((hd - md) * kf_d) + ex2((td - md) * kf_d);
   if (mt != mt) s_t = NAN;
   if (md != md) s_d = NAN;
   // rescale every lane's sum to the warp maximum and add them up
   const float Mt = warp_max_nan(mt), Md = warp_max_nan(md);
-  if (lt && Mt > mt) s_t *= ex2((mt - Mt) * kf);
-  if (ld && Md > md) s_d *= ex2((md - Md) * kf);
+  if (lt && Mt > mt) s_t *= ex2((mt - Mt) * kf_t);
+  if (ld && Md > md) s_d *= ex2((md - Md) * kf_d);
   if (Mt != Mt) s_t = NAN;
   if (Md != Md) s_d = NAN;
 #pragma unroll
@@ -604,25 +671,27 @@ __device__ float4 reduce_share_ms(const Params& P, const Share<MAXV>& sh, bool h
 }
 
 // This warp's (largest value, lowest index among its occurrences, NaN seen)
-// over its share of one target row chunk; indices are within the row.
+// over its share of one target row chunk: body vectors `vec` (the slot's
+// first or second segment, this warp's run of it in the contiguous map), the
+// chunk at `gseg` starting at element e0 of its row with `head` single
+// leading elements, nb body elements, n in all; indices are within the row.
 template <int DT, class G>
-__device__ float4 reduce_share_argmax(const Params& P, const Share<G::MAXV>& sh, int wg, int lane) {
+__device__ float4 reduce_share_argmax(const uint4 (&vec)[G::MAXV], const unsigned char* gseg,
+                                      int e0, int head, int nb, int n, int wg, int lane) {
   using E = Elem<DT>;
   constexpr int MAXV = G::MAXV;
-  constexpr int NCT = G::GW * 32;
-  const int tid = wg * 32 + lane;
-  const unsigned char* gseg = P.Lt + ((size_t(sh.b) * P.R + sh.i) * size_t(P.V) + sh.e0) * E::ES;
+  const int pw = (nb / E::VEC + G::GW - 1) / G::GW;
   float best = -INFINITY;
   int bi = INT_MAX, nan = 0;
-  if (wg == 0 && lane < sh.head_t) {
+  if (wg == 0 && lane < head) {
     const float l = E::load(gseg, lane);
     if (l != l) nan = 1;
-    else if (l > best) { best = l; bi = sh.e0 + lane; }
+    else if (l > best) { best = l; bi = e0 + lane; }
   }
 #pragma unroll
   for (int u = 0; u < MAXV; ++u) {
-    const int j = tid + u * NCT;
-    const uint4 v = sh.t[u];
+    const int j = wg * pw + lane + 32 * u;
+    const uint4 v = vec[u];
     const float vm = E::vmax(v);
     if (vm != vm) {
       nan = 1;
@@ -634,15 +703,15 @@ __device__ float4 reduce_share_argmax(const Params& P, const Share<G::MAXV>& sh,
       for (int e = E::VEC - 1; e >= 0; --e)
         if (f[e] == vm) first = e;
       best = vm;
-      bi = sh.e0 + sh.head_t + j * E::VEC + first;
+      bi = e0 + head + j * E::VEC + first;
     }
   }
-  if (wg == 0) {
-    const int t0 = sh.head_t + sh.nb_t;
-    if (lane < sh.n - t0) {
+  if (wg == G::GW - 1) {
+    const int t0 = head + nb;
+    if (lane < n - t0) {
       const float l = E::load(gseg, t0 + lane);
       if (l != l) nan = 1;
-      else if (l > best) { best = l; bi = sh.e0 + t0 + lane; }
+      else if (l > best) { best = l; bi = e0 + t0 + lane; }
     }
   }
 #pragma unroll
@@ -766,7 +835,11 @@ __device__ void end_markers(const Params& P, SmemCtl<G>& C, long long seq) {
 
 // Producer (one lane): this CTA's contiguous range of chunks, in order, into
 // the slot ring.  Chunk t is chunk t % nch1 of row t / nch1 (row = b * R + i).
-template <int DT, bool GREEDY>
+// A slot holds a target chunk and the same span of the draft row; where no
+// draft rows are streamed (greedy verification, given draft normalisers,
+// draft sampling) it holds two consecutive target chunks instead (a pair),
+// so every slot still carries up to two half-slots of logits.
+template <int DT, bool GREEDY, bool PAIRS>
 __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* slots) {
   using E = Elem<DT>;
   using G = GeoReduce;
@@ -780,8 +853,22 @@ __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* 
   float T_next = (!GREEDY && b + 1 < P.B) ? __ldg(P.temp + b + 1) : 1.f;
   const unsigned char* trow = P.Lt + (size_t(b) * P.R + i) * size_t(P.V) * E::ES;
   const unsigned char* drow =
-      (!GREEDY && i < P.gamma) ? P.Ld + (size_t(b) * P.gamma + i) * size_t(P.V) * E::ES : nullptr;
-  for (long long t = t0, seq = 0; t <= t1; ++t, ++seq) {
+      (!GREEDY && i < P.gs) ? P.Ld + (size_t(b) * P.gamma + i) * size_t(P.V) * E::ES : nullptr;
+  auto advance = [&]() {  // to the next chunk
+    if (++c == P.nch1) {
+      c = 0;
+      if (++i == P.R) {
+        i = 0;
+        ++b;
+        T = T_next;
+        if (!GREEDY && b + 1 < P.B) T_next = __ldg(P.temp + b + 1);
+      }
+      trow = P.Lt + (size_t(b) * P.R + i) * size_t(P.V) * E::ES;
+      drow = (!GREEDY && i < P.gs) ? P.Ld + (size_t(b) * P.gamma + i) * size_t(P.V) * E::ES
+                                   : nullptr;
+    }
+  };
+  for (long long t = t0, seq = 0; t <= t1; ++seq) {
     const int s = int(seq % NS);
     const unsigned use = unsigned(seq / NS);
     if (t == t1 || C.abort) {
@@ -795,11 +882,29 @@ __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* 
     d.e0 = c * P.ch1;
     d.n = min(P.ch1, P.V - d.e0);
     d.kf = LOG2E_F / T;
+    if (PAIRS) {
+      d.kf2 = d.kf;
+      d.pair = 0;
+      d.n2 = 0;
+    }
     const unsigned char* tseg = trow + size_t(d.e0) * E::ES;
     const unsigned char* dseg = drow ? drow + size_t(d.e0) * E::ES : nullptr;
     split<DT>(tseg, d.n, d.head_t, d.nb_t);
-    d.head_d = d.nb_d = 0;
-    if (dseg) split<DT>(dseg, d.n, d.head_d, d.nb_d);
+    ++t;
+    if (PAIRS && t < t1) {  // the next target chunk into the second half
+      advance();
+      const int e0b = c * P.ch1;
+      d.pair = 1;
+      d.n2 = min(P.ch1, P.V - e0b);
+      d.kf2 = LOG2E_F / T;
+      dseg = trow + size_t(e0b) * E::ES;
+      split<DT>(dseg, d.n2, d.head_d, d.nb_d);
+      ++t;
+    } else if (dseg) {
+      split<DT>(dseg, d.n, d.head_d, d.nb_d);
+    } else {
+      d.head_d = d.nb_d = 0;
+    }
     const unsigned bt = unsigned(d.nb_t) * E::ES, bd = unsigned(d.nb_d) * E::ES;
     if (bt + bd == 0u) {
       mbar_arrive(&C.full[s]);
@@ -810,27 +915,16 @@ __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* 
         bulk_g2s(slots + size_t(s) * SLOT + HALF, dseg + size_t(d.head_d) * E::ES, bd,
                  &C.full[s]);
     }
-    // the next chunk
-    if (++c == P.nch1) {
-      c = 0;
-      if (++i == P.R) {
-        i = 0;
-        ++b;
-        T = T_next;
-        if (!GREEDY && b + 1 < P.B) T_next = __ldg(P.temp + b + 1);
-      }
-      trow = P.Lt + (size_t(b) * P.R + i) * size_t(P.V) * E::ES;
-      drow = (!GREEDY && i < P.gamma) ? P.Ld + (size_t(b) * P.gamma + i) * size_t(P.V) * E::ES
-                                      : nullptr;
-    }
+    advance();  // after the copies are on their way (it may load a temperature)
   }
 }
 
 // Consumers: every warp loads its share of a slot into registers and hands
 // the slot back at once (so the producer can refill it while the share is
-// reduced), then publishes its own partial.
-template <int DT, bool GREEDY>
+// reduced), then publishes its own partial (two for a pair of target chunks).
+template <int DT, bool GREEDY, bool PAIRS>
 __device__ void consumer(const Params& P, SmemCtl<GeoReduce>& C, const unsigned char* slots) {
+  using E = Elem<DT>;
   using G = GeoReduce;
   constexpr int NS = G::NS, SLOT = G::SLOT, GW = G::GW;
   const int lane = threadIdx.x & 31;
@@ -844,17 +938,42 @@ __device__ void consumer(const Params& P, SmemCtl<GeoReduce>& C, const unsigned 
     if (!mbar_wait(&C.full[s], use & 1u, P, &C.abort)) return false;
     const Desc& d = C.desc[s];
     if (d.end) return false;
-    load_share<DT, G>(d, slots + size_t(s) * SLOT, !GREEDY && d.i < P.gamma, wg, lane, sh);
+    const bool second = PAIRS ? d.pair != 0 : d.i < P.gs;
+    load_share<DT, G, PAIRS>(d, slots + size_t(s) * SLOT, second, wg, lane, sh);
     __syncwarp();
     if (lane == 0) mbar_arrive(&C.empty[s]);
     return true;
   };
   auto process = [&](const Share<G::MAXV>& sh) {
-    const float4 out = GREEDY ? reduce_share_argmax<DT, G>(P, sh, wg, lane)
-                              : reduce_share_ms<DT, G::MAXV>(P, sh, sh.i < P.gamma, wg, lane);
+    float4 out, out2 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (GREEDY) {
+      const unsigned char* gt =
+          P.Lt + ((size_t(sh.b) * P.R + sh.i) * size_t(P.V) + sh.e0) * E::ES;
+      out = reduce_share_argmax<DT, G>(sh.t, gt, sh.e0, sh.head_t, sh.nb_t, sh.n, wg, lane);
+      if (sh.pair) {
+        int b2 = sh.b, i2 = sh.i, c2 = sh.c;
+        next_chunk(P, b2, i2, c2);
+        const unsigned char* g2 =
+            P.Lt + ((size_t(b2) * P.R + i2) * size_t(P.V) + size_t(c2) * P.ch1) * E::ES;
+        out2 = reduce_share_argmax<DT, G>(sh.d, g2, c2 * P.ch1, sh.head_d, sh.nb_d, sh.n2, wg,
+                                          lane);
+      }
+    } else if (PAIRS) {
+      const float4 r = reduce_share_ms<DT, G::MAXV, GW, true>(P, sh, wg, lane);
+      out = make_float4(r.x, r.y, -INFINITY, 0.f);
+      out2 = make_float4(r.z, r.w, -INFINITY, 0.f);
+    } else {
+      out = reduce_share_ms<DT, G::MAXV, GW, false>(P, sh, wg, lane);
+    }
     if (lane == 0) {
       Partial* dst = P.part + ((size_t(sh.b) * P.R + sh.i) * P.nch1 + sh.c) * GW + wg;
       *reinterpret_cast<float4*>(dst) = out;
+      if (PAIRS && sh.pair) {
+        int b2 = sh.b, i2 = sh.i, c2 = sh.c;
+        next_chunk(P, b2, i2, c2);
+        Partial* dst2 = P.part + ((size_t(b2) * P.R + i2) * P.nch1 + c2) * GW + wg;
+        *reinterpret_cast<float4*>(dst2) = out2;
+      }
     }
   };
   Share<G::MAXV> sh;
@@ -864,7 +983,11 @@ __device__ void consumer(const Params& P, SmemCtl<GeoReduce>& C, const unsigned 
   }
 }
 
-template <int DT, bool GREEDY>
+// GREEDY: chunk argmax instead of (max, sum); PAIRS: no draft rows are
+// streamed, a slot carries two target chunks and the warps' shares are
+// contiguous spans (greedy verification, given draft normalisers, draft
+// sampling).
+template <int DT, bool GREEDY, bool PAIRS>
 __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
   using G = GeoReduce;
   // every CTA of this grid is resident from the start (one per SM), so the
@@ -888,9 +1011,9 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
   }
   __syncthreads();
   if (threadIdx.x < 32) {
-    if (threadIdx.x == 0) producer<DT, GREEDY>(P, C, slots);
+    if (threadIdx.x == 0) producer<DT, GREEDY, PAIRS>(P, C, slots);
   } else {
-    consumer<DT, GREEDY>(P, C, slots);
+    consumer<DT, GREEDY, PAIRS>(P, C, slots);
   }
 }
 
@@ -1088,12 +1211,14 @@ __device__ void decide_greedy(const Params& P, int b, const RowStat* rows) {
 
 // One CTA per request: DECIDE_WARPS warps combine the rows (row i by warp
 // i % DECIDE_WARPS), then warp 0 decides.  The draft tokens, their logits and
-// the uniforms are loaded by warp 0 before its rows.
+// the uniforms are loaded by warp 0 before its rows; given draft normalisers
+// (dstats) replace the draft rows' combine.
 template <int DT, bool GREEDY>
 __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, bool last) {
   using E = Elem<DT>;
   __shared__ RowStat rows[MAXR];
   __shared__ Cand cand[MAXR];
+  __shared__ float2 dst_sh[MAXR];
   __shared__ int2 mode_k;
   const int b = blockIdx.x, warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int g = P.gamma, R = P.R, V = P.V;
@@ -1110,9 +1235,14 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
     }
   }
   const float kf = GREEDY ? 0.f : LOG2E_F / __ldg(P.temp + b);
+  const bool cached = !GREEDY && P.dstats != nullptr;
+  if (cached && int(threadIdx.x) < g)
+    dst_sh[threadIdx.x] = __ldg(reinterpret_cast<const float2*>(P.dstats) + size_t(b) * g +
+                                threadIdx.x);
   // the loads above read only the call's inputs; the partials come from the
   // reduce kernel
   wait_previous_kernel();
+  if (cached) __syncthreads();
   for (int i = warp; i < R; i += DECIDE_WARPS) {
     const Partial* pp = P.part + (size_t(b) * R + i) * size_t(P.np1);
     if (GREEDY) {
@@ -1129,7 +1259,11 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
     } else {
       float mt, md;
       double St, Sd;
-      row_combine(pp, P.np1, kf, i < g, mt, St, md, Sd);
+      row_combine(pp, P.np1, kf, i < P.gs, mt, St, md, Sd);
+      if (cached && i < g) {  // the draft row's normaliser, as given
+        md = dst_sh[i].x;
+        Sd = double(dst_sh[i].y);
+      }
       if (lane == 0) {
         RowStat r;
         r.mt = mt; r.md = md; r.St = St; r.Sd = Sd;
@@ -1651,6 +1785,207 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
   if (last_cta && threadIdx.x == 0) P.ctrl->state = 0ull;
 }
 
+// ---------------------------------------------------------- draft sampling
+
+// Block-wide inclusive prefix of float pairs in thread order (all threads of
+// the CTA take part); `total` gets the CTA's sum.  wsum holds one entry per
+// warp; the CTA synchronises twice.
+__device__ FF block_scan_ff(FF v, FF* wsum, FF& total) {
+  const int warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
+  FF incl = v;
+  warp_scan_ff(incl.h, incl.l, lane);
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  FF off = ff(0.f), tot = ff(0.f);
+  for (int w = 0; w < DRAW_WARPS; ++w) {
+    if (w < warp) off = off + wsum[w];
+    tot = tot + wsum[w];
+  }
+  __syncthreads();
+  total = tot;
+  return off + incl;
+}
+
+// Mass of the reduce's partial q of a row (a consumer warp's sum over its
+// span) relative to the row maximum m, as a float.
+__device__ __forceinline__ float partial_mass(const Partial* pp, int q, float m, float kf) {
+  const float4 v = __ldg(reinterpret_cast<const float4*>(pp + q));
+  return (m == -INFINITY) ? v.y : v.y * ex2((v.x - m) * kf);
+}
+
+// Element span [lo, hi) of a row that the reduce's partial q covers (chunk
+// q / GW, consumer warp q % GW), as load_share assigns it: the warp's run of
+// the chunk's aligned body, with the unaligned head on warp 0 and the tail on
+// warp GW - 1.
+template <int DT>
+__device__ __forceinline__ void partial_span(const Params& P, const unsigned char* row, int q,
+                                             int& lo, int& hi) {
+  using E = Elem<DT>;
+  constexpr int GW = GeoReduce::GW;
+  const int c = q / GW, w = q - c * GW;
+  const int e0 = c * P.ch1, n = min(P.ch1, P.V - e0);
+  int head, nb;
+  split<DT>(row + size_t(e0) * E::ES, n, head, nb);
+  const int nv = nb / E::VEC, pw = (nv + GW - 1) / GW;
+  const int v0 = min(nv, w * pw), v1 = min(nv, (w + 1) * pw);
+  lo = (w == 0) ? e0 : e0 + head + v0 * E::VEC;
+  hi = (w == GW - 1) ? e0 + n : e0 + head + v1 * E::VEC;
+}
+
+// a partial's span: a warp's run of at most ceil(HALF / 16 / GW) vectors plus
+// a head or tail shorter than a vector, and a vector of margin
+constexpr int SAMPLE_STAGE =
+    ((GeoReduce::HALF / 16 + GeoReduce::GW - 1) / GeoReduce::GW) * 16 + 48;
+constexpr int SAMPLE_KV = (SAMPLE_STAGE / 16 + 32 * DRAW_WARPS - 1) / (32 * DRAW_WARPS);
+
+// Draft-token sampling, one CTA per draft row (row r = b * R + i of the
+// reduce's rows): the row's maximum and normaliser S from the reduce's
+// partials, the partial (a contiguous span of the row) where the running mass
+// crosses tau = u * S, scanned over the partials in index order, then that
+// span's elements, staged in shared memory: each thread sums a contiguous
+// run of weights, a block prefix finds the crossing run, whose thread scans
+// it in index order.  Writes the token and the row's (max, S) to column
+// col + i of request b.
+template <int DT>
+__global__ void __launch_bounds__(32 * DRAW_WARPS) sv_sample(const Params P) {
+  using E = Elem<DT>;
+  constexpr int NT = 32 * DRAW_WARPS;
+  __shared__ FF wsum[DRAW_WARPS];
+  __shared__ float wmax[DRAW_WARPS];
+  __shared__ FF sh_rest, sh_rest_last;
+  __shared__ int sh_hit, sh_last, sh_tok_hit, sh_tok_last;
+  __shared__ __align__(16) unsigned char stage[SAMPLE_STAGE];
+  const int r = int(blockIdx.x), tid = int(threadIdx.x);
+  const int warp = tid >> 5, lane = tid & 31;
+  const int b = r / P.R, i = r - b * P.R;
+  const size_t o = size_t(b) * P.ncols + P.col + i;
+  // inputs, loaded before the wait for the partials
+  const float u = __ldg(P.u_res + r);
+  const float T = __ldg(P.temp + b);
+  const bool t_ok = isfinite(T) && T >= 0x1p-126f;
+  const float kf = LOG2E_F / T;
+  if (tid == 0) {
+    sh_hit = INT_MAX;
+    sh_last = -1;
+    sh_tok_hit = INT_MAX;
+    sh_tok_last = -1;
+  }
+  wait_previous_kernel();
+  const Partial* pp = P.part + size_t(r) * P.np1;
+  const int np = P.np1;
+  // 1. the row maximum over the partials' maxima (NaN shows in the sums)
+  float m = -INFINITY;
+  for (int q = tid; q < np; q += NT) m = fmaxf(m, __ldg(&pp[q].a));
+  m = warp_max(m);
+  if (lane == 0) wmax[warp] = m;
+  __syncthreads();
+  m = wmax[0];
+  for (int w = 1; w < DRAW_WARPS; ++w) m = fmaxf(m, wmax[w]);
+  // 2. the normaliser S, the sum of the partials' masses
+  FF part = ff(0.f);
+  for (int q = tid; q < np; q += NT) ff_add(part.h, part.l, partial_mass(pp, q, m, kf));
+  FF S;
+  block_scan_ff(part, wsum, S);
+  const double Sd = ff_val(S.h, S.l);
+  const bool ok = t_ok && row_ok(m, Sd);  // the same in every thread
+  if (!ok) {
+    if (tid == 0) {
+      P.out_tokens[o] = -1;
+      P.out_stats[2 * o] = NAN;
+      P.out_stats[2 * o + 1] = NAN;
+      set_status(P, t_ok ? SV_ST_NONFINITE : SV_ST_BAD_TEMP);
+      if (r == 0) P.ctrl->state = 0ull;
+    }
+    return;
+  }
+  // 3. the crossing partial, in rounds of NT partials
+  const FF tau = ff_mul(u, S);
+  FF base = ff(0.f);
+  for (int q0 = 0; q0 < np; q0 += NT) {
+    const int q = q0 + tid;
+    const FF z = ff(q < np ? partial_mass(pp, q, m, kf) : 0.f);
+    FF rtot;
+    const FF incl = block_scan_ff(z, wsum, rtot);
+    const bool pos = q < np && ff_pos(z);
+    if (pos && ff_gt(base + incl, tau)) atomicMin(&sh_hit, q);
+    if (pos) atomicMax(&sh_last, q);
+    __syncthreads();
+    if (q == sh_hit) sh_rest = tau - (base + (incl - z));
+    if (q == sh_last) sh_rest_last = z;  // the span's whole mass: its last element
+    if (sh_hit != INT_MAX) break;        // the same in every thread
+    base = base + rtot;
+    __syncthreads();                     // sh_last is read above before the next round's updates
+  }
+  __syncthreads();
+  const bool hit = sh_hit != INT_MAX;
+  const int qs = hit ? sh_hit : sh_last;
+  const FF rest = hit ? sh_rest : sh_rest_last;
+  // 4. the span's elements, staged in shared memory: the body with 16-byte
+  // loads, an unaligned head and tail element by element; element e sits at
+  // stage index VEC + (e - a), a the span's first element on a 16-byte
+  // boundary
+  Record rr;
+  rr.k = 0; rr.mode = MODE_BONUS; rr.mt = m; rr.kf = kf;
+  rr.ist_hi = rr.ist_lo = rr.c0_hi = rr.c0_lo = 0.f;
+  const unsigned char* row = P.Lt + size_t(r) * size_t(P.V) * E::ES;
+  int lo, hi;
+  partial_span<DT>(P, row, qs, lo, hi);
+  int head, nbody;
+  split<DT>(row + size_t(lo) * E::ES, hi - lo, head, nbody);
+  const int a = lo + head, nvec = nbody / E::VEC;
+  {
+    const uint4* gv = reinterpret_cast<const uint4*>(row + size_t(a) * E::ES);
+    uint4* sv = reinterpret_cast<uint4*>(stage);
+    uint4 buf[SAMPLE_KV];
+#pragma unroll
+    for (int k = 0; k < SAMPLE_KV; ++k) {
+      const int j = tid + k * NT;
+      if (j < nvec) buf[k] = __ldg(gv + j);
+    }
+#pragma unroll
+    for (int k = 0; k < SAMPLE_KV; ++k) {
+      const int j = tid + k * NT;
+      if (j < nvec) sv[1 + j] = buf[k];
+    }
+    for (int e = lo + tid; e < a; e += NT) E::sts(stage, E::VEC + (e - a), E::load(row, e));
+    for (int e = a + nbody + tid; e < hi; e += NT)
+      E::sts(stage, E::VEC + (e - a), E::load(row, e));
+  }
+  __syncthreads();
+  // a contiguous run of the span per thread
+  const int per = (hi - lo + NT - 1) / NT;
+  const int a0 = min(hi, lo + tid * per), a1 = min(hi, a0 + per);
+  FF run = ff(0.f);
+  int lastpos = -1;
+  for (int e = a0; e < a1; ++e) {
+    const float w = weight(rr, E::lds(stage, E::VEC + (e - a)), 0.f);
+    ff_add(run.h, run.l, w);
+    if (w > 0.f) lastpos = e;
+  }
+  FF rtot;
+  const FF incl = block_scan_ff(run, wsum, rtot);
+  if (a0 < a1 && ff_pos(run) && ff_gt(incl, rest)) atomicMin(&sh_tok_hit, tid);
+  if (lastpos >= 0) atomicMax(&sh_tok_last, lastpos);
+  __syncthreads();
+  if (tid == sh_tok_hit) {
+    FF acc = incl - run;
+    int tok = lastpos;
+    for (int e = a0; e < a1; ++e) {
+      const float w = weight(rr, E::lds(stage, E::VEC + (e - a)), 0.f);
+      ff_add(acc.h, acc.l, w);
+      if (ff_gt(acc, rest)) { tok = e; break; }
+    }
+    P.out_tokens[o] = tok;
+  } else if (sh_tok_hit == INT_MAX && tid == 0) {  // rounding: the span's last element with mass
+    P.out_tokens[o] = sh_tok_last < 0 ? lo : sh_tok_last;
+  }
+  if (tid == 0) {
+    P.out_stats[2 * o] = m;
+    P.out_stats[2 * o + 1] = float(Sd);
+    if (r == 0) P.ctrl->state = 0ull;
+  }
+}
+
 // ---------------------------------------------------------------- host
 
 struct Tuning {
@@ -1667,13 +2002,17 @@ struct DevCache {
 std::mutex g_mu;
 DevCache g_dev[64];
 
-template <int DT, bool G>
+template <int DT>
 bool prepare_kernel() {
-  if (!G && cudaFuncSetAttribute(sv_residual<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(smem_bytes<GeoResidual>())) != cudaSuccess)
-    return false;
-  return cudaFuncSetAttribute(sv_reduce<DT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(smem_bytes<GeoReduce>())) == cudaSuccess;
+  const int r = int(smem_bytes<GeoReduce>());
+  return cudaFuncSetAttribute(sv_residual<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(smem_bytes<GeoResidual>())) == cudaSuccess &&
+         cudaFuncSetAttribute(sv_reduce<DT, false, false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, r) == cudaSuccess &&
+         cudaFuncSetAttribute(sv_reduce<DT, false, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, r) == cudaSuccess &&
+         cudaFuncSetAttribute(sv_reduce<DT, true, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, r) == cudaSuccess;
 }
 
 int device_info(int& sms) {
@@ -1684,8 +2023,7 @@ int device_info(int& sms) {
   if (!d.init) {
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return SV_ERR_CUDA;
-    if (!prepare_kernel<SV_F32, false>() || !prepare_kernel<SV_F32, true>() ||
-        !prepare_kernel<SV_BF16, false>() || !prepare_kernel<SV_BF16, true>())
+    if (!prepare_kernel<SV_F32>() || !prepare_kernel<SV_BF16>())
       return SV_ERR_CUDA;
     d.init = true;
   }
@@ -1714,27 +2052,69 @@ cudaError_t launch_after(void (*kern)(KArgs...), unsigned grid, unsigned block, 
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const float* u_acc,
-           const float* u_res, const float* temp, int B, int gamma, int V, int dtype,
-           int32_t* out_tokens, int32_t* out_n, float* out_p, float* out_Z, void* ws,
-           size_t ws_bytes, int32_t* status, void* stream) {
-  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
-  if (B < 0 || gamma < 0 || gamma > SV_MAX_GAMMA || V < 1) return SV_ERR_INVALID_ARG;
-  if (B == 0) return SV_OK;  // nothing to do; empty buffers may be NULL
-  const int ES = dtype == SV_F32 ? 4 : 2;
-  if (!Lt || (!x && gamma > 0) || !out_tokens || !out_n) return SV_ERR_INVALID_ARG;
-  if (!greedy && (!u_res || !temp || (gamma > 0 && (!Ld || !u_acc)))) return SV_ERR_INVALID_ARG;
-  auto mis = [](const void* p, int a) { return p && (reinterpret_cast<uintptr_t>(p) % a) != 0; };
-  if (mis(Lt, ES) || mis(Ld, ES) || mis(x, 4) || mis(u_acc, 4) || mis(u_res, 4) || mis(temp, 4) ||
-      mis(out_tokens, 4) || mis(out_n, 4) || mis(out_p, 4) || mis(out_Z, 4) || mis(status, 4))
+// One library call: which path, and its arguments as the C ABI gives them.
+enum CallKind { CALL_SAMPLE = 0, CALL_GREEDY = 1, CALL_CACHED = 2, CALL_DRAFT = 3 };
+struct Call {
+  int kind = CALL_SAMPLE;
+  const void* Lt = nullptr;   // target logits; the draft logits for CALL_DRAFT
+  const void* Ld = nullptr;
+  const int32_t* x = nullptr;
+  const float* u_acc = nullptr;
+  const float* u_res = nullptr;  // u_resample; u_draft for CALL_DRAFT
+  const float* temp = nullptr;
+  const float* dstats = nullptr;
+  int B = 0, gamma = 0, V = 0, dtype = SV_F32;
+  int n = 0;                  // CALL_DRAFT: rows per request
+  int32_t* out_tokens = nullptr;
+  int32_t* out_n = nullptr;
+  float* out_p = nullptr;
+  float* out_Z = nullptr;
+  float* out_stats = nullptr;
+  int col = 0, ncols = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  int32_t* status = nullptr;
+  void* stream = nullptr;
+};
+
+int launch(const Call& a) {
+  const bool greedy = a.kind == CALL_GREEDY, draft = a.kind == CALL_DRAFT;
+  if (a.dtype != SV_F32 && a.dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (a.B < 0 || a.V < 1) return SV_ERR_INVALID_ARG;
+  if (draft) {
+    if (a.n < 1 || a.n > SV_MAX_GAMMA || a.col < 0 || a.ncols < a.col + a.n)
+      return SV_ERR_INVALID_ARG;
+  } else if (a.gamma < 0 || a.gamma > SV_MAX_GAMMA) {
     return SV_ERR_INVALID_ARG;
-  const Layout L = make_layout(B, gamma, V);
-  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return SV_ERR_WORKSPACE;
+  }
+  if (a.B == 0) return SV_OK;  // nothing to do; empty buffers may be NULL
+  const int ES = a.dtype == SV_F32 ? 4 : 2;
+  const int gamma = draft ? 0 : a.gamma;
+  const int R = draft ? a.n : gamma + 1;
+  if (!a.Lt || !a.out_tokens) return SV_ERR_INVALID_ARG;
+  if (draft) {
+    if (!a.u_res || !a.temp || !a.out_stats) return SV_ERR_INVALID_ARG;
+  } else {
+    if (!a.out_n || (!a.x && gamma > 0)) return SV_ERR_INVALID_ARG;
+    if (!greedy && (!a.u_res || !a.temp || (gamma > 0 && (!a.Ld || !a.u_acc))))
+      return SV_ERR_INVALID_ARG;
+    if (a.kind == CALL_CACHED && gamma > 0 && !a.dstats) return SV_ERR_INVALID_ARG;
+  }
+  auto mis = [](const void* p, int al) {
+    return p && (reinterpret_cast<uintptr_t>(p) % al) != 0;
+  };
+  if (mis(a.Lt, ES) || mis(a.Ld, ES) || mis(a.x, 4) || mis(a.u_acc, 4) || mis(a.u_res, 4) ||
+      mis(a.temp, 4) || mis(a.dstats, 8) || mis(a.out_tokens, 4) || mis(a.out_n, 4) ||
+      mis(a.out_p, 4) || mis(a.out_Z, 4) || mis(a.out_stats, 4) || mis(a.status, 4))
+    return SV_ERR_INVALID_ARG;
+  const int B = a.B, V = a.V;
+  const Layout L = make_layout(B, R - 1, V);
+  if (!a.ws || (reinterpret_cast<uintptr_t>(a.ws) & 255u) || a.ws_bytes < L.total)
+    return SV_ERR_WORKSPACE;
 
   int sms = 0;
   int rc = device_info(sms);
   if (rc != SV_OK) return rc;
-  const int R = gamma + 1;
   const long long units = (long long)B * R;
   const int chmax = GeoReduce::HALF / ES;     // a phase-1 chunk fits half a slot
   const int chmax2 = GeoResidual::HALF / ES;  // phase 2 likewise
@@ -1757,10 +2137,12 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
   if (nch1 > L.nch1_max) return SV_ERR_INVALID_ARG;
 
   Params P;
-  P.Lt = static_cast<const unsigned char*>(Lt);
-  P.Ld = static_cast<const unsigned char*>(Ld);
-  P.x = x; P.u_acc = u_acc; P.u_res = u_res; P.temp = temp;
+  P.Lt = static_cast<const unsigned char*>(a.Lt);
+  P.Ld = static_cast<const unsigned char*>(a.Ld);
+  P.x = a.x; P.u_acc = a.u_acc; P.u_res = a.u_res; P.temp = a.temp;
   P.B = B; P.gamma = gamma; P.V = V; P.R = R;
+  P.gs = (a.kind == CALL_SAMPLE) ? gamma : 0;  // draft rows the reduce streams
+  P.dstats = (a.kind == CALL_CACHED && gamma > 0) ? a.dstats : nullptr;
   P.ch1 = ch1; P.nch1 = nch1;
   P.np1 = nch1 * GeoReduce::GW;
   P.tasks = (long long)B * R * nch1;
@@ -1769,16 +2151,17 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
   // each residual warp takes a contiguous sub-range of a phase-2 chunk, a
   // whole number of 16-byte vectors long (the last one may be shorter)
   P.sub = round_up((chmax2 + GeoResidual::GW - 1) / GeoResidual::GW, 8);
-  P.out_tokens = out_tokens; P.out_n = out_n; P.out_p = out_p; P.out_Z = out_Z;
-  P.status = status;
-  unsigned char* w = static_cast<unsigned char*>(ws);
+  P.out_tokens = a.out_tokens; P.out_n = a.out_n; P.out_p = a.out_p; P.out_Z = a.out_Z;
+  P.out_stats = a.out_stats; P.col = a.col; P.ncols = a.ncols;
+  P.status = a.status;
+  unsigned char* w = static_cast<unsigned char*>(a.ws);
   P.ctrl = reinterpret_cast<Ctrl*>(w + L.ctrl);
   P.part = reinterpret_cast<Partial*>(w + L.part);
   P.rec = reinterpret_cast<Record*>(w + L.rec);
   P.mass = reinterpret_cast<Mass*>(w + L.mass);
-  if ((long long)B * P.nch2 > 0x7fffffffLL) return SV_ERR_INVALID_ARG;
+  if ((long long)B * P.nch2 > 0x7fffffffLL || units > 0x7fffffffLL) return SV_ERR_INVALID_ARG;
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t st = static_cast<cudaStream_t>(a.stream);
   const unsigned grid = unsigned(min((long long)sms, P.tasks));
   const unsigned gres = unsigned(min((long long)sms, (long long)B * P.nch2));
   // profiling aid: event j after the j-th kernel (event 0 before the first)
@@ -1788,10 +2171,16 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
   };
   mark(0);
   cudaError_t e = cudaSuccess;
-  auto run = [&](auto reduce_k, auto decide_k, auto residual_k, auto draw_k) {
+  auto run = [&](auto reduce_k, auto decide_k, auto residual_k, auto draw_k, auto sample_k) {
     reduce_k<<<grid, NTHR, smem_bytes<GeoReduce>(), st>>>(P);
     e = cudaGetLastError();
     mark(1);
+    if (draft) {
+      if (e == cudaSuccess)
+        e = launch_after(sample_k, unsigned(units), 32 * DRAW_WARPS, 0, st, P);
+      mark(2);
+      return;
+    }
     if (e == cudaSuccess)
       e = launch_after(decide_k, unsigned(B), 32 * DECIDE_WARPS, 0, st, P, greedy);
     mark(2);
@@ -1801,22 +2190,48 @@ int launch(bool greedy, const void* Lt, const void* Ld, const int32_t* x, const 
     if (e == cudaSuccess) e = launch_after(draw_k, unsigned(B), 32 * DRAW_WARPS, 0, st, P);
     mark(4);
   };
-  if (dtype == SV_F32) {
+  // the reduce streams draft rows only for CALL_SAMPLE; the other paths pair
+  // target chunks in its slots
+  const bool pairs = a.kind != CALL_SAMPLE;
+  if (a.dtype == SV_F32) {
     if (greedy)
-      run(sv_reduce<SV_F32, true>, sv_decide<SV_F32, true>, sv_residual<SV_F32>, sv_draw<SV_F32>);
+      run(sv_reduce<SV_F32, true, true>, sv_decide<SV_F32, true>, sv_residual<SV_F32>,
+          sv_draw<SV_F32>, sv_sample<SV_F32>);
+    else if (pairs)
+      run(sv_reduce<SV_F32, false, true>, sv_decide<SV_F32, false>, sv_residual<SV_F32>,
+          sv_draw<SV_F32>, sv_sample<SV_F32>);
     else
-      run(sv_reduce<SV_F32, false>, sv_decide<SV_F32, false>, sv_residual<SV_F32>,
-          sv_draw<SV_F32>);
+      run(sv_reduce<SV_F32, false, false>, sv_decide<SV_F32, false>, sv_residual<SV_F32>,
+          sv_draw<SV_F32>, sv_sample<SV_F32>);
   } else {
     if (greedy)
-      run(sv_reduce<SV_BF16, true>, sv_decide<SV_BF16, true>, sv_residual<SV_BF16>,
-          sv_draw<SV_BF16>);
+      run(sv_reduce<SV_BF16, true, true>, sv_decide<SV_BF16, true>, sv_residual<SV_BF16>,
+          sv_draw<SV_BF16>, sv_sample<SV_BF16>);
+    else if (pairs)
+      run(sv_reduce<SV_BF16, false, true>, sv_decide<SV_BF16, false>, sv_residual<SV_BF16>,
+          sv_draw<SV_BF16>, sv_sample<SV_BF16>);
     else
-      run(sv_reduce<SV_BF16, false>, sv_decide<SV_BF16, false>, sv_residual<SV_BF16>,
-          sv_draw<SV_BF16>);
+      run(sv_reduce<SV_BF16, false, false>, sv_decide<SV_BF16, false>, sv_residual<SV_BF16>,
+          sv_draw<SV_BF16>, sv_sample<SV_BF16>);
   }
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
+}
+
+Call sampling_call(const void* target_logits, const void* draft_logits,
+                   const int32_t* draft_tokens, const float* u_accept, const float* u_resample,
+                   const float* temperature, int B, int gamma, int V, int dtype,
+                   int32_t* out_tokens, int32_t* out_num_accepted, void* workspace,
+                   size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  Call c;
+  c.kind = CALL_SAMPLE;
+  c.Lt = target_logits; c.Ld = draft_logits; c.x = draft_tokens;
+  c.u_acc = u_accept; c.u_res = u_resample; c.temp = temperature;
+  c.B = B; c.gamma = gamma; c.V = V; c.dtype = dtype;
+  c.out_tokens = out_tokens; c.out_n = out_num_accepted;
+  c.ws = workspace; c.ws_bytes = workspace_bytes;
+  c.status = dev_status; c.stream = stream;
+  return c;
 }
 
 }  // namespace
@@ -1836,33 +2251,77 @@ int sv_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
              : SV_ERR_CUDA;
 }
 
+
 int spec_verify_diag(const void* target_logits, const void* draft_logits,
                      const int32_t* draft_tokens, const float* u_accept,
                      const float* u_resample, const float* temperature, int B, int gamma,
                      int V, int dtype, int32_t* out_tokens, int32_t* out_num_accepted,
                      float* out_p, float* out_Z, void* workspace, size_t workspace_bytes,
                      int32_t* dev_status, void* stream) {
-  return launch(false, target_logits, draft_logits, draft_tokens, u_accept, u_resample,
-                temperature, B, gamma, V, dtype, out_tokens, out_num_accepted, out_p, out_Z,
-                workspace, workspace_bytes, dev_status, stream);
+  Call c = sampling_call(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                         temperature, B, gamma, V, dtype, out_tokens, out_num_accepted,
+                         workspace, workspace_bytes, dev_status, stream);
+  c.out_p = out_p;
+  c.out_Z = out_Z;
+  return launch(c);
 }
 
 int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
                 const float* u_accept, const float* u_resample, const float* temperature, int B,
                 int gamma, int V, int dtype, int32_t* out_tokens, int32_t* out_num_accepted,
                 void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  return launch(false, target_logits, draft_logits, draft_tokens, u_accept, u_resample,
-                temperature, B, gamma, V, dtype, out_tokens, out_num_accepted, nullptr, nullptr,
-                workspace, workspace_bytes, dev_status, stream);
+  return launch(sampling_call(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                              temperature, B, gamma, V, dtype, out_tokens, out_num_accepted,
+                              workspace, workspace_bytes, dev_status, stream));
+}
+
+int spec_verify_cached(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, const float* draft_stats,
+                       const float* u_accept, const float* u_resample, const float* temperature,
+                       int B, int gamma, int V, int dtype, int32_t* out_tokens,
+                       int32_t* out_num_accepted, float* out_p, float* out_Z, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  Call c = sampling_call(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                         temperature, B, gamma, V, dtype, out_tokens, out_num_accepted,
+                         workspace, workspace_bytes, dev_status, stream);
+  c.kind = CALL_CACHED;
+  c.dstats = draft_stats;
+  c.out_p = out_p;
+  c.out_Z = out_Z;
+  return launch(c);
 }
 
 int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int gamma,
                        int V, int dtype, int32_t* out_tokens, int32_t* out_num_accepted,
                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
                        void* stream) {
-  return launch(true, target_logits, nullptr, draft_tokens, nullptr, nullptr, nullptr, B, gamma,
-                V, dtype, out_tokens, out_num_accepted, nullptr, nullptr, workspace,
-                workspace_bytes, dev_status, stream);
+  Call c;
+  c.kind = CALL_GREEDY;
+  c.Lt = target_logits; c.x = draft_tokens;
+  c.B = B; c.gamma = gamma; c.V = V; c.dtype = dtype;
+  c.out_tokens = out_tokens; c.out_n = out_num_accepted;
+  c.ws = workspace; c.ws_bytes = workspace_bytes;
+  c.status = dev_status; c.stream = stream;
+  return launch(c);
+}
+
+size_t sv_draft_workspace_bytes(int B, int n, int V) {
+  if (B < 0 || n < 1 || n > SV_MAX_GAMMA || V < 1) return 0;
+  return make_layout(B, n - 1, V).total;
+}
+
+int sv_draft_sample(const void* draft_logits, const float* u_draft, const float* temperature,
+                    int B, int n, int V, int dtype, int col, int ncols, int32_t* out_tokens,
+                    float* out_stats, void* workspace, size_t workspace_bytes,
+                    int32_t* dev_status, void* stream) {
+  Call c;
+  c.kind = CALL_DRAFT;
+  c.Lt = draft_logits; c.u_res = u_draft; c.temp = temperature;
+  c.B = B; c.n = n; c.V = V; c.dtype = dtype; c.col = col; c.ncols = ncols;
+  c.out_tokens = out_tokens; c.out_stats = out_stats;
+  c.ws = workspace; c.ws_bytes = workspace_bytes;
+  c.status = dev_status; c.stream = stream;
+  return launch(c);
 }
 
 }  // extern "C"
@@ -1905,9 +2364,9 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
     return SV_ERR_WORKSPACE;  // too large for the built-in scratch
   if (B <= 0 || (dtype != SV_F32 && dtype != SV_BF16) || gamma < 0 || gamma > SV_MAX_GAMMA ||
       V < 1)  // argument errors and the empty batch: no scratch needed
-    return launch(false, target_logits, draft_logits, draft_tokens, u_accept, u_resample,
-                  temperature, B, gamma, V, dtype, out_tokens, out_num_accepted, nullptr,
-                  nullptr, nullptr, 0, dev_status, stream);
+    return launch(sampling_call(target_logits, draft_logits, draft_tokens, u_accept,
+                                u_resample, temperature, B, gamma, V, dtype, out_tokens,
+                                out_num_accepted, nullptr, 0, dev_status, stream));
   void* scratch = nullptr;
   int rc = noalloc_scratch(&scratch);
   if (rc != SV_OK) return rc;
@@ -1915,9 +2374,9 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
   // the control block starts every call in its ready state (calls that may
   // overlap are the caller's to serialise)
   if (cudaMemsetAsync(scratch, 0, sizeof(Ctrl), st) != cudaSuccess) return SV_ERR_CUDA;
-  return launch(false, target_logits, draft_logits, draft_tokens, u_accept, u_resample,
-                temperature, B, gamma, V, dtype, out_tokens, out_num_accepted, nullptr, nullptr,
-                scratch, SV_NOALLOC_MAX_WORKSPACE, dev_status, stream);
+  return launch(sampling_call(target_logits, draft_logits, draft_tokens, u_accept, u_resample,
+                              temperature, B, gamma, V, dtype, out_tokens, out_num_accepted,
+                              scratch, SV_NOALLOC_MAX_WORKSPACE, dev_status, stream));
 }
 
 int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests) {
@@ -1948,6 +2407,6 @@ const char* sv_error_string(int code) {
   }
 }
 
-int sv_version(void) { return 300; }
+int sv_version(void) { return 400; }
 
 }  // extern "C"

@@ -53,6 +53,7 @@ CONFIGS = {
 BASE_SEED = 20260
 
 _TAG_TARGET, _TAG_DRAFT, _TAG_AUX, _TAG_TOKEN, _TAG_UNIFORM, _TAG_TEMP = range(6)
+_TAG_DRAFT_UNIFORM, _TAG_KV = 6, 7
 
 
 @dataclasses.dataclass
@@ -209,3 +210,8 @@ def custom_config(B: int, gamma: int, V: int, dtype: str = "bf16", kind: str = "
     d.update(defaults)
     d.update(kw)
     return d
+
+
+def draft_uniforms(B: int, n: int, seed: int, set_index: int = 0) -> np.ndarray:
+    """u_draft [B][n]: fp32 uniforms in [0, 1) for sampling the draft rows."""
+    return rng_for(seed, set_index, _TAG_DRAFT_UNIFORM).random((B, n), dtype=np.float32)

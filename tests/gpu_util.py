@@ -121,3 +121,95 @@ def compare_greedy(got: dict, ref: dict) -> None:
     assert np.array_equal(got["n"], ref["n"]), "greedy counts differ"
     want = expected_status(ref["flags"])
     assert got["status"] == want, f"status {got['status']:#x} != {want:#x}"
+
+
+# ------------------------------------------------------------ draft side
+
+S_RTOL = 1e-5  # the draft rows' normaliser S
+
+
+def run_draft(L, u, temp, dtype: int, ncols: int | None = None, col: int = 0, ws=None,
+              out=None) -> dict:
+    """sv_draft_sample on host arrays L [B][n][V] (float32 or bf16 bits), u [B][n], temp [B];
+    returns tokens [B][ncols], stats [B][ncols][2] and the status word."""
+    B, n, V = L.shape
+    ncols = n if ncols is None else ncols
+    Ld = torch.from_numpy(np.ascontiguousarray(L)).to(DEV)
+    if dtype == synth.BF16:
+        Ld = Ld.view(torch.bfloat16)
+    ud = torch.from_numpy(np.ascontiguousarray(u, dtype=np.float32)).to(DEV)
+    td = torch.from_numpy(np.ascontiguousarray(temp, dtype=np.float32)).to(DEV)
+    if out is None:
+        out = (torch.full((B, ncols), -7, dtype=torch.int32, device=DEV),
+               torch.full((B, ncols, 2), -7.0, dtype=torch.float32, device=DEV))
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    if ws is None:
+        ws = binding.make_draft_workspace(B, n, V, DEV)
+    binding.sv_draft_sample(Ld, ud, td, out[0], out[1], ws, col=col, dev_status=st)
+    torch.cuda.synchronize()
+    return dict(tokens=out[0].cpu().numpy(), stats=out[1].cpu().numpy(), status=int(st.item()),
+                out=out)
+
+
+def _cdf_edges(L, dtype, temp, b, i, v):
+    """fp64 CDF of draft row (b, i) of the stored logits just before and at
+    token v, normalised: the interval of u that selects v."""
+    w = synth.widen(L[b, i], dtype) / float(temp[b])
+    p = np.exp(w - w.max())
+    c = np.cumsum(p) / p.sum()
+    return (c[v - 1] if v > 0 else 0.0), c[v]
+
+
+def compare_draft(got: dict, ref: dict, col: int = 0, L=None, dtype=None, temp=None,
+                  u=None) -> dict:
+    """Draft tokens bit-exact except at rows the oracle flags as near a CDF
+    edge; m exact (the stored maximum); S within relative S_RTOL; invalid rows
+    -1 with NaN stats.  Given the rows (L, dtype, temp, u), a differing token
+    must still be a valid draw: u within 1e-6 of the token's CDF interval."""
+    n = ref["tokens"].shape[1]
+    tok = got["tokens"][:, col:col + n]
+    m, S = got["stats"][:, col:col + n, 0], got["stats"][:, col:col + n, 1]
+    inv = (ref["flags"] & oracle.INVALID_ANY) != 0
+    near = (ref["flags"] & oracle.NEAR_SAMPLE) != 0
+    assert np.all(tok[inv] == -1) and np.all(np.isnan(S[inv])) and np.all(np.isnan(m[inv]))
+    ok = ~inv
+    assert np.all(m[ok].astype(np.float64) == ref["m"][ok]), "row maxima differ"
+    rel = np.abs(S[ok].astype(np.float64) - ref["S"][ok]) / ref["S"][ok]
+    assert np.all(rel <= S_RTOL), f"S: max rel err {rel.max()}"
+    mism = ok & (tok != ref["tokens"])
+    bad = mism & ~near
+    assert not bad.any(), (f"{int(bad.sum())} draft tokens differ, e.g. "
+                           f"{np.argwhere(bad)[0]}: gpu {tok[bad][0]} oracle {ref['tokens'][bad][0]}")
+    if L is not None:
+        for b, i in np.argwhere(mism):
+            lo, hi = _cdf_edges(L, dtype, temp, b, i, int(tok[b, i]))
+            uu = float(u[b, i])
+            assert lo - 1e-6 <= uu < hi + 1e-6, (b, i, lo, uu, hi)
+    want = 0
+    if np.any(ref["flags"] & oracle.INVALID_NONFINITE):
+        want |= binding.SV_ST_NONFINITE
+    if np.any(ref["flags"] & oracle.INVALID_TEMP):
+        want |= binding.SV_ST_BAD_TEMP
+    assert got["status"] == want, f"status {got['status']:#x} != {want:#x}"
+    return dict(rows=int(ok.sum()), near=int(near.sum()), mismatches=int(mism.sum()),
+                max_rel_S=float(rel.max()) if rel.size else 0.0)
+
+
+def run_cached(inp: synth.Inputs, stats: np.ndarray, d: dict | None = None, ws=None) -> dict:
+    """spec_verify_cached with the draft normalisers `stats` [B][gamma][2]."""
+    d = d or to_dev(inp)
+    B, g = inp.B, inp.gamma
+    tok = torch.full((B, g + 1), -7, dtype=torch.int32, device=DEV)
+    n = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+    p = torch.full((B, g, 2), -7.0, dtype=torch.float32, device=DEV)
+    Z = torch.full((B,), -7.0, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sd = torch.from_numpy(np.ascontiguousarray(stats, dtype=np.float32)).to(DEV)
+    if ws is None:
+        ws = binding.make_workspace(B, g, inp.V, DEV)
+    binding.spec_verify_cached(d["Lt"], d["Ld"] if g > 0 else None, d["x"] if g > 0 else None,
+                               sd if g > 0 else None, d["u_acc"] if g > 0 else None, d["u_res"],
+                               d["temp"], tok, n, ws, out_p=p, out_Z=Z, dev_status=st)
+    torch.cuda.synchronize()
+    return dict(tokens=tok.cpu().numpy(), n=n.cpu().numpy(), p=p.cpu().numpy(),
+                Z=Z.cpu().numpy(), status=int(st.item()))

@@ -100,3 +100,41 @@ def test_stage_events_validation(L):
     nul = (ctypes.c_void_p * 2)(FAKE, None)
     assert L.sv_set_stage_events(nul, 2) == binding.SV_ERR_INVALID_ARG   # a NULL handle
     assert L.sv_set_stage_events(None, 0) == binding.SV_OK               # off
+
+
+def test_draft_and_cached_validation(L):
+    ws = 1 << 30
+    assert binding.sv_draft_workspace_bytes(4, 0, 100) == 0
+    assert binding.sv_draft_workspace_bytes(4, 33, 100) == 0
+    assert binding.sv_draft_workspace_bytes(4, 3, 100) == binding.sv_workspace_bytes(4, 2, 100)
+
+    def draft(**kw):
+        a = dict(L=FAKE, u=FAKE, T=FAKE, B=2, n=3, V=100, dt=1, col=0, ncols=3, tok=FAKE,
+                 st=FAKE, ws=FAKE, wsb=ws)
+        a.update(kw)
+        return L.sv_draft_sample(a["L"], a["u"], a["T"], a["B"], a["n"], a["V"], a["dt"],
+                                 a["col"], a["ncols"], a["tok"], a["st"], a["ws"], a["wsb"],
+                                 None, None)
+    assert draft(dt=3) == binding.SV_ERR_DTYPE
+    assert draft(n=0) == binding.SV_ERR_INVALID_ARG
+    assert draft(col=-1) == binding.SV_ERR_INVALID_ARG
+    assert draft(col=1) == binding.SV_ERR_INVALID_ARG       # col + n > ncols
+    assert draft(st=None) == binding.SV_ERR_INVALID_ARG
+    assert draft(u=None) == binding.SV_ERR_INVALID_ARG
+    assert draft(L=FAKE + 1) == binding.SV_ERR_INVALID_ARG  # bf16 needs 2-byte alignment
+    assert draft(wsb=64) == binding.SV_ERR_WORKSPACE
+    assert draft(B=0) == binding.SV_OK
+
+    def cached(**kw):
+        a = dict(Lt=FAKE, Ld=FAKE, x=FAKE, ds=FAKE, ua=FAKE, ur=FAKE, T=FAKE, B=2, g=3, V=100,
+                 dt=0, tok=FAKE, n=FAKE, ws=FAKE, wsb=ws)
+        a.update(kw)
+        return L.spec_verify_cached(a["Lt"], a["Ld"], a["x"], a["ds"], a["ua"], a["ur"], a["T"],
+                                    a["B"], a["g"], a["V"], a["dt"], a["tok"], a["n"], None,
+                                    None, a["ws"], a["wsb"], None, None)
+    assert cached(ds=None) == binding.SV_ERR_INVALID_ARG
+    assert cached(ds=FAKE + 4) == binding.SV_ERR_INVALID_ARG  # stats pairs need 8-byte alignment
+    assert cached(g=0, ds=None, Ld=None, x=None, ua=None, wsb=64) == binding.SV_ERR_WORKSPACE
+    if not __import__("torch").cuda.is_available():
+        assert cached() == binding.SV_ERR_CUDA
+        assert draft() == binding.SV_ERR_CUDA
