@@ -37,6 +37,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "specverify.h"
 
@@ -544,7 +545,7 @@ struct Share {
   float kf, kf2;
   int pair, n2;
 };
-template <int DT, class G, bool CONTIG>
+template <int DT, class G, bool CONTIG, bool PAIRS>
 __device__ __forceinline__ void load_share(const Desc& d, const unsigned char* slot, bool has_d,
                                            int wg, int lane, Share<G::MAXV>& sh) {
   using E = Elem<DT>;
@@ -573,7 +574,7 @@ __device__ __forceinline__ void load_share(const Desc& d, const unsigned char* s
   sh.b = d.b; sh.i = d.i; sh.c = d.c; sh.e0 = d.e0; sh.n = d.n;
   sh.head_t = d.head_t; sh.nb_t = d.nb_t; sh.head_d = d.head_d; sh.nb_d = d.nb_d;
   sh.kf = d.kf;
-  if (CONTIG) {
+  if (PAIRS) {
     sh.kf2 = d.kf2;
     sh.pair = d.pair;
     sh.n2 = d.n2;
@@ -594,16 +595,16 @@ __device__ __forceinline__ void next_chunk(const Params& P, int& b, int& i, int&
 // chunk (PAIRS true, when the slot holds a pair), with its own element count
 // and temperature.  The body vectors are in `sh`; consumer warp 0 also takes
 // the few unaligned head elements, and the tail elements go to warp GW - 1
-// (contiguous map, PAIRS) or warp 0 (interleaved map), from global memory.
-// Each lane sums relative to its own maximum; the lanes' sums are rescaled to
-// the warp's.
-template <int DT, int MAXV, int GW, bool PAIRS>
+// (contiguous map) or warp 0 (interleaved map), from global memory.  Each
+// lane sums relative to its own maximum; the lanes' sums are rescaled to the
+// warp's.
+template <int DT, int MAXV, int GW, bool PAIRS, bool CONTIG>
 __device__ float4 reduce_share_ms(const Params& P, const Share<MAXV>& sh, int wg, int lane) {
   using E = Elem<DT>;
   const bool has_d = PAIRS ? sh.pair != 0 : sh.i < P.gs;
   const float kf_t = sh.kf, kf_d = PAIRS ? sh.kf2 : sh.kf;
   float ht = -INFINITY, tt = -INFINITY, hd = -INFINITY, td = -INFINITY;
-  if (wg == 0 || wg == (PAIRS ? GW - 1 : 0)) {
+  if (wg == 0 || wg == (CONTIG ? GW - 1 : 0)) {
     const int n_t = sh.n, n_d = PAIRS ? sh.n2 : sh.n;
     const unsigned char* gt =
         P.Lt + ((size_t(sh.b) * P.R + sh.i) * size_t(P.V) + sh.e0) * E::ES;
@@ -621,7 +622,7 @@ __device__ float4 reduce_share_ms(const Params& P, const Share<MAXV>& sh, int wg
       if (lane < sh.head_t) ht = E::load(gt, lane);
       if (has_d && lane < sh.head_d) hd = E::load(gd, lane);
     }
-    if (wg == (PAIRS ? GW - 1 : 0)) {
+    if (wg == (CONTIG ? GW - 1 : 0)) {
       if (lane < n_t - sh.head_t - sh.nb_t) tt = E::load(gt, sh.head_t + sh.nb_t + lane);
       if (has_d && lane < n_d - sh.head_d - sh.nb_d) td = E::load(gd, sh.head_d + sh.nb_d + lane);
     }
@@ -672,10 +673,10 @@ __device__ float4 reduce_share_ms(const Params& P, const Share<MAXV>& sh, int wg
 
 // This warp's (largest value, lowest index among its occurrences, NaN seen)
 // over its share of one target row chunk: body vectors `vec` (the slot's
-// first or second segment, this warp's run of it in the contiguous map), the
+// first or second segment, mapped to the threads as load_share maps it), the
 // chunk at `gseg` starting at element e0 of its row with `head` single
 // leading elements, nb body elements, n in all; indices are within the row.
-template <int DT, class G>
+template <int DT, class G, bool CONTIG>
 __device__ float4 reduce_share_argmax(const uint4 (&vec)[G::MAXV], const unsigned char* gseg,
                                       int e0, int head, int nb, int n, int wg, int lane) {
   using E = Elem<DT>;
@@ -690,7 +691,7 @@ __device__ float4 reduce_share_argmax(const uint4 (&vec)[G::MAXV], const unsigne
   }
 #pragma unroll
   for (int u = 0; u < MAXV; ++u) {
-    const int j = wg * pw + lane + 32 * u;
+    const int j = CONTIG ? wg * pw + lane + 32 * u : (wg * 32 + lane) + u * G::GW * 32;
     const uint4 v = vec[u];
     const float vm = E::vmax(v);
     if (vm != vm) {
@@ -706,7 +707,7 @@ __device__ float4 reduce_share_argmax(const uint4 (&vec)[G::MAXV], const unsigne
       bi = e0 + head + j * E::VEC + first;
     }
   }
-  if (wg == G::GW - 1) {
+  if (wg == (CONTIG ? G::GW - 1 : 0)) {
     const int t0 = head + nb;
     if (lane < n - t0) {
       const float l = E::load(gseg, t0 + lane);
@@ -833,6 +834,22 @@ __device__ void end_markers(const Params& P, SmemCtl<G>& C, long long seq) {
   }
 }
 
+// First task of CTA x of nb, splitting the reduce's tasks so that every CTA
+// streams about the same bytes: a chunk of a row that also streams its draft
+// row weighs 2, a target-only chunk 1.  A request's tasks weigh
+// w_req = nch1 * (R + gs): its first gs rows 2 * nch1 each, the rest nch1.
+// The CTA starts at the smallest task whose weight before it reaches
+// ceil(x / nb) of the total, found in closed form.
+__device__ __forceinline__ long long tasks_split(const Params& P, long long x, long long nb) {
+  const long long per_req = (long long)P.R * P.nch1;
+  const long long w_req = (long long)P.nch1 * (P.R + P.gs);
+  const long long w2 = 2LL * P.gs * P.nch1;  // weight of a request's two-row chunks
+  const long long target = (w_req * P.B * x + nb - 1) / nb;
+  const long long b = target / w_req, rem = target - b * w_req;
+  const long long t_in = rem <= w2 ? (rem + 1) / 2 : P.gs * (long long)P.nch1 + (rem - w2);
+  return b * per_req + t_in;
+}
+
 // Producer (one lane): this CTA's contiguous range of chunks, in order, into
 // the slot ring.  Chunk t is chunk t % nch1 of row t / nch1 (row = b * R + i).
 // A slot holds a target chunk and the same span of the draft row; where no
@@ -845,7 +862,7 @@ __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* 
   using G = GeoReduce;
   constexpr int NS = G::NS, SLOT = G::SLOT, HALF = G::HALF;
   const long long nb = gridDim.x;
-  const long long t0 = P.tasks * blockIdx.x / nb, t1 = P.tasks * (blockIdx.x + 1) / nb;
+  const long long t0 = tasks_split(P, blockIdx.x, nb), t1 = tasks_split(P, blockIdx.x + 1, nb);
   const long long row0 = t0 / P.nch1;
   int c = int(t0 - row0 * P.nch1);
   int b = int(row0 / P.R), i = int(row0 - (long long)b * P.R);
@@ -922,7 +939,7 @@ __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* 
 // Consumers: every warp loads its share of a slot into registers and hands
 // the slot back at once (so the producer can refill it while the share is
 // reduced), then publishes its own partial (two for a pair of target chunks).
-template <int DT, bool GREEDY, bool PAIRS>
+template <int DT, bool GREEDY, bool PAIRS, bool CONTIG>
 __device__ void consumer(const Params& P, SmemCtl<GeoReduce>& C, const unsigned char* slots) {
   using E = Elem<DT>;
   using G = GeoReduce;
@@ -939,7 +956,7 @@ __device__ void consumer(const Params& P, SmemCtl<GeoReduce>& C, const unsigned 
     const Desc& d = C.desc[s];
     if (d.end) return false;
     const bool second = PAIRS ? d.pair != 0 : d.i < P.gs;
-    load_share<DT, G, PAIRS>(d, slots + size_t(s) * SLOT, second, wg, lane, sh);
+    load_share<DT, G, CONTIG, PAIRS>(d, slots + size_t(s) * SLOT, second, wg, lane, sh);
     __syncwarp();
     if (lane == 0) mbar_arrive(&C.empty[s]);
     return true;
@@ -949,21 +966,22 @@ __device__ void consumer(const Params& P, SmemCtl<GeoReduce>& C, const unsigned 
     if (GREEDY) {
       const unsigned char* gt =
           P.Lt + ((size_t(sh.b) * P.R + sh.i) * size_t(P.V) + sh.e0) * E::ES;
-      out = reduce_share_argmax<DT, G>(sh.t, gt, sh.e0, sh.head_t, sh.nb_t, sh.n, wg, lane);
+      out = reduce_share_argmax<DT, G, CONTIG>(sh.t, gt, sh.e0, sh.head_t, sh.nb_t, sh.n, wg,
+                                               lane);
       if (sh.pair) {
         int b2 = sh.b, i2 = sh.i, c2 = sh.c;
         next_chunk(P, b2, i2, c2);
         const unsigned char* g2 =
             P.Lt + ((size_t(b2) * P.R + i2) * size_t(P.V) + size_t(c2) * P.ch1) * E::ES;
-        out2 = reduce_share_argmax<DT, G>(sh.d, g2, c2 * P.ch1, sh.head_d, sh.nb_d, sh.n2, wg,
-                                          lane);
+        out2 = reduce_share_argmax<DT, G, CONTIG>(sh.d, g2, c2 * P.ch1, sh.head_d, sh.nb_d,
+                                                  sh.n2, wg, lane);
       }
     } else if (PAIRS) {
-      const float4 r = reduce_share_ms<DT, G::MAXV, GW, true>(P, sh, wg, lane);
+      const float4 r = reduce_share_ms<DT, G::MAXV, GW, true, CONTIG>(P, sh, wg, lane);
       out = make_float4(r.x, r.y, -INFINITY, 0.f);
       out2 = make_float4(r.z, r.w, -INFINITY, 0.f);
     } else {
-      out = reduce_share_ms<DT, G::MAXV, GW, false>(P, sh, wg, lane);
+      out = reduce_share_ms<DT, G::MAXV, GW, false, CONTIG>(P, sh, wg, lane);
     }
     if (lane == 0) {
       Partial* dst = P.part + ((size_t(sh.b) * P.R + sh.i) * P.nch1 + sh.c) * GW + wg;
@@ -984,10 +1002,10 @@ __device__ void consumer(const Params& P, SmemCtl<GeoReduce>& C, const unsigned 
 }
 
 // GREEDY: chunk argmax instead of (max, sum); PAIRS: no draft rows are
-// streamed, a slot carries two target chunks and the warps' shares are
-// contiguous spans (greedy verification, given draft normalisers, draft
-// sampling).
-template <int DT, bool GREEDY, bool PAIRS>
+// streamed and a slot carries two target chunks (greedy verification, given
+// draft normalisers, draft sampling); CONTIG: the warps' shares are
+// contiguous spans of the row (draft sampling searches them).
+template <int DT, bool GREEDY, bool PAIRS, bool CONTIG>
 __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
   using G = GeoReduce;
   // every CTA of this grid is resident from the start (one per SM), so the
@@ -1013,7 +1031,7 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
   if (threadIdx.x < 32) {
     if (threadIdx.x == 0) producer<DT, GREEDY, PAIRS>(P, C, slots);
   } else {
-    consumer<DT, GREEDY, PAIRS>(P, C, slots);
+    consumer<DT, GREEDY, PAIRS, CONTIG>(P, C, slots);
   }
 }
 
@@ -2007,11 +2025,13 @@ bool prepare_kernel() {
   const int r = int(smem_bytes<GeoReduce>());
   return cudaFuncSetAttribute(sv_residual<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(smem_bytes<GeoResidual>())) == cudaSuccess &&
-         cudaFuncSetAttribute(sv_reduce<DT, false, false>,
+         cudaFuncSetAttribute(sv_reduce<DT, false, false, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, r) == cudaSuccess &&
-         cudaFuncSetAttribute(sv_reduce<DT, false, true>,
+         cudaFuncSetAttribute(sv_reduce<DT, false, true, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, r) == cudaSuccess &&
-         cudaFuncSetAttribute(sv_reduce<DT, true, true>,
+         cudaFuncSetAttribute(sv_reduce<DT, false, true, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, r) == cudaSuccess &&
+         cudaFuncSetAttribute(sv_reduce<DT, true, true, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, r) == cudaSuccess;
 }
 
@@ -2191,29 +2211,26 @@ int launch(const Call& a) {
     mark(4);
   };
   // the reduce streams draft rows only for CALL_SAMPLE; the other paths pair
-  // target chunks in its slots
-  const bool pairs = a.kind != CALL_SAMPLE;
-  if (a.dtype == SV_F32) {
+  // target chunks in its slots, and draft sampling needs contiguous shares
+  auto dispatch = [&](auto dt) {
+    constexpr int D = decltype(dt)::value;
     if (greedy)
-      run(sv_reduce<SV_F32, true, true>, sv_decide<SV_F32, true>, sv_residual<SV_F32>,
-          sv_draw<SV_F32>, sv_sample<SV_F32>);
-    else if (pairs)
-      run(sv_reduce<SV_F32, false, true>, sv_decide<SV_F32, false>, sv_residual<SV_F32>,
-          sv_draw<SV_F32>, sv_sample<SV_F32>);
+      run(sv_reduce<D, true, true, false>, sv_decide<D, true>, sv_residual<D>, sv_draw<D>,
+          sv_sample<D>);
+    else if (draft)
+      run(sv_reduce<D, false, true, true>, sv_decide<D, false>, sv_residual<D>, sv_draw<D>,
+          sv_sample<D>);
+    else if (a.kind == CALL_CACHED)
+      run(sv_reduce<D, false, true, false>, sv_decide<D, false>, sv_residual<D>, sv_draw<D>,
+          sv_sample<D>);
     else
-      run(sv_reduce<SV_F32, false, false>, sv_decide<SV_F32, false>, sv_residual<SV_F32>,
-          sv_draw<SV_F32>, sv_sample<SV_F32>);
-  } else {
-    if (greedy)
-      run(sv_reduce<SV_BF16, true, true>, sv_decide<SV_BF16, true>, sv_residual<SV_BF16>,
-          sv_draw<SV_BF16>, sv_sample<SV_BF16>);
-    else if (pairs)
-      run(sv_reduce<SV_BF16, false, true>, sv_decide<SV_BF16, false>, sv_residual<SV_BF16>,
-          sv_draw<SV_BF16>, sv_sample<SV_BF16>);
-    else
-      run(sv_reduce<SV_BF16, false, false>, sv_decide<SV_BF16, false>, sv_residual<SV_BF16>,
-          sv_draw<SV_BF16>, sv_sample<SV_BF16>);
-  }
+      run(sv_reduce<D, false, false, false>, sv_decide<D, false>, sv_residual<D>, sv_draw<D>,
+          sv_sample<D>);
+  };
+  if (a.dtype == SV_F32)
+    dispatch(std::integral_constant<int, SV_F32>());
+  else
+    dispatch(std::integral_constant<int, SV_BF16>());
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
 }
