@@ -7,8 +7,8 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "specverify.cu")
-HEADER = os.path.join(ROOT, "include", "specverify.h")
+SRCS = [os.path.join(PKG, "csrc", f) for f in ("specverify.cu", "kvcache.cu")]
+HEADERS = [os.path.join(ROOT, "include", f) for f in ("specverify.h", "svkv.h")]
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libspecverify.so")
 
@@ -27,7 +27,7 @@ def up_to_date() -> bool:
     if not os.path.exists(LIB_PATH):
         return False
     t = os.path.getmtime(LIB_PATH)
-    return all(os.path.getmtime(p) <= t for p in (SRC, HEADER, __file__))
+    return all(os.path.getmtime(p) <= t for p in (*SRCS, *HEADERS, __file__))
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
@@ -35,7 +35,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
         return LIB_PATH
     os.makedirs(OUT_DIR, exist_ok=True)
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *NVCC_FLAGS, *(extra_flags or []), "-I", os.path.join(ROOT, "include"), SRC,
+    cmd = [_nvcc(), *NVCC_FLAGS, *(extra_flags or []), "-I", os.path.join(ROOT, "include"), *SRCS,
            "-o", tmp]
     if verbose:
         print(" ".join(cmd))

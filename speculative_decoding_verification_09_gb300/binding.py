@@ -18,12 +18,15 @@ SV_F32, SV_BF16 = 0, 1
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_DTYPE, SV_ERR_CUDA, SV_ERR_WORKSPACE = range(5)
 SV_ST_NONFINITE, SV_ST_BAD_TOKEN, SV_ST_BAD_TEMP = 0x1, 0x2, 0x4
 SV_ST_TIMEOUT, SV_ST_WORKSPACE, SV_ST_DEGENERATE = 0x8, 0x10, 0x20
+SV_ST_BAD_LENGTH = 0x40
 SV_MAX_GAMMA = 32
 
 EXPORTED = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_diag",
             "spec_verify_greedy", "spec_verify_noalloc", "spec_verify_cached",
             "sv_draft_workspace_bytes", "sv_draft_sample", "sv_set_tuning",
-            "sv_set_stage_events", "sv_error_string", "sv_version")
+            "sv_set_stage_events", "sv_error_string", "sv_version",
+            "sv_kv_commit", "sv_kv_valid_slots", "sv_window_cols", "sv_window_block_table",
+            "sv_window_seq_lens_host")
 SV_NOALLOC_MAX_WORKSPACE = 16 << 20
 
 _lib = None
@@ -52,13 +55,20 @@ def lib() -> ctypes.CDLL:
         L.sv_draft_workspace_bytes.argtypes = [I, I, I]
         L.sv_draft_workspace_bytes.restype = Z
         L.sv_draft_sample.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, Z, P, P]
+        L.sv_kv_commit.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P]
+        L.sv_kv_valid_slots.argtypes = [P, I, I, I, P, P, P, P]
+        L.sv_window_cols.argtypes = [I, I]
+        L.sv_window_block_table.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
+        L.sv_window_seq_lens_host.argtypes = [P, I, I, I, I, P]
         L.sv_set_tuning.argtypes = [I, I, I]
         L.sv_set_stage_events.argtypes = [P, I]
         L.sv_error_string.argtypes = [I]
         L.sv_error_string.restype = ctypes.c_char_p
         for name in ("sv_workspace_init", "spec_verify", "spec_verify_diag",
                      "spec_verify_greedy", "spec_verify_noalloc", "spec_verify_cached",
-                     "sv_draft_sample", "sv_set_tuning", "sv_set_stage_events", "sv_version"):
+                     "sv_draft_sample", "sv_set_tuning", "sv_set_stage_events", "sv_version",
+                     "sv_kv_commit", "sv_kv_valid_slots", "sv_window_cols",
+                     "sv_window_block_table", "sv_window_seq_lens_host"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -252,3 +262,69 @@ def spec_verify_cached(target_logits, draft_logits, draft_tokens, draft_stats, u
         _dev(out_p, torch.float32, "out_p"), _dev(out_Z, torch.float32, "out_Z"),
         _dev(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _dev(dev_status, torch.int32, "dev_status"), _stream(stream, target_logits.device)))
+
+
+# ------------------------------------------------------------ KV-cache steps
+
+def sv_kv_commit(k_pool, v_pool, k_new, v_new, num_accepted, pos, sink: int, window: int,
+                 dev_status=None, stream=None) -> None:
+    """Commit the accepted staged entries to a sink + ring KV cache.
+    k_pool/v_pool [B][LH][sink+window][D], k_new/v_new [B][LH][R][D] (any
+    element type, D * element size a multiple of 16); num_accepted [B] and
+    pos [B] int32 (pos is advanced in place)."""
+    if k_pool.dim() != 4 or k_new.dim() != 4:
+        raise SpecVerifyError("pools must be [B][LH][sink+window][D], staged entries [B][LH][R][D]")
+    B, LH, C, D = k_pool.shape
+    R = k_new.shape[2]
+    if (tuple(v_pool.shape) != tuple(k_pool.shape) or tuple(v_new.shape) != tuple(k_new.shape)
+            or tuple(k_new.shape) != (B, LH, R, D) or C != sink + window):
+        raise SpecVerifyError("KV shapes disagree")
+    if len({k_pool.dtype, v_pool.dtype, k_new.dtype, v_new.dtype}) != 1:
+        raise SpecVerifyError("KV buffers must share one dtype")
+    _check(lib().sv_kv_commit(
+        _dev(k_pool, None, "k_pool"), _dev(v_pool, None, "v_pool"), _dev(k_new, None, "k_new"),
+        _dev(v_new, None, "v_new"), _dev(num_accepted, torch.int32, "num_accepted"),
+        _dev(pos, torch.int32, "pos"), B, LH, R, D * k_pool.element_size(), sink, window,
+        _dev(dev_status, torch.int32, "dev_status"), _stream(stream, k_pool.device)))
+
+
+def sv_kv_valid_slots(pos, sink: int, window: int, out_slots, out_len, dev_status=None,
+                      stream=None) -> None:
+    """Valid physical slots of every request in logical order: out_slots
+    [B][sink+window] (-1 padded) and out_len [B], int32."""
+    B = pos.shape[0]
+    _check(lib().sv_kv_valid_slots(
+        _dev(pos, torch.int32, "pos"), B, sink, window, _dev(out_slots, torch.int32, "out_slots"),
+        _dev(out_len, torch.int32, "out_len"), _dev(dev_status, torch.int32, "dev_status"),
+        _stream(stream, pos.device)))
+
+
+def sv_window_cols(window: int, block_size: int) -> int:
+    return int(lib().sv_window_cols(window, block_size))
+
+
+def sv_window_block_table(seq_lens, block_table, window: int, block_size: int,
+                          future_offset: int, out_seq_lens, out_block_table,
+                          out_start_block=None, dev_status=None, stream=None) -> None:
+    """Draft KV sliding window on the device: windowed lengths and the
+    zero-padded block-table clone [B][sv_window_cols(window, block_size)]."""
+    B, full_cols = block_table.shape
+    _check(lib().sv_window_block_table(
+        _dev(seq_lens, torch.int32, "seq_lens"), _dev(block_table, torch.int32, "block_table"),
+        B, full_cols, window, block_size, future_offset,
+        _dev(out_seq_lens, torch.int32, "out_seq_lens"),
+        _dev(out_block_table, torch.int32, "out_block_table"),
+        _dev(out_start_block, torch.int32, "out_start_block"),
+        _dev(dev_status, torch.int32, "dev_status"), _stream(stream, seq_lens.device)))
+
+
+def sv_window_seq_lens_host(seq_lens, window: int, block_size: int, future_offset: int):
+    """The same windowing of lengths on the host (for host-side mirrors):
+    an int32 numpy array in, a new one out."""
+    import numpy as np
+    src = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    out = np.empty_like(src)
+    _check(lib().sv_window_seq_lens_host(
+        src.ctypes.data_as(ctypes.c_void_p), int(src.size), window, block_size, future_offset,
+        out.ctypes.data_as(ctypes.c_void_p)))
+    return out

@@ -11,7 +11,7 @@ import __graft_entry__
 from speculative_decoding_verification_09_gb300 import binding
 from speculative_decoding_verification_09_gb300._build_lib import LIB_PATH, ROOT
 
-HEADER = os.path.join(ROOT, "include", "specverify.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in ("specverify.h", "svkv.h")]
 
 
 @pytest.fixture(scope="module")
@@ -22,7 +22,7 @@ def L():
 
 
 def header_functions():
-    text = open(HEADER).read()
+    text = "\n".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|void)\s*\**\s*"
                                  r"([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)))
@@ -138,3 +138,41 @@ def test_draft_and_cached_validation(L):
     if not __import__("torch").cuda.is_available():
         assert cached() == binding.SV_ERR_CUDA
         assert draft() == binding.SV_ERR_CUDA
+
+
+def test_kv_and_window_validation(L):
+    assert L.sv_window_cols(64, 16) == 5 and L.sv_window_cols(100, 16) == 8
+    assert L.sv_window_cols(5, 1) == 6 and L.sv_window_cols(0, 16) == -1
+    assert L.sv_window_cols(16, 0) == -1
+    # commit: row bytes a multiple of 16, window >= R, aligned buffers
+    def commit(**kw):
+        a = dict(kp=FAKE, vp=FAKE, kn=FAKE, vn=FAKE, na=FAKE, pos=FAKE, B=2, LH=3, R=4, rb=256,
+                 S=4, W=8)
+        a.update(kw)
+        return L.sv_kv_commit(a["kp"], a["vp"], a["kn"], a["vn"], a["na"], a["pos"], a["B"],
+                              a["LH"], a["R"], a["rb"], a["S"], a["W"], None, None)
+    assert commit(rb=24) == binding.SV_ERR_INVALID_ARG
+    assert commit(W=3) == binding.SV_ERR_INVALID_ARG
+    assert commit(S=-1) == binding.SV_ERR_INVALID_ARG
+    assert commit(kp=FAKE + 8) == binding.SV_ERR_INVALID_ARG
+    assert commit(pos=None) == binding.SV_ERR_INVALID_ARG
+    assert commit(B=0) == binding.SV_OK
+    assert L.sv_kv_valid_slots(FAKE, 2, 4, 0, FAKE, FAKE, None, None) == binding.SV_ERR_INVALID_ARG
+    assert L.sv_window_block_table(FAKE, FAKE, 2, 4, 64, 16, -1, FAKE, FAKE, None, None,
+                                   None) == binding.SV_ERR_INVALID_ARG
+    assert L.sv_window_block_table(FAKE, FAKE, 2, 0, 64, 16, 3, FAKE, FAKE, None, None,
+                                   None) == binding.SV_ERR_INVALID_ARG
+
+
+def test_window_host_mirror_matches_oracle():
+    """The host windowing of lengths (the library's CPU code for length
+    mirrors) against the oracle, including the page's unit-test example."""
+    import numpy as np
+    import oracle
+    got = binding.sv_window_seq_lens_host([10, 60, 200, 64], 64, 16, 3)
+    assert list(got) == [10, 60, 72, 64]
+    rng = np.random.default_rng(3)
+    for W, blk, K in ((64, 16, 3), (100, 16, 0), (7, 4, 2), (2048, 128, 5)):
+        seq = rng.integers(-3, 100000, size=500).astype(np.int32)
+        ref = oracle.window_block_table(seq, np.zeros((500, 1), np.int32), W, blk, K)
+        assert np.array_equal(binding.sv_window_seq_lens_host(seq, W, blk, K), ref["seq"])
