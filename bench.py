@@ -228,6 +228,77 @@ def measure_draft_side(binding, torch, dev, stream, sets, host_sets, B, g, V, ws
     }
 
 
+KV_MODEL = dict(layers=24, kv_heads=16, head_dim=128, elem_bytes=2, sink=4, window=256)
+
+
+def measure_kv_side(binding, torch, dev, stream, B, g, num_accepted, steps, warmup, peak) -> dict:
+    """The KV steps after verification, each timed alone over `steps` calls
+    (CUDA events on the stream): committing the accepted entries of a
+    1.8B-class target (24 layers x 16 KV heads, head dim 128, bf16; 4 sink
+    slots and a ring of 256) with the verification's own accepted counts, the
+    valid-slot lists, and a draft block-table window (W = 2048, block 128,
+    K = gamma, lengths up to 32768)."""
+    m = KV_MODEL
+    LH, D, S, W, R = m["layers"] * m["kv_heads"], m["head_dim"], m["sink"], m["window"], g + 1
+    pools = [torch.zeros(B, LH, S + W, D, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    staged = [torch.randn(B, LH, R, D, generator=gen, device=dev).to(torch.bfloat16)
+              for _ in range(2)]
+    pos = torch.zeros(B, dtype=torch.int32, device=dev)
+    slots = torch.empty(B, S + W, dtype=torch.int32, device=dev)
+    lens = torch.empty(B, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    blk, Wd = 128, 2048
+    full = 32768 // blk
+    seq = torch.randint(1, 32768, (B,), generator=gen, device=dev, dtype=torch.int32)
+    table = torch.randint(1, 1 << 30, (B, full), generator=gen, device=dev, dtype=torch.int32)
+    cols = binding.sv_window_cols(Wd, blk)
+    wseq = torch.empty(B, dtype=torch.int32, device=dev)
+    wtab = torch.empty(B, cols, dtype=torch.int32, device=dev)
+
+    def commit(i):
+        binding.sv_kv_commit(pools[0], pools[1], staged[0], staged[1], num_accepted, pos, S, W,
+                             dev_status=st, stream=stream)
+
+    def valid(i):
+        binding.sv_kv_valid_slots(pos, S, W, slots, lens, dev_status=st, stream=stream)
+
+    def window(i):
+        binding.sv_window_block_table(seq, table, Wd, blk, g, wseq, wtab, dev_status=st,
+                                      stream=stream)
+
+    def timed(fn):
+        for i in range(warmup):
+            fn(i)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for i in range(steps):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / steps
+
+    c_ms, v_ms, w_ms = timed(commit), timed(valid), timed(window)
+    entries = int((num_accepted.clamp(min=-1) + 1).sum().item())
+    moved = entries * LH * D * m["elem_bytes"] * 2 * 2  # K and V, read and written
+    st_v = int(st.item())
+    del pools, staged
+    return {
+        "model": f"{m['layers']} layers x {m['kv_heads']} KV heads x {D}, bf16, sink {S}, "
+                 f"ring {W}, B {B}, R {R}",
+        "sv_kv_commit": {"ms_per_call": c_ms, "entries_per_call": entries,
+                         "algorithmic_bytes": moved,
+                         "achieved_gbs": moved / (c_ms / 1e3) / 1e9,
+                         "frac_of_peak": moved / (c_ms / 1e3) / 1e9 / peak, "kernels": 2},
+        "sv_kv_valid_slots": {"ms_per_call": v_ms, "slots": B * (S + W)},
+        "sv_window_block_table": {"ms_per_call": w_ms, "B": B, "window": Wd, "block": blk,
+                                  "cols": cols},
+        "status": st_v,
+    }
+
+
 def run_ours(args) -> None:
     import torch
 
@@ -335,6 +406,11 @@ def run_ours(args) -> None:
     draft_side = None if (greedy or args.no_draft_side) else measure_draft_side(
         binding, torch, dev, stream, sets, host_sets, B, g, V, ws, out_tok, out_n, status,
         args.steps, args.warmup, peak)
+    kv_side = None
+    if not args.no_kv_side:
+        step(sets[0])  # the accepted counts of one verification drive the commit
+        kv_side = measure_kv_side(binding, torch, dev, stream, B, g, out_n.clone(), args.steps,
+                                  args.warmup, peak)
     per_launch = [a.elapsed_time(b) for a, b in ev]
     if pg:
         tt = torch.tensor([total_ms], device=dev)
@@ -419,7 +495,7 @@ def run_ours(args) -> None:
                                "right after the timed loop (same inputs)"},
         "stages_ms_extra_calls": stage_ms, "call_ms": launch_ms,
         "call_equivalent_gbs": logit_bytes / (launch_ms / 1e3) / 1e9,
-        "draft_side": draft_side,
+        "draft_side": draft_side, "kv_side": kv_side,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_kern * args.steps, "clocks": clk,
         "status": st, "wall_s_timed": t_wall,
         "tuning": {"chunk": args.chunk},
@@ -444,6 +520,8 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-draft-side", action="store_true",
                     help="skip timing sv_draft_sample and spec_verify_cached")
+    ap.add_argument("--no-kv-side", action="store_true",
+                    help="skip timing the KV commit, valid slots and block-table window")
     ap.add_argument("--cpu-requests", type=int, default=256)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="approximate seconds of oracle work for cpu_baseline")
