@@ -231,7 +231,8 @@ def measure_draft_side(binding, torch, dev, stream, sets, host_sets, B, g, V, ws
 KV_MODEL = dict(layers=24, kv_heads=16, head_dim=128, elem_bytes=2, sink=4, window=256)
 
 
-def measure_kv_side(binding, torch, dev, stream, B, g, num_accepted, steps, warmup, peak) -> dict:
+def measure_kv_side(binding, torch, dev, stream, B, g, num_accepted, steps, warmup, peak,
+                    window: int) -> dict:
     """The KV steps after verification, each timed alone over `steps` calls
     (CUDA events on the stream): committing the accepted entries of a
     1.8B-class target (24 layers x 16 KV heads, head dim 128, bf16; 4 sink
@@ -239,7 +240,7 @@ def measure_kv_side(binding, torch, dev, stream, B, g, num_accepted, steps, warm
     valid-slot lists, and a draft block-table window (W = 2048, block 128,
     K = gamma, lengths up to 32768)."""
     m = KV_MODEL
-    LH, D, S, W, R = m["layers"] * m["kv_heads"], m["head_dim"], m["sink"], m["window"], g + 1
+    LH, D, S, W, R = m["layers"] * m["kv_heads"], m["head_dim"], m["sink"], window, g + 1
     pools = [torch.zeros(B, LH, S + W, D, dtype=torch.bfloat16, device=dev) for _ in range(2)]
     gen = torch.Generator(device=dev)
     gen.manual_seed(11)
@@ -410,7 +411,7 @@ def run_ours(args) -> None:
     if not args.no_kv_side:
         step(sets[0])  # the accepted counts of one verification drive the commit
         kv_side = measure_kv_side(binding, torch, dev, stream, B, g, out_n.clone(), args.steps,
-                                  args.warmup, peak)
+                                  args.warmup, peak, args.kv_window)
     per_launch = [a.elapsed_time(b) for a, b in ev]
     if pg:
         tt = torch.tensor([total_ms], device=dev)
@@ -522,6 +523,8 @@ def main():
                     help="skip timing sv_draft_sample and spec_verify_cached")
     ap.add_argument("--no-kv-side", action="store_true",
                     help="skip timing the KV commit, valid slots and block-table window")
+    ap.add_argument("--kv-window", type=int, default=KV_MODEL["window"],
+                    help="ring slots of the KV-commit measurement (smaller for profiling captures)")
     ap.add_argument("--cpu-requests", type=int, default=256)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="approximate seconds of oracle work for cpu_baseline")
