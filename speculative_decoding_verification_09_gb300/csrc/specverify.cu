@@ -110,7 +110,7 @@ struct Mass {                 // per (request, phase-2 chunk, consumer warp)
 // A row's decision inputs, in shared memory of the decide kernel.
 struct RowStat {
   float mt, md;               // row maxima
-  double St, Sd;              // sum of 2^((l - max) * kf) over the row
+  float St_h, St_l, Sd_h, Sd_l;  // sum of 2^((l - max) * kf) over the row, float pairs
   int bad, amax;              // SV_ST_* bits, greedy argmax
 };
 static_assert(sizeof(Ctrl) == 64 && sizeof(Partial) == 16 && sizeof(Record) == 48 &&
@@ -428,6 +428,90 @@ __device__ __forceinline__ void warp_scan_ff(float& hi, float& lo, int lane) {
 }
 __device__ __forceinline__ double ff_val(float hi, float lo) { return double(hi) + double(lo); }
 
+// Float pairs (hi, lo), hi + lo the value: comparisons and the product with a
+// float, in fp32 arithmetic (the fp64 units are slow on this part).
+struct FF {
+  float h, l;
+};
+__device__ __forceinline__ FF ff(float h, float l = 0.f) { return FF{h, l}; }
+__device__ __forceinline__ FF operator+(FF a, FF b) {
+  ff_add2(a.h, a.l, b.h, b.l);
+  return a;
+}
+__device__ __forceinline__ FF operator-(FF a, FF b) {
+  ff_add2(a.h, a.l, -b.h, -b.l);
+  return a;
+}
+__device__ __forceinline__ bool ff_gt(FF a, FF b) {  // a > b
+  const FF d = a - b;
+  return d.h > 0.f || (d.h == 0.f && d.l > 0.f);
+}
+__device__ __forceinline__ bool ff_pos(FF a) { return a.h > 0.f || (a.h == 0.f && a.l > 0.f); }
+__device__ __forceinline__ FF ff_mul(float u, FF z) {  // u * z
+  const float p = u * z.h;
+  const float e = fmaf(u, z.h, -p);  // the product's rounding error, exactly
+  const float t = e + u * z.l;
+  FF r;
+  r.h = p + t;
+  r.l = t - (r.h - p);
+  return r;
+}
+__device__ __forceinline__ FF ff_shfl(FF a, int src) {
+  return FF{__shfl_sync(0xffffffffu, a.h, src), __shfl_sync(0xffffffffu, a.l, src)};
+}
+
+// a - b exactly, as a float pair
+__device__ __forceinline__ FF ff_diff(float a, float b) {
+  FF r;
+  two_sum(a, -b, r.h, r.l);
+  return r;
+}
+// a * b for a float pair a and a float b, as a float pair (fma gives the
+// rounding error of the leading product exactly)
+__device__ __forceinline__ FF ff_mulf(FF a, float b) {
+  const float p = a.h * b;
+  const float e = fmaf(a.h, b, -p) + a.l * b;
+  FF r;
+  two_sum(p, e, r.h, r.l);
+  return r;
+}
+// a * b for float pairs
+__device__ __forceinline__ FF ff_mul2(FF a, FF b) {
+  const float p = a.h * b.h;
+  const float e = fmaf(a.h, b.h, -p) + (a.h * b.l + a.l * b.h);
+  FF r;
+  two_sum(p, e, r.h, r.l);
+  return r;
+}
+// a / b for float pairs (one correction step of the float quotient)
+__device__ __forceinline__ FF ff_div(FF a, FF b) {
+  const float q = __fdiv_rn(a.h, b.h);
+  const float rem = fmaf(-q, b.h, a.h) + (a.l - q * b.l);
+  FF r;
+  two_sum(q, __fdiv_rn(rem, b.h), r.h, r.l);
+  return r;
+}
+// log2(e) / T as a float pair (log2(e) split into a float and its remainder)
+__device__ __forceinline__ FF ff_log2e_over(float T) {
+  constexpr float L_HI = 1.44269502162933349609375f;        // log2(e) rounded to a float
+  constexpr float L_LO = 1.925963033500011e-08f;            // log2(e) - L_HI
+  const float q = __fdiv_rn(L_HI, T);
+  const float rem = fmaf(-q, T, L_HI) + L_LO;
+  FF r;
+  two_sum(q, __fdiv_rn(rem, T), r.h, r.l);
+  return r;
+}
+// 2^e for a float pair e: 2^n * exp2f(f) with n = rint(e), f = e - n
+// (|f| <= 1/2 + tiny), the scaling saturating to 0 or +inf like the exact value
+__device__ __forceinline__ float ff_exp2(FF e) {
+  if (!(e.h == e.h)) return e.h;
+  if (e.h > 300.f) return INFINITY;
+  if (e.h < -300.f) return 0.f;
+  const float n = rintf(e.h);
+  return ldexpf(exp2f((e.h - n) + e.l), int(n));
+}
+
+
 // 2^x in fp64 for the acceptance test: x = n + f with n = rint(x) and
 // |f| <= 1/2, e^(f ln 2) by its Taylor series to degree 11 (truncation below
 // 1e-14 relative), scaled by 2^n built in the exponent field in two factors.
@@ -457,6 +541,9 @@ __device__ __forceinline__ double exp2_d(double x) {
 
 __device__ __forceinline__ bool row_ok(float m, double S) {
   return (m > -INFINITY) && (m < INFINITY) && (S > 0.0) && (S < INFINITY);
+}
+__device__ __forceinline__ bool row_ok_ff(float m, float S_hi) {
+  return (m > -INFINITY) && (m < INFINITY) && (S_hi > 0.f) && (S_hi < INFINITY);
 }
 
 // ------------------------------------------------ reduce: slots
@@ -1041,7 +1128,7 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
 // maxima and S = sum s_c * 2^((m_c - m) * kf), accumulated as float pairs.
 // Target in fields (a, b), draft in (c, d).  Result valid in every lane.
 __device__ void row_combine(const Partial* pp, int np, float kf, bool draft, float& mt,
-                            double& St, float& md, double& Sd) {
+                            FF& St, float& md, FF& Sd) {
   const int lane = threadIdx.x & 31;
   mt = -INFINITY;
   md = -INFINITY;
@@ -1059,13 +1146,13 @@ __device__ void row_combine(const Partial* pp, int np, float kf, bool draft, flo
     if (draft) ff_add(dh, dl, (md == -INFINITY) ? v.w : v.w * ex2((v.z - md) * kf));
   }
   warp_sum_ff(th, tl);
-  St = ff_val(th, tl);
+  St = ff(th, tl);
   if (draft) {
     warp_sum_ff(dh, dl);
-    Sd = ff_val(dh, dl);
+    Sd = ff(dh, dl);
   } else {
     md = 0.f;
-    Sd = 1.0;
+    Sd = ff(1.f);
   }
 }
 
@@ -1090,7 +1177,11 @@ __device__ void row_argmax(const Partial* pp, int np, float& best, int& bi, int&
 
 // The draw's normalisers of every row i (one warp, lane i), whichever row
 // turns out to be the first rejection: 1/S_t and, for i < gamma,
-// c0 = (m_t - m_d) * kf + log2(S_t / S_d), each as an unevaluated float pair.
+// c0 = (m_t - m_d) * kf + log2(S_t / S_d), each as an unevaluated float pair,
+// in fp32 arithmetic: (m_t - m_d) * kf exactly (kf is the factor the row
+// sums were formed with), log2 of the ratio as its binary exponent plus
+// log2f of the mantissa in [1/2, 1) (absolute error about 1e-7) plus the
+// ratio's low part.
 struct Cand {
   float ist_hi, ist_lo, c0_hi, c0_lo;
 };
@@ -1102,14 +1193,20 @@ __device__ void record_candidates(const Params& P, int b, const RowStat* rows, C
     const RowStat& rk = rows[i];
     Cand c{0.f, 0.f, 0.f, 0.f};
     if (rk.bad == 0) {
-      const double ist = 1.0 / rk.St;
-      c.ist_hi = float(ist);
-      c.ist_lo = float(ist - double(c.ist_hi));
+      const FF St = ff(rk.St_h, rk.St_l);
+      const FF ist = ff_div(ff(1.f), St);
+      c.ist_hi = ist.h;
+      c.ist_lo = ist.l;
       if (i < g) {
         // log2(P_d[v] / P_t[v]) = (l_d[v] - l_t[v]) * kf + (m_t - m_d) * kf + log2(S_t / S_d)
-        const double c0 = (double(rk.mt) - double(rk.md)) * double(kf) + log2(rk.St / rk.Sd);
-        c.c0_hi = float(c0);
-        c.c0_lo = float(c0 - double(c.c0_hi));
+        const FF q = ff_div(St, ff(rk.Sd_h, rk.Sd_l));
+        int e = 0;
+        const float mant = frexpf(q.h, &e);
+        const float lg = log2f(mant) + q.l / (q.h * 0.69314718055994531f);
+        FF c0 = ff_mulf(ff_diff(rk.mt, rk.md), kf);
+        c0 = c0 + ff(float(e)) + ff(lg);
+        c.c0_hi = c0.h;
+        c.c0_lo = c0.l;
       }
     }
     cand[i] = c;
@@ -1118,9 +1215,14 @@ __device__ void record_candidates(const Params& P, int b, const RowStat* rows, C
 
 // Sampling decision of request b (warp 0 of the CTA, rows in `rows`): lane
 // i < gamma tests position i, accept iff u <= min(1, P_t / P_d) with
-// P_t / P_d = 2^((l_t - m_t) * k - (l_d - m_d) * k) * S_d / S_t in fp64;
-// then the first rejection k and the outputs but token k.  Returns the
-// record's mode and k (in lane 0).
+// P_t / P_d = 2^E * S_d / S_t, E = ((l_t - l_d) - (m_t - m_d)) * log2(e) / T,
+// E formed in float pairs (exact differences, log2(e) / T as a pair) and
+// 2^E by exp2f: the ratio carries a relative error of a few 1e-7, below the
+// 1e-6 window in which the oracle flags a decision as a near-tie.  P_d = 0 in
+// fp64 (l_d = -inf, or (l_d - m_d) / T so far below m_d that the oracle's
+// fp64 underflows) accepts: the rare second case is settled in fp64 as the
+// oracle does.  Then the first rejection k and the outputs but token k.
+// Returns the record's mode and k (in lane 0).
 template <int DT>
 __device__ int2 decide_sample(const Params& P, int b, const RowStat* rows, float lt, float ld,
                               float u, bool tok_ok, int xi) {
@@ -1128,7 +1230,7 @@ __device__ int2 decide_sample(const Params& P, int b, const RowStat* rows, float
   const int lane = threadIdx.x & 31;
   const float T = __ldg(P.temp + b);
   const bool t_ok = isfinite(T) && T >= 0x1p-126f;
-  const double k64 = LOG2E_D / double(T);
+  const FF k2 = ff_log2e_over(T);
   int bad = 0, acc = 1;
   float pt = NAN, pd = NAN;
   for (int i = lane; i < R; i += 32) bad |= rows[i].bad;
@@ -1137,15 +1239,28 @@ __device__ int2 decide_sample(const Params& P, int b, const RowStat* rows, float
     if (!tok_ok) {
       bad |= SV_ST_BAD_TOKEN;
     } else if (bad == 0 && t_ok) {
-      const double et = (double(lt) - double(r.mt)) * k64;  // log2(P_t * S_t)
-      const double ed = (double(ld) - double(r.md)) * k64;
-      // P_d = 0 (including its fp64 underflow, ed far below -1000) accepts
-      const bool pd_zero = ld == -INFINITY || (ed < -1000.0 && exp2_d(ed) / r.Sd == 0.0);
-      const double ratio = pd_zero ? 1.0 : fmin(1.0, exp2_d(et - ed) * (r.Sd / r.St));
-      acc = double(u) <= ratio;
+      const FF St = ff(r.St_h, r.St_l), Sd = ff(r.Sd_h, r.Sd_l);
+      const FF et = ff_mul2(ff_diff(lt, r.mt), k2);  // log2(P_t * S_t)
+      const FF ed = ff_mul2(ff_diff(ld, r.md), k2);  // log2(P_d * S_d)
+      bool pd_zero = ld == -INFINITY;
+      if (!pd_zero && ed.h < -1000.f) {  // rare: does the oracle's fp64 P_d underflow?
+        const double e64 = (double(ld) - double(r.md)) * (LOG2E_D / double(T));
+        pd_zero = exp2_d(e64) / (double(r.Sd_h) + double(r.Sd_l)) == 0.0;
+      }
+      float ratio = 1.f;
+      if (!pd_zero) {
+        if (lt == -INFINITY) {  // P_t = 0
+          ratio = 0.f;
+        } else {
+          const float p2 = ff_exp2(et - ed);
+          const FF q = ff_div(Sd, St);
+          ratio = fminf(1.f, p2 * q.h + p2 * q.l);
+        }
+      }
+      acc = u <= ratio;
       if (P.out_p) {
-        pt = float(exp2_d(et) / r.St);
-        pd = float(exp2_d(ed) / r.Sd);
+        pt = lt == -INFINITY ? 0.f : ff_exp2(et) * ff_div(ff(1.f), St).h;
+        pd = ld == -INFINITY ? 0.f : ff_exp2(ed) * ff_div(ff(1.f), Sd).h;
       }
     }
   }
@@ -1269,23 +1384,24 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
       row_argmax(pp, P.np1, best, bi, nan);
       if (lane == 0) {
         RowStat r;
-        r.mt = best; r.md = 0.f; r.St = r.Sd = 0.0;
+        r.mt = best; r.md = 0.f; r.St_h = r.St_l = r.Sd_h = r.Sd_l = 0.f;
         r.bad = (nan || bi == INT_MAX || best == INFINITY) ? SV_ST_NONFINITE : 0;
         r.amax = bi;
         rows[i] = r;
       }
     } else {
       float mt, md;
-      double St, Sd;
+      FF St, Sd;
       row_combine(pp, P.np1, kf, i < P.gs, mt, St, md, Sd);
       if (cached && i < g) {  // the draft row's normaliser, as given
         md = dst_sh[i].x;
-        Sd = double(dst_sh[i].y);
+        Sd = ff(dst_sh[i].y);
       }
       if (lane == 0) {
         RowStat r;
-        r.mt = mt; r.md = md; r.St = St; r.Sd = Sd;
-        r.bad = (!row_ok(mt, St) || (i < g && !row_ok(md, Sd))) ? SV_ST_NONFINITE : 0;
+        r.mt = mt; r.md = md;
+        r.St_h = St.h; r.St_l = St.l; r.Sd_h = Sd.h; r.Sd_l = Sd.l;
+        r.bad = (!row_ok_ff(mt, St.h) || (i < g && !row_ok_ff(md, Sd.h))) ? SV_ST_NONFINITE : 0;
         r.amax = -1;
         rows[i] = r;
       }
@@ -1512,38 +1628,6 @@ __global__ void __launch_bounds__(NTHR, 1) sv_residual(const Params P) {
 }
 
 // ------------------------------------------------------------ draw
-
-// Float pairs (hi, lo), hi + lo the value: comparisons and the product with a
-// float, in fp32 arithmetic (the fp64 units are slow on this part).
-struct FF {
-  float h, l;
-};
-__device__ __forceinline__ FF ff(float h, float l = 0.f) { return FF{h, l}; }
-__device__ __forceinline__ FF operator+(FF a, FF b) {
-  ff_add2(a.h, a.l, b.h, b.l);
-  return a;
-}
-__device__ __forceinline__ FF operator-(FF a, FF b) {
-  ff_add2(a.h, a.l, -b.h, -b.l);
-  return a;
-}
-__device__ __forceinline__ bool ff_gt(FF a, FF b) {  // a > b
-  const FF d = a - b;
-  return d.h > 0.f || (d.h == 0.f && d.l > 0.f);
-}
-__device__ __forceinline__ bool ff_pos(FF a) { return a.h > 0.f || (a.h == 0.f && a.l > 0.f); }
-__device__ __forceinline__ FF ff_mul(float u, FF z) {  // u * z
-  const float p = u * z.h;
-  const float e = fmaf(u, z.h, -p);  // the product's rounding error, exactly
-  const float t = e + u * z.l;
-  FF r;
-  r.h = p + t;
-  r.l = t - (r.h - p);
-  return r;
-}
-__device__ __forceinline__ FF ff_shfl(FF a, int src) {
-  return FF{__shfl_sync(0xffffffffu, a.h, src), __shfl_sync(0xffffffffu, a.l, src)};
-}
 
 // Token k of request b, one CTA of DRAW_WARPS warps:
 //   1. every warp takes a contiguous run of sub-ranges, loads their masses
