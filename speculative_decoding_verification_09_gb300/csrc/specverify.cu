@@ -1107,6 +1107,12 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
       mbar_init(&C.full[s], 1);
       mbar_init(&C.empty[s], G::GW);
     }
+  }
+  // launched programmatically after the previous kernel in the stream (the
+  // last kernel of an earlier call, or whatever wrote the logits): nothing
+  // it wrote is read before it has completed
+  wait_previous_kernel();
+  if (threadIdx.x == 0) {
     // the workspace is in its ready state between calls; mark this call
     if (blockIdx.x == 0) {
       if (P.ctrl->state != 0ull || P.ctrl->reserved != 0ull) set_status(P, SV_ST_WORKSPACE);
@@ -1653,6 +1659,9 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
   // every uniform of the request (only entry k is used): an input, loaded
   // before the wait
   const float u_lane = lane < R ? __ldg(P.u_res + size_t(b) * R + lane) : 0.f;
+  // the next call's reduce may be placed as SMs free up: it waits for this
+  // grid's completion before it reads anything
+  allow_next_kernel();
   wait_previous_kernel();  // the masses (and, before them, the records)
   Record r;
   {
@@ -1972,6 +1981,7 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_sample(const Params P) {
     sh_tok_hit = INT_MAX;
     sh_tok_last = -1;
   }
+  allow_next_kernel();  // the next call's reduce waits for this grid's completion
   wait_previous_kernel();
   const Partial* pp = P.part + size_t(r) * P.np1;
   const int np = P.np1;
@@ -2276,8 +2286,9 @@ int launch(const Call& a) {
   mark(0);
   cudaError_t e = cudaSuccess;
   auto run = [&](auto reduce_k, auto decide_k, auto residual_k, auto draw_k, auto sample_k) {
-    reduce_k<<<grid, NTHR, smem_bytes<GeoReduce>(), st>>>(P);
-    e = cudaGetLastError();
+    // programmatic launch: the reduce's CTAs may be placed while the previous
+    // kernel in the stream finishes; it waits for that kernel on the device
+    e = launch_after(reduce_k, grid, NTHR, smem_bytes<GeoReduce>(), st, P);
     mark(1);
     if (draft) {
       if (e == cudaSuccess)
