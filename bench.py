@@ -133,6 +133,26 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_set_index(rank: int, s: int) -> int:
+    """Input set s of a rank: every rank verifies its own requests (weak
+    scaling, no data shared between ranks)."""
+    return 1000 * rank + s
+
+
+def max_over_ranks(x: float, dist_mod, device) -> float:
+    """The job's time is the slowest rank's: MAX all-reduce of one float
+    (NCCL on the GPU path; any backend works)."""
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: int, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's time."""
+    return units_per_rank_step * world * steps / (total_ms / 1e3)
+
+
 def oracle_positions_per_s(inp: synth.Inputs, n_req: int, threads: int) -> tuple[float, float]:
     import oracle
     sl = slice(0, n_req)
@@ -323,7 +343,8 @@ def run_ours(args) -> None:
     stream = torch.cuda.current_stream(dev)
 
     # input sets: host copies (pinned, for the end-to-end leg) and device copies
-    host_sets = [synth.make_inputs(cid, set_index=1000 * rank + s, B=B) for s in range(args.sets)]
+    host_sets = [synth.make_inputs(cid, set_index=rank_set_index(rank, s), B=B)
+                 for s in range(args.sets)]
     logit_bytes = host_sets[0].Lt.nbytes if greedy else host_sets[0].logit_bytes
 
     def dev_tensors(inp):
@@ -414,13 +435,10 @@ def run_ours(args) -> None:
                                   args.warmup, peak, args.kv_window)
     per_launch = [a.elapsed_time(b) for a, b in ev]
     if pg:
-        tt = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        total_ms = max_over_ranks(total_ms, pg, dev)
     st = int(status.item())
     ms_step = total_ms / args.steps
-    positions = B * g * ws_n * args.steps
-    value = positions / (total_ms / 1e3)
+    value = job_throughput(B * g, ws_n, args.steps, total_ms)
     launch_ms = float(np.mean(per_launch))
     # the dominant kernel is the streaming reduce: it reads every logit once
     achieved = logit_bytes / (reduce_ms / 1e3) / 1e9
