@@ -318,6 +318,12 @@ struct Elem<SV_F32> {
   __device__ static void sts(unsigned char* base, int idx, float v) {
     reinterpret_cast<float*>(base)[idx] = v;
   }
+  // the VEC elements from element p of a shared-memory body, p >= 0 (any
+  // alignment), as a vector
+  __device__ static uint4 gather_shifted(const unsigned char* body, int p) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(body) + p;
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
   __device__ static void unpack(const uint4& v, float* f) {
     f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
     f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
@@ -356,6 +362,16 @@ struct Elem<SV_BF16> {
   }
   __device__ static void sts(unsigned char* base, int idx, float v) {  // v holds a bf16 value
     reinterpret_cast<unsigned short*>(base)[idx] = (unsigned short)(__float_as_uint(v) >> 16);
+  }
+  // the VEC elements from element p of a shared-memory body, p >= 0 (any
+  // alignment), as a vector: four words at an even p, else five words
+  // (elements p - 1 .. p + 8, the last one unused) funnel-shifted by 16 bits
+  __device__ static uint4 gather_shifted(const unsigned char* body, int p) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(body) + (p >> 1);
+    if ((p & 1) == 0) return make_uint4(w[0], w[1], w[2], w[3]);
+    const uint32_t* v = w;  // word p >> 1 holds elements p - 1 and p
+    return make_uint4(__funnelshift_r(v[0], v[1], 16), __funnelshift_r(v[1], v[2], 16),
+                      __funnelshift_r(v[2], v[3], 16), __funnelshift_r(v[3], v[4], 16));
   }
   __device__ static void unpack(const uint4& v, float* f) {
     f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
@@ -1532,8 +1548,10 @@ __device__ void producer_res(const Params& P, SmemCtl<GeoResidual>& C, unsigned 
 
 // Mass of this warp's contiguous sub-range [cw*sub, (cw+1)*sub) of a
 // phase-2 chunk held in a slot (target body at +0, draft body at +HALF),
-// returned as a float pair (hi, lo) valid in every lane.
-template <int DT, typename Release>
+// returned as a float pair (hi, lo) valid in every lane.  ALIGNED: every row
+// of the call starts on a 16-byte boundary (the unaligned path is not
+// compiled in).
+template <int DT, bool ALIGNED, typename Release>
 __device__ float2 warp_slot_mass(const Params& P, const Desc& d, const Record& r,
                                  const unsigned char* slot, int wg, int lane, Release release) {
   using E = Elem<DT>;
@@ -1549,7 +1567,7 @@ __device__ float2 warp_slot_mass(const Params& P, const Desc& d, const Record& r
     const unsigned char* trow = P.Lt + ((size_t(d.b) * P.R + d.i) * size_t(P.V) + d.e0) * E::ES;
     const unsigned char* drow =
         two ? P.Ld + ((size_t(d.b) * P.gamma + r.k) * size_t(P.V) + d.e0) * E::ES : nullptr;
-    if (d.head_t == 0 && (!two || d.head_d == 0)) {
+    if (ALIGNED || (d.head_t == 0 && (!two || d.head_d == 0))) {
       // aligned: whole 16-byte vectors from shared memory, held in registers
       constexpr int PV = G::MAXV;  // a sub-range has at most 32 * PV vectors
       const uint4* tv = reinterpret_cast<const uint4*>(slot);
@@ -1570,16 +1588,64 @@ __device__ float2 warp_slot_mass(const Params& P, const Desc& d, const Record& r
       for (int u = 0; u < PV; ++u) acc += vec_weights<DT>(r, vt[u], vd[u], two);
       for (int e = max(lo, d.nb_t) + lane; e < hi; e += 32)
         acc += weight(r, E::load(trow, e), two ? E::load(drow, e) : 0.f);
-    } else {
-      // unaligned rows: element by element, from shared memory where held
-      for (int e = lo + lane; e < hi; e += 32) {
-        const int et = e - d.head_t, ed = e - d.head_d;
-        const float lt = (et >= 0 && et < d.nb_t) ? E::lds(slot, et) : E::load(trow, e);
-        float ld = 0.f;
-        if (two) ld = (ed >= 0 && ed < d.nb_d) ? E::lds(slot + HALF, ed) : E::load(drow, e);
-        acc += weight(r, lt, ld);
+    } else if constexpr (!ALIGNED) {
+      // rows not on 16-byte boundaries: the target body's whole vectors in
+      // this warp's range, each paired with the draft elements of the same
+      // indices, read from the draft body at a shift of delta = head_t -
+      // head_d elements with narrower loads; the few other elements of the
+      // range one by one (from shared memory before the slot is handed back,
+      // from global memory after)
+      constexpr int PV = G::MAXV;
+      const int hd = two ? d.head_d : d.head_t;
+      const int delta = d.head_t - hd;  // draft body index of target body index t: t + delta
+      const int nvt = d.nb_t / E::VEC;
+      auto cdiv = [](int x) { return x >= 0 ? (x + E::VEC - 1) / E::VEC : -((-x) / E::VEC); };
+      auto fdiv = [](int x) { return x >= 0 ? x / E::VEC : -((-x + E::VEC - 1) / E::VEC); };
+      int va = max(0, cdiv(lo - d.head_t)), vb = min(nvt, fdiv(hi - d.head_t));
+      if (two) {
+        va = max(va, cdiv(-delta));
+        vb = min(vb, fdiv(d.nb_d - delta));
       }
+      vb = max(va, vb);
+      const uint4* tv = reinterpret_cast<const uint4*>(slot);
+      const unsigned char* dbody = slot + HALF;
+      const uint4 neg =
+          make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD);
+      uint4 vt[PV], vd[PV];
+#pragma unroll
+      for (int u = 0; u < PV; ++u) {
+        const int j = va + lane + 32 * u;
+        vt[u] = neg;
+        vd[u] = neg;
+        if (j < vb) {
+          vt[u] = tv[j];
+          vd[u] = two ? E::gather_shifted(dbody, j * E::VEC + delta) : vt[u];
+        }
+      }
+      // elements outside those vectors: [lo, s1) and [s2, hi)
+      const int s1 = min(hi, d.head_t + va * E::VEC);
+      const int s2 = max(s1, d.head_t + vb * E::VEC);
+      auto in_t = [&](int e) { return e - d.head_t >= 0 && e - d.head_t < d.nb_t; };
+      auto in_d = [&](int e) { return !two || (e - hd >= 0 && e - hd < d.nb_d); };
+      auto scalar = [&](bool from_smem) {
+        for (int e = lo + lane; e < s1; e += 32) {
+          if ((in_t(e) && in_d(e)) != from_smem) continue;
+          const float lt = in_t(e) ? E::lds(slot, e - d.head_t) : E::load(trow, e);
+          const float ld = !two ? 0.f : in_d(e) ? E::lds(dbody, e - hd) : E::load(drow, e);
+          acc += weight(r, lt, ld);
+        }
+        for (int e = s2 + lane; e < hi; e += 32) {
+          if ((in_t(e) && in_d(e)) != from_smem) continue;
+          const float lt = in_t(e) ? E::lds(slot, e - d.head_t) : E::load(trow, e);
+          const float ld = !two ? 0.f : in_d(e) ? E::lds(dbody, e - hd) : E::load(drow, e);
+          acc += weight(r, lt, ld);
+        }
+      };
+      scalar(true);
       release();
+      scalar(false);
+#pragma unroll
+      for (int u = 0; u < PV; ++u) acc += vec_weights<DT>(r, vt[u], vd[u], two);
     }
   }
   float2 m = make_float2(acc, 0.f);
@@ -1587,7 +1653,7 @@ __device__ float2 warp_slot_mass(const Params& P, const Desc& d, const Record& r
   return m;
 }
 
-template <int DT>
+template <int DT, bool ALIGNED>
 __device__ void consumer_res(const Params& P, SmemCtl<GeoResidual>& C,
                              const unsigned char* slots) {
   using G = GeoResidual;
@@ -1605,12 +1671,16 @@ __device__ void consumer_res(const Params& P, SmemCtl<GeoResidual>& C,
       __syncwarp();
       if (lane == 0) mbar_arrive(&C.empty[s]);
     };
-    const float2 m = warp_slot_mass<DT>(P, d, d.rec, slots + size_t(s) * SLOT, wg, lane, release);
+    const float2 m =
+        warp_slot_mass<DT, ALIGNED>(P, d, d.rec, slots + size_t(s) * SLOT, wg, lane, release);
     if (lane == 0) P.mass[(size_t(d.b) * P.nch2 + d.c) * GW + wg] = Mass{m.x, m.y};
   }
 }
 
-template <int DT>
+// ALIGNED: every target and draft row of the call starts on a 16-byte
+// boundary (so does every phase-2 chunk); the kernel for other calls also
+// pairs unaligned rows.
+template <int DT, bool ALIGNED>
 __global__ void __launch_bounds__(NTHR, 1) sv_residual(const Params P) {
   using G = GeoResidual;
   allow_next_kernel();  // one CTA per SM: every CTA of this grid is resident
@@ -1629,7 +1699,7 @@ __global__ void __launch_bounds__(NTHR, 1) sv_residual(const Params P) {
   if (threadIdx.x < 32) {
     if (threadIdx.x == 0) producer_res<DT>(P, C, slots);
   } else {
-    consumer_res<DT>(P, C, slots);
+    consumer_res<DT, ALIGNED>(P, C, slots);
   }
 }
 
@@ -2117,7 +2187,10 @@ DevCache g_dev[64];
 template <int DT>
 bool prepare_kernel() {
   const int r = int(smem_bytes<GeoReduce>());
-  return cudaFuncSetAttribute(sv_residual<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(sv_residual<DT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(smem_bytes<GeoResidual>())) == cudaSuccess &&
+         cudaFuncSetAttribute(sv_residual<DT, false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(smem_bytes<GeoResidual>())) == cudaSuccess &&
          cudaFuncSetAttribute(sv_reduce<DT, false, false, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, r) == cudaSuccess &&
@@ -2307,20 +2380,26 @@ int launch(const Call& a) {
   };
   // the reduce streams draft rows only for CALL_SAMPLE; the other paths pair
   // target chunks in its slots, and draft sampling needs contiguous shares
+  // rows on 16-byte boundaries throughout: the residual kernel without the
+  // unaligned-row path
+  const bool aligned_rows = (uintptr_t(a.Lt) % 16 == 0) && (!a.Ld || uintptr_t(a.Ld) % 16 == 0) &&
+                            (size_t(V) * ES) % 16 == 0;
   auto dispatch = [&](auto dt) {
     constexpr int D = decltype(dt)::value;
+    auto go = [&](auto reduce_k, auto decide_k) {
+      if (aligned_rows)
+        run(reduce_k, decide_k, sv_residual<D, true>, sv_draw<D>, sv_sample<D>);
+      else
+        run(reduce_k, decide_k, sv_residual<D, false>, sv_draw<D>, sv_sample<D>);
+    };
     if (greedy)
-      run(sv_reduce<D, true, true, false>, sv_decide<D, true>, sv_residual<D>, sv_draw<D>,
-          sv_sample<D>);
+      go(sv_reduce<D, true, true, false>, sv_decide<D, true>);
     else if (draft)
-      run(sv_reduce<D, false, true, true>, sv_decide<D, false>, sv_residual<D>, sv_draw<D>,
-          sv_sample<D>);
+      go(sv_reduce<D, false, true, true>, sv_decide<D, false>);
     else if (a.kind == CALL_CACHED)
-      run(sv_reduce<D, false, true, false>, sv_decide<D, false>, sv_residual<D>, sv_draw<D>,
-          sv_sample<D>);
+      go(sv_reduce<D, false, true, false>, sv_decide<D, false>);
     else
-      run(sv_reduce<D, false, false, false>, sv_decide<D, false>, sv_residual<D>, sv_draw<D>,
-          sv_sample<D>);
+      go(sv_reduce<D, false, false, false>, sv_decide<D, false>);
   };
   if (a.dtype == SV_F32)
     dispatch(std::integral_constant<int, SV_F32>());
