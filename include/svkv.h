@@ -54,7 +54,8 @@ extern "C" {
  *   num_accepted [B] int32; pos [B] int32, updated in place.
  * Requires row_bytes a positive multiple of 16, all four KV buffers 16-byte
  * aligned, window >= R (a commit never laps the ring), sink >= 0, LH >= 1,
- * LH * R * row_bytes <= 2^34 and B <= 65535; positions stay below 2^31 - R
+ * R <= 64, row_bytes <= 8192, LH * R * row_bytes <= 2^34 and B <= 65535;
+ * positions stay below 2^31 - R
  * (a larger one is reported as SV_ST_BAD_LENGTH).
  * Two kernels: the copy, then the position update.
  */

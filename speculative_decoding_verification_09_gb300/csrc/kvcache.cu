@@ -26,7 +26,18 @@ namespace {
 
 constexpr int KV_THREADS = 256;
 constexpr int KV_UNROLL = 4;     // 16-byte vectors in flight per thread
+constexpr int KV_MAX_R = 64;     // staged entries per request
+constexpr int KV_MAX_NVEC = 512; // 16-byte vectors per KV row (8 KB rows)
 constexpr int MAP_THREADS = 128;
+
+// n / d for 0 <= n < 2^31 and 1 <= d <= 512 as (n * ceil(2^40 / d)) >> 40: the
+// multiplier's excess over 2^40 / d is below 1, so the product's excess over
+// n * 2^40 / d stays below 2^31 / 2^40 <= 1 / d, less than the distance from
+// n / d to the next integer.
+unsigned long long div_magic(int d) { return ((1ull << 40) + unsigned(d) - 1) / unsigned(d); }
+__device__ __forceinline__ int div_by(int n, unsigned long long m) {
+  return int((unsigned long long)(unsigned)n * m >> 40);
+}
 
 __device__ __forceinline__ void allow_next_kernel() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -53,6 +64,7 @@ struct KvParams {
   int32_t* status;
   int B, LH, R, nvec, sink, window;  // nvec: 16-byte vectors per row
   int per_req;                       // LH * R * nvec, staged vectors per request
+  unsigned long long m_nvec, m_R;    // division multipliers (div_magic)
 };
 
 // Copy of the accepted entries.  Request b = blockIdx.y; the CTAs of a
@@ -61,11 +73,15 @@ struct KvParams {
 // pools at slot Slot(pos + j).  KV_UNROLL vectors of K and of V per thread
 // are loaded before any is stored.
 __global__ void __launch_bounds__(KV_THREADS) sv_kv_copy(const KvParams K) {
+  __shared__ int slot_of[KV_MAX_R];  // Slot(pos + j) of the committed entries
   allow_next_kernel();  // the position update waits for this grid's completion
   const int b = int(blockIdx.y);
   const int k = __ldg(K.num_accepted + b);
   const int p = __ldg(K.pos + b);
   if (k < 0 || k >= K.R || p < 0 || p > 0x7fffffff - K.R) return;  // dropped or invalid
+  if (int(threadIdx.x) <= k)
+    slot_of[threadIdx.x] = int(ring_slot((long long)p + threadIdx.x, K.sink, K.window));
+  __syncthreads();
   const int C = K.sink + K.window;
   const uint4* kn = reinterpret_cast<const uint4*>(K.k_new) + size_t(b) * K.per_req;
   const uint4* vn = reinterpret_cast<const uint4*>(K.v_new) + size_t(b) * K.per_req;
@@ -80,11 +96,10 @@ __global__ void __launch_bounds__(KV_THREADS) sv_kv_copy(const KvParams K) {
 #pragma unroll
     for (int u = 0; u < KV_UNROLL; ++u) {
       const int f = f0 + u * stride;
-      const int row = f / K.nvec, q = f - row * K.nvec;
-      const int lh = row / K.R, j = row - lh * K.R;
+      const int row = div_by(f, K.m_nvec), q = f - row * K.nvec;
+      const int lh = div_by(row, K.m_R), j = row - lh * K.R;
       use[u] = f < K.per_req && j <= k;
-      dst[u] = ((size_t(b) * K.LH + lh) * C + size_t(ring_slot((long long)p + j, K.sink, K.window))) *
-                   K.nvec + q;
+      dst[u] = use[u] ? ((size_t(b) * K.LH + lh) * C + size_t(slot_of[j])) * K.nvec + q : 0;
       if (use[u]) {
         kv[u] = __ldg(kn + f);
         vv[u] = __ldg(vn + f);
@@ -195,8 +210,9 @@ extern "C" {
 int sv_kv_commit(void* k_pool, void* v_pool, const void* k_new, const void* v_new,
                  const int32_t* num_accepted, int32_t* pos, int B, int LH, int R, int row_bytes,
                  int sink, int window, int32_t* dev_status, void* stream) {
-  if (B < 0 || LH < 1 || R < 1 || row_bytes < 16 || (row_bytes % 16) != 0 || sink < 0 ||
-      window < R || (long long)sink + window > 0x7fffffffLL)
+  if (B < 0 || LH < 1 || R < 1 || R > KV_MAX_R || row_bytes < 16 || (row_bytes % 16) != 0 ||
+      row_bytes / 16 > KV_MAX_NVEC || sink < 0 || window < R ||
+      (long long)sink + window > 0x7fffffffLL)
     return SV_ERR_INVALID_ARG;
   if (B == 0) return SV_OK;
   if (!k_pool || !v_pool || !k_new || !v_new || !num_accepted || !pos) return SV_ERR_INVALID_ARG;
@@ -217,6 +233,8 @@ int sv_kv_commit(void* k_pool, void* v_pool, const void* k_new, const void* v_ne
   K.B = B; K.LH = LH; K.R = R; K.nvec = row_bytes / 16;
   K.sink = sink; K.window = window;
   K.per_req = int(per_req);
+  K.m_nvec = div_magic(K.nvec);
+  K.m_R = div_magic(R);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // CTAs per request: enough for KV_UNROLL vectors per thread per pass
   const long long per_cta = (long long)KV_THREADS * KV_UNROLL;

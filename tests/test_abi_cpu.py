@@ -152,6 +152,8 @@ def test_kv_and_window_validation(L):
         return L.sv_kv_commit(a["kp"], a["vp"], a["kn"], a["vn"], a["na"], a["pos"], a["B"],
                               a["LH"], a["R"], a["rb"], a["S"], a["W"], None, None)
     assert commit(rb=24) == binding.SV_ERR_INVALID_ARG
+    assert commit(rb=8192 + 16) == binding.SV_ERR_INVALID_ARG   # rows of at most 8 KB
+    assert commit(R=65, W=80) == binding.SV_ERR_INVALID_ARG     # at most 64 staged entries
     assert commit(W=3) == binding.SV_ERR_INVALID_ARG
     assert commit(S=-1) == binding.SV_ERR_INVALID_ARG
     assert commit(kp=FAKE + 8) == binding.SV_ERR_INVALID_ARG
