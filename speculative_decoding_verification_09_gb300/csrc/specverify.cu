@@ -81,6 +81,7 @@ constexpr int SMS_CAP = 256;           // the chunk heuristic assumes at most th
 constexpr int MAXR = SV_MAX_GAMMA + 1;
 constexpr int DECIDE_WARPS = 8;        // decide: warps per request
 constexpr int DRAW_WARPS = 8;          // draw: warps per request
+constexpr int SAMPLE_WARPS = 4;        // draft sampling: warps per draft row
 constexpr float LOG2E_F = 1.4426950408889634f;
 constexpr double LOG2E_D = 1.4426950408889634;
 constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;  // one second
@@ -1971,6 +1972,7 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
 // Block-wide inclusive prefix of float pairs in thread order (all threads of
 // the CTA take part); `total` gets the CTA's sum.  wsum holds one entry per
 // warp; the CTA synchronises twice.
+template <int NW>
 __device__ FF block_scan_ff(FF v, FF* wsum, FF& total) {
   const int warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
   FF incl = v;
@@ -1978,7 +1980,7 @@ __device__ FF block_scan_ff(FF v, FF* wsum, FF& total) {
   if (lane == 31) wsum[warp] = incl;
   __syncthreads();
   FF off = ff(0.f), tot = ff(0.f);
-  for (int w = 0; w < DRAW_WARPS; ++w) {
+  for (int w = 0; w < NW; ++w) {
     if (w < warp) off = off + wsum[w];
     tot = tot + wsum[w];
   }
@@ -2017,7 +2019,7 @@ __device__ __forceinline__ void partial_span(const Params& P, const unsigned cha
 // a head or tail shorter than a vector, and a vector of margin
 constexpr int SAMPLE_STAGE =
     ((GeoReduce::HALF / 16 + GeoReduce::GW - 1) / GeoReduce::GW) * 16 + 48;
-constexpr int SAMPLE_KV = (SAMPLE_STAGE / 16 + 32 * DRAW_WARPS - 1) / (32 * DRAW_WARPS);
+constexpr int SAMPLE_KV = (SAMPLE_STAGE / 16 + 32 * SAMPLE_WARPS - 1) / (32 * SAMPLE_WARPS);
 
 // Draft-token sampling, one CTA per draft row (row r = b * R + i of the
 // reduce's rows): the row's maximum and normaliser S from the reduce's
@@ -2028,11 +2030,11 @@ constexpr int SAMPLE_KV = (SAMPLE_STAGE / 16 + 32 * DRAW_WARPS - 1) / (32 * DRAW
 // it in index order.  Writes the token and the row's (max, S) to column
 // col + i of request b.
 template <int DT>
-__global__ void __launch_bounds__(32 * DRAW_WARPS) sv_sample(const Params P) {
+__global__ void __launch_bounds__(32 * SAMPLE_WARPS) sv_sample(const Params P) {
   using E = Elem<DT>;
-  constexpr int NT = 32 * DRAW_WARPS;
-  __shared__ FF wsum[DRAW_WARPS];
-  __shared__ float wmax[DRAW_WARPS];
+  constexpr int NW = SAMPLE_WARPS, NT = 32 * NW;
+  __shared__ FF wsum[NW];
+  __shared__ float wmax[NW];
   __shared__ FF sh_rest, sh_rest_last;
   __shared__ int sh_hit, sh_last, sh_tok_hit, sh_tok_last;
   __shared__ __align__(16) unsigned char stage[SAMPLE_STAGE];
@@ -2062,12 +2064,12 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_sample(const Params P) {
   if (lane == 0) wmax[warp] = m;
   __syncthreads();
   m = wmax[0];
-  for (int w = 1; w < DRAW_WARPS; ++w) m = fmaxf(m, wmax[w]);
+  for (int w = 1; w < NW; ++w) m = fmaxf(m, wmax[w]);
   // 2. the normaliser S, the sum of the partials' masses
   FF part = ff(0.f);
   for (int q = tid; q < np; q += NT) ff_add(part.h, part.l, partial_mass(pp, q, m, kf));
   FF S;
-  block_scan_ff(part, wsum, S);
+  block_scan_ff<NW>(part, wsum, S);
   const double Sd = ff_val(S.h, S.l);
   const bool ok = t_ok && row_ok(m, Sd);  // the same in every thread
   if (!ok) {
@@ -2087,7 +2089,7 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_sample(const Params P) {
     const int q = q0 + tid;
     const FF z = ff(q < np ? partial_mass(pp, q, m, kf) : 0.f);
     FF rtot;
-    const FF incl = block_scan_ff(z, wsum, rtot);
+    const FF incl = block_scan_ff<NW>(z, wsum, rtot);
     const bool pos = q < np && ff_pos(z);
     if (pos && ff_gt(base + incl, tau)) atomicMin(&sh_hit, q);
     if (pos) atomicMax(&sh_last, q);
@@ -2145,7 +2147,7 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_sample(const Params P) {
     if (w > 0.f) lastpos = e;
   }
   FF rtot;
-  const FF incl = block_scan_ff(run, wsum, rtot);
+  const FF incl = block_scan_ff<NW>(run, wsum, rtot);
   if (a0 < a1 && ff_pos(run) && ff_gt(incl, rest)) atomicMin(&sh_tok_hit, tid);
   if (lastpos >= 0) atomicMax(&sh_tok_last, lastpos);
   __syncthreads();
@@ -2365,7 +2367,7 @@ int launch(const Call& a) {
     mark(1);
     if (draft) {
       if (e == cudaSuccess)
-        e = launch_after(sample_k, unsigned(units), 32 * DRAW_WARPS, 0, st, P);
+        e = launch_after(sample_k, unsigned(units), 32 * SAMPLE_WARPS, 0, st, P);
       mark(2);
       return;
     }
