@@ -228,6 +228,16 @@ int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests);
  */
 int sv_set_stage_events(void* const* events, int n);
 
+/*
+ * Failure-handling test aid: while enabled, the next calls' streaming kernel
+ * withholds one of its shared-memory slots (block 0 never fills its first
+ * slot), so the waits on that slot run out after their one-second limit: the
+ * call reports SV_ST_TIMEOUT in *dev_status, its results are void, and the
+ * context stays usable for the calls after it.  No fault, trap or endless
+ * wait is involved.  Not thread-safe, like sv_set_tuning().  Returns SV_OK.
+ */
+int sv_test_withhold_slot(int enable);
+
 /* Human-readable name of a host return code. */
 const char* sv_error_string(int code);
 

@@ -24,7 +24,7 @@ SV_MAX_GAMMA = 32
 EXPORTED = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_diag",
             "spec_verify_greedy", "spec_verify_noalloc", "spec_verify_cached",
             "sv_draft_workspace_bytes", "sv_draft_sample", "sv_set_tuning",
-            "sv_set_stage_events", "sv_error_string", "sv_version",
+            "sv_set_stage_events", "sv_test_withhold_slot", "sv_error_string", "sv_version",
             "sv_kv_commit", "sv_kv_valid_slots", "sv_window_cols", "sv_window_block_table",
             "sv_window_seq_lens_host")
 SV_NOALLOC_MAX_WORKSPACE = 16 << 20
@@ -62,11 +62,13 @@ def lib() -> ctypes.CDLL:
         L.sv_window_seq_lens_host.argtypes = [P, I, I, I, I, P]
         L.sv_set_tuning.argtypes = [I, I, I]
         L.sv_set_stage_events.argtypes = [P, I]
+        L.sv_test_withhold_slot.argtypes = [I]
         L.sv_error_string.argtypes = [I]
         L.sv_error_string.restype = ctypes.c_char_p
         for name in ("sv_workspace_init", "spec_verify", "spec_verify_diag",
                      "spec_verify_greedy", "spec_verify_noalloc", "spec_verify_cached",
                      "sv_draft_sample", "sv_set_tuning", "sv_set_stage_events", "sv_version",
+                     "sv_test_withhold_slot",
                      "sv_kv_commit", "sv_kv_valid_slots", "sv_window_cols",
                      "sv_window_block_table", "sv_window_seq_lens_host"):
             getattr(L, name).restype = I
@@ -123,6 +125,12 @@ def make_workspace(B: int, gamma: int, V: int, device) -> torch.Tensor:
 
 def sv_set_tuning(chunk_elems: int = 0, ctas_per_sm: int = 0, lag_requests: int = 0) -> None:
     _check(lib().sv_set_tuning(chunk_elems, ctas_per_sm, lag_requests))
+
+
+def sv_test_withhold_slot(enable: bool) -> None:
+    """Failure-handling test aid: the next calls' streaming kernel leaves one
+    slot unfilled, so its bounded wait runs out (SV_ST_TIMEOUT)."""
+    _check(lib().sv_test_withhold_slot(1 if enable else 0))
 
 
 def sv_set_stage_events(events) -> None:

@@ -164,6 +164,7 @@ struct Params {
   float* out_p;
   float* out_Z;
   float* out_stats;           // draft sampling: row normalisers (m, S)
+  int withhold_slot;          // failure-handling test: CTA 0 never fills its first reduce slot
   int col, ncols;             // draft sampling: row i of request b goes to column col + i of ncols
   int32_t* status;
   Ctrl* ctrl;
@@ -1027,7 +1028,10 @@ __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* 
       d.head_d = d.nb_d = 0;
     }
     const unsigned bt = unsigned(d.nb_t) * E::ES, bd = unsigned(d.nb_d) * E::ES;
-    if (bt + bd == 0u) {
+    if (P.withhold_slot && blockIdx.x == 0 && seq == 0) {
+      // failure-handling test: the first slot of CTA 0 is never filled, so its
+      // consumers' bounded wait runs out (SV_ST_TIMEOUT) and the CTA gives up
+    } else if (bt + bd == 0u) {
       mbar_arrive(&C.full[s]);
     } else {
       mbar_arrive_tx(&C.full[s], bt + bd);
@@ -2174,6 +2178,7 @@ __global__ void __launch_bounds__(32 * SAMPLE_WARPS) sv_sample(const Params P) {
 
 struct Tuning {
   int chunk = 0;
+  int withhold_slot = 0;         // failure-handling test (sv_test_withhold_slot)
   cudaEvent_t stage_ev[5] = {};  // profiling: events recorded around the kernels
   int stage_n = 0;
 };
@@ -2342,6 +2347,7 @@ int launch(const Call& a) {
   P.sub = round_up((chmax2 + GeoResidual::GW - 1) / GeoResidual::GW, 8);
   P.out_tokens = a.out_tokens; P.out_n = a.out_n; P.out_p = a.out_p; P.out_Z = a.out_Z;
   P.out_stats = a.out_stats; P.col = a.col; P.ncols = a.ncols;
+  P.withhold_slot = g_tune.withhold_slot;
   P.status = a.status;
   unsigned char* w = static_cast<unsigned char*>(a.ws);
   P.ctrl = reinterpret_cast<Ctrl*>(w + L.ctrl);
@@ -2576,6 +2582,11 @@ int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests) {
   (void)ctas_per_sm;   // the reduce kernel always runs one CTA per SM
   (void)lag_requests;  // the stages run as separate kernels: there is no lag
   g_tune.chunk = chunk_elems > 0 ? chunk_elems : 0;
+  return SV_OK;
+}
+
+int sv_test_withhold_slot(int enable) {
+  g_tune.withhold_slot = enable ? 1 : 0;
   return SV_OK;
 }
 

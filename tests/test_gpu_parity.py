@@ -231,6 +231,29 @@ def test_poisoned_task_counter_is_detected_and_repaired():
     compare_sampling(inp, run_sampling(inp, d, ws), ref)
 
 
+def test_bounded_wait_reports_timeout_and_context_recovers():
+    """Failure handling without a fault: with one reduce slot withheld, that
+    slot's waits run out after their one-second limit; the call reports
+    SV_ST_TIMEOUT, and the next calls (sampling and greedy) are correct."""
+    import time
+    cfg = synth.custom_config(6, 3, 5000, "bf16", "normal")
+    inp = synth.make_inputs(cfg, seed=15)
+    d = to_dev(inp)
+    ws = binding.make_workspace(inp.B, inp.gamma, inp.V, DEV)
+    ref = oracle_sampling(inp)
+    binding.sv_test_withhold_slot(True)
+    try:
+        t0 = time.perf_counter()
+        bad = run_sampling(inp, d, ws)
+        waited = time.perf_counter() - t0
+    finally:
+        binding.sv_test_withhold_slot(False)
+    assert bad["status"] & binding.SV_ST_TIMEOUT
+    assert 0.5 < waited < 30.0
+    compare_sampling(inp, run_sampling(inp, d, ws), ref)
+    compare_greedy(run_greedy(inp, ws=ws), oracle.greedy(inp.Lt, inp.x, inp.dtype))
+
+
 def test_gamma_zero_is_plain_sampling():
     cfg = synth.custom_config(50, 0, 700, "f32", "normal", temp=1.3)
     inp = synth.make_inputs(cfg, seed=14)
