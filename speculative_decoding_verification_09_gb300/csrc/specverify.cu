@@ -8,26 +8,30 @@
 // scheduler section "动态推迟投机验证调度器设计": tempered softmax, accept in
 // draft order, stop at the first rejection, index-order inverse CDF).
 //
-// GPU structure: four kernels in stream order per call (the stream order is
-// the only synchronisation between them):
+// GPU structure: four kernels in stream order per call, each launched with
+// programmatic stream serialisation (its CTAs are placed early and wait on
+// the device for the previous kernel's memory):
 //   reduce   one CTA per SM, each streaming a contiguous range of row chunks
-//            (chunk c of target row i and draft row i of request b) from HBM
-//            into a ring of shared-memory slots with TMA bulk copies
-//            (cp.async.bulk, completion counted on an mbarrier) issued by one
-//            producer lane; NCW consumer warps reduce each slot from
-//            registers and publish one partial per warp: (max, sum of
-//            2^((l - max) * log2e / T)) of the target and draft shares, or
-//            (max, lowest index, NaN seen) for greedy verification.
+//            (chunk c of target row i and draft row i of request b; or two
+//            target chunks when no draft rows are streamed) from HBM into a
+//            ring of shared-memory slots with TMA bulk copies (cp.async.bulk,
+//            completion counted on an mbarrier) issued by one producer lane;
+//            consumer warps reduce each slot from registers and publish one
+//            partial per warp: (max, sum of 2^((l - max) * log2e / T)) of the
+//            target and draft shares, or (max, lowest index, NaN seen) for
+//            greedy verification.
 //   decide   one CTA per request: every row's partials combined (maxima, sums
-//            as float pairs), then per position the acceptance test in fp64,
-//            the first rejection k, all outputs but token k, and a decision
-//            record (row k's normalisers) for the draw.
-//   residual one CTA per (request, phase-2 chunk) of the row token k is drawn
-//            from (residual of row k, or target row gamma for the bonus): the
-//            mass of each warp's contiguous sub-range.
-//   draw     one warp per request: the sub-range where the running mass
+//            as float pairs), then per position the acceptance test in
+//            float-pair arithmetic, the first rejection k, all outputs but
+//            token k, and a decision record (row k's normalisers) for the draw.
+//   residual one CTA per SM over the phase-2 chunks of the rows token k is
+//            drawn from (residual of row k, or target row gamma for the
+//            bonus): the mass of each warp's contiguous sub-range.
+//   draw     one CTA per request: the sub-range where the running mass
 //            crosses u * Z, scanned in index order: token k.
-// Greedy verification runs reduce (chunk argmax) and decide only.
+// Greedy verification runs reduce (chunk argmax) and decide only; draft
+// sampling runs reduce (contiguous warp shares) and sample (one CTA per draft
+// row: the crossing partial's span, scanned in index order).
 #include <cuda_runtime.h>
 #include <limits.h>
 #include <math.h>
@@ -101,7 +105,7 @@ enum { MODE_INVALID = 0, MODE_REJECT = 1, MODE_BONUS = 2, MODE_TARGET = 3 };
 struct Record {               // per request, 48 bytes
   int k, mode;
   float mt, kf;               // max logit of target row k; log2(e)/T in fp32
-  float ist_hi, ist_lo;       // 1/S_t of row k as an unevaluated float pair (fp64 precision)
+  float ist_hi, ist_lo;       // 1/S_t of row k as an unevaluated float pair
   float c0_hi, c0_lo;         // log2(P_d/P_t) = (l_d - l_t) * kf + c0 on row k, c0 as a pair
   int pad[4];
 };
@@ -530,7 +534,8 @@ __device__ __forceinline__ float ff_exp2(FF e) {
 }
 
 
-// 2^x in fp64 for the acceptance test: x = n + f with n = rint(x) and
+// 2^x in fp64 (used only for the rare P_d underflow case of the acceptance
+// test, where the oracle's fp64 rounding decides): x = n + f with n = rint(x) and
 // |f| <= 1/2, e^(f ln 2) by its Taylor series to degree 11 (truncation below
 // 1e-14 relative), scaled by 2^n built in the exponent field in two factors.
 // Out-of-range x saturate to 0 or +inf; NaN stays NaN.
