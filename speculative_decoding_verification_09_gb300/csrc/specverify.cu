@@ -95,7 +95,7 @@ constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;  // one second
 struct Ctrl {                 // 64 bytes at the start of the workspace
   // both 0 between calls (the ready state); state is 1 while a call runs
   unsigned long long state, reserved;
-  unsigned long long pad[6];
+  unsigned long long pad[6];  // pad[0]: the residual kernel's chunk-claim counter
 };
 struct Partial {              // per (request, position, chunk, consumer warp)
   float a, b, c, d;           // sampling: m_t, s_t, m_d, s_d; greedy: value, index, nan, 0
@@ -1144,6 +1144,7 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
       if (P.ctrl->state != 0ull || P.ctrl->reserved != 0ull) set_status(P, SV_ST_WORKSPACE);
       P.ctrl->state = 1ull;
       P.ctrl->reserved = 0ull;
+      P.ctrl->pad[0] = 0ull;  // the residual kernel's chunk claims
     }
   }
   __syncthreads();
@@ -1502,27 +1503,37 @@ __device__ void span_mass(const Record& r, const unsigned char* trow, const unsi
   warp_sum_ff(mh, ml);
 }
 
-// Residual producer (one lane): phase-2 chunks t = x, x + G, x + 2G, ... (CTA
-// x of G; chunk t % nch2 of request t / nch2), interleaved so that every CTA
-// gets a similar mix of rejections (a target and a draft chunk) and bonus
-// draws (a target chunk); chunks of invalid requests are skipped.  Each slot
-// gets the chunk of target row k (gamma for the bonus), the draft row k chunk
-// after a rejection, and the request's record.  The next chunk's (k, mode)
-// is loaded one chunk ahead.
+// Residual producer (one lane): phase-2 chunks claimed one at a time from a
+// counter the whole grid shares (reset by the reduce kernel), so CTAs that
+// finish their chunks early take more: the work spreads by bytes, whatever
+// the mix of rejections (a target and a draft chunk) and bonus draws (a
+// target chunk); a static cyclic split left the busiest CTA about 20 %
+// above the mean.  Chunks are numbered chunk-major, t = c * B + b, so the
+// short last chunks of the rows are claimed last; chunks of invalid requests
+// are skipped.  Each slot gets the chunk of target row k (gamma for the
+// bonus), the draft row k chunk after a rejection, and the request's record.
+// Every CTA starts with chunk x of its own; claims run two chunks ahead and a
+// chunk's (k, mode) is loaded one chunk ahead, so neither round trip is
+// waited for.
 template <int DT>
 __device__ void producer_res(const Params& P, SmemCtl<GeoResidual>& C, unsigned char* slots) {
   using E = Elem<DT>;
   using G = GeoResidual;
   constexpr int NS = G::NS, SLOT = G::SLOT, HALF = G::HALF;
-  const long long T = (long long)P.B * P.nch2, stride = gridDim.x;
-  long long t = blockIdx.x;
+  const long long T = (long long)P.B * P.nch2;
+  unsigned long long* claims = &P.ctrl->pad[0];
+  // chunk x first (no claim to wait for), then chunks G, G + 1, ... by claim
+  auto claim = [&]() { return (long long)gridDim.x + (long long)atomicAdd(claims, 1ull); };
   auto km_of = [&](long long tt) {
-    return tt < T ? __ldg(reinterpret_cast<const int2*>(P.rec + tt / P.nch2)) : make_int2(0, 0);
+    return tt < T ? __ldg(reinterpret_cast<const int2*>(P.rec + tt % P.B)) : make_int2(0, 0);
   };
-  int2 km = km_of(t), km_next = km_of(t + stride);
+  long long t = blockIdx.x, t_next = claim();
+  int2 km = km_of(t);
   long long seq = 0;
-  for (; t < T; t += stride) {
-    const int b = int(t / P.nch2), c = int(t - (long long)b * P.nch2);
+  while (t < T) {
+    const int2 km_next = km_of(t_next);  // used in the next iteration
+    const long long t_next2 = claim();
+    const int c = int(t / P.B), b = int(t - (long long)c * P.B);
     if (km.y == MODE_REJECT || km.y == MODE_BONUS) {
       const int s = int(seq % NS);
       const unsigned use = unsigned(seq / NS);
@@ -1550,8 +1561,9 @@ __device__ void producer_res(const Params& P, SmemCtl<GeoResidual>& C, unsigned 
                  &C.full[s]);
       bulk_g2s(&d.rec, P.rec + b, unsigned(sizeof(Record)), &C.full[s]);
     }
+    t = t_next;
     km = km_next;
-    km_next = km_of(t + 2 * stride);
+    t_next = t_next2;
   }
   end_markers(P, C, seq);
 }
