@@ -186,8 +186,9 @@ def run_reference(args) -> None:
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": cfg["name"], "B": n_req,
-                                        "gamma": cfg["gamma"], "V": cfg["V"]},
+        "data": "synthetic", "config": {"workload": cfg["name"], "B": cfg["B"],
+                                        "gamma": cfg["gamma"], "V": cfg["V"],
+                                        "sample_requests_per_step": n_req},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
