@@ -1649,19 +1649,18 @@ __device__ float2 warp_slot_mass(const Params& P, const Desc& d, const Record& r
       const int s2 = max(s1, d.head_t + vb * E::VEC);
       auto in_t = [&](int e) { return e - d.head_t >= 0 && e - d.head_t < d.nb_t; };
       auto in_d = [&](int e) { return !two || (e - hd >= 0 && e - hd < d.nb_d); };
+      // from_smem: the elements both of whose values are in the slot, read
+      // before it is handed back; otherwise the rest, both values read from
+      // global memory (the slot may already hold the next chunk)
       auto scalar = [&](bool from_smem) {
-        for (int e = lo + lane; e < s1; e += 32) {
-          if ((in_t(e) && in_d(e)) != from_smem) continue;
-          const float lt = in_t(e) ? E::lds(slot, e - d.head_t) : E::load(trow, e);
-          const float ld = !two ? 0.f : in_d(e) ? E::lds(dbody, e - hd) : E::load(drow, e);
+        auto one = [&](int e) {
+          if ((in_t(e) && in_d(e)) != from_smem) return;
+          const float lt = from_smem ? E::lds(slot, e - d.head_t) : E::load(trow, e);
+          const float ld = !two ? 0.f : from_smem ? E::lds(dbody, e - hd) : E::load(drow, e);
           acc += weight(r, lt, ld);
-        }
-        for (int e = s2 + lane; e < hi; e += 32) {
-          if ((in_t(e) && in_d(e)) != from_smem) continue;
-          const float lt = in_t(e) ? E::lds(slot, e - d.head_t) : E::load(trow, e);
-          const float ld = !two ? 0.f : in_d(e) ? E::lds(dbody, e - hd) : E::load(drow, e);
-          acc += weight(r, lt, ld);
-        }
+        };
+        for (int e = lo + lane; e < s1; e += 32) one(e);
+        for (int e = s2 + lane; e < hi; e += 32) one(e);
       };
       scalar(true);
       release();

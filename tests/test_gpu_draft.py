@@ -182,3 +182,14 @@ def test_cached_invalid_stats_isolated():
     ok = np.array([0, 4, 5])
     assert np.array_equal(got["tokens"][ok], ref["tokens"][ok]) or \
         np.all(ref["flags"][ok] & oracle.NEAR_ANY)
+
+
+def test_draft_sample_limits():
+    """n = SV_MAX_GAMMA rows per request, a vocabulary of a million (many
+    rounds of partials in the sampler), and many small rows."""
+    for (B, n, V, dt, seed) in ((3, binding.SV_MAX_GAMMA, 2003, "f32", 31),
+                                (2, 2, 1000003, "bf16", 32), (1500, 2, 129, "bf16", 33)):
+        inp, u = _draft_case(B, n, V, dt, seed=seed)
+        got = run_draft(inp.Ld, u, inp.temp, inp.dtype)
+        ref = oracle.draft_sample(inp.Ld, u, inp.temp, inp.dtype)
+        compare_draft(got, ref, L=inp.Ld, dtype=inp.dtype, temp=inp.temp, u=u)

@@ -268,3 +268,31 @@ def test_near_tie_rate_small_sweep():
     pos = sum(s["positions"] for s in NEAR_LOG)
     near = sum(s["near"] for s in NEAR_LOG)
     print(f"\nsmall sweep: {near} near-ties over {pos} positions")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_maximum_gamma(dtype):
+    """gamma = SV_MAX_GAMMA (33 rows per request: lane 0 also handles row 32)."""
+    cfg = synth.custom_config(5, binding.SV_MAX_GAMMA, 3001, dtype, "normal", temp=0.7,
+                              sigma_noise=0.2)
+    inp = synth.make_inputs(cfg, seed=21)
+    stats = compare_sampling(inp, run_sampling(inp), oracle_sampling(inp))
+    assert stats["mismatches"] <= 1
+    compare_greedy(run_greedy(inp), oracle.greedy(inp.Lt, inp.x, inp.dtype))
+
+
+def test_vocabulary_of_a_million():
+    """V = 1000003 (odd: unaligned rows; ~40 phase-1 chunks and 41 phase-2
+    chunks per row, several rounds of partials in the draw)."""
+    cfg = synth.custom_config(3, 2, 1000003, "bf16", "normal", temp=1.0)
+    inp = synth.make_inputs(cfg, seed=22)
+    stats = compare_sampling(inp, run_sampling(inp), oracle_sampling(inp))
+    assert stats["mismatches"] <= 1
+
+
+def test_many_requests_small_rows():
+    """B = 3000 requests of V = 257: one chunk per row, many rows per CTA."""
+    cfg = synth.custom_config(3000, 3, 257, "f32", "normal", temp=("uniform", 0.5, 1.5))
+    inp = synth.make_inputs(cfg, seed=23)
+    stats = compare_sampling(inp, run_sampling(inp), oracle_sampling(inp))
+    assert stats["mismatches"] <= 1
