@@ -360,8 +360,8 @@ def run_ours(args) -> None:
     out_n = torch.empty(B, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = binding.make_workspace(B, g, V, dev)
-    if args.chunk or args.lag:
-        binding.sv_set_tuning(args.chunk, 0, args.lag)
+    if args.chunk:
+        binding.sv_set_tuning(args.chunk)
 
     def step(t):
         if greedy:
@@ -576,7 +576,6 @@ def main():
                     help="approximate seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-requests", type=int, default=32)
     ap.add_argument("--chunk", type=int, default=0, help="phase-1 chunk elements (0 = auto)")
-    ap.add_argument("--lag", type=int, default=0, help="accepted and ignored (no lag)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

@@ -210,13 +210,11 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
 
 /*
  * Process-wide tuning override for benchmarking sweeps (0 = automatic):
- * elements per phase-1 chunk (rounded up to a multiple of 64, capped at 32 KB
- * of logits).  ctas_per_sm and lag_requests are accepted for compatibility
- * and ignored (the streaming kernel runs one CTA per SM; the stages are
- * separate kernels, so there is no lag).  Not thread-safe; set it before
- * issuing calls.  Returns SV_OK.
+ * elements per phase-1 chunk (rounded up to a multiple of 64, capped at half
+ * a reduce slot of logits).  Not thread-safe; set it before issuing calls.
+ * Returns SV_OK.
  */
-int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests);
+int sv_set_tuning(int chunk_elems);
 
 /*
  * Profiling aid: the next calls record the caller's CUDA events (cudaEvent_t

@@ -60,7 +60,7 @@ def lib() -> ctypes.CDLL:
         L.sv_window_cols.argtypes = [I, I]
         L.sv_window_block_table.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
         L.sv_window_seq_lens_host.argtypes = [P, I, I, I, I, P]
-        L.sv_set_tuning.argtypes = [I, I, I]
+        L.sv_set_tuning.argtypes = [I]
         L.sv_set_stage_events.argtypes = [P, I]
         L.sv_test_withhold_slot.argtypes = [I]
         L.sv_error_string.argtypes = [I]
@@ -123,8 +123,9 @@ def make_workspace(B: int, gamma: int, V: int, device) -> torch.Tensor:
     return ws
 
 
-def sv_set_tuning(chunk_elems: int = 0, ctas_per_sm: int = 0, lag_requests: int = 0) -> None:
-    _check(lib().sv_set_tuning(chunk_elems, ctas_per_sm, lag_requests))
+def sv_set_tuning(chunk_elems: int = 0) -> None:
+    """Elements per phase-1 chunk for the next calls (0 = automatic)."""
+    _check(lib().sv_set_tuning(chunk_elems))
 
 
 def sv_test_withhold_slot(enable: bool) -> None:

@@ -2594,9 +2594,7 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
                               scratch, SV_NOALLOC_MAX_WORKSPACE, dev_status, stream));
 }
 
-int sv_set_tuning(int chunk_elems, int ctas_per_sm, int lag_requests) {
-  (void)ctas_per_sm;   // the reduce kernel always runs one CTA per SM
-  (void)lag_requests;  // the stages run as separate kernels: there is no lag
+int sv_set_tuning(int chunk_elems) {
   g_tune.chunk = chunk_elems > 0 ? chunk_elems : 0;
   return SV_OK;
 }
