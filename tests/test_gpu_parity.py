@@ -296,3 +296,42 @@ def test_many_requests_small_rows():
     inp = synth.make_inputs(cfg, seed=23)
     stats = compare_sampling(inp, run_sampling(inp), oracle_sampling(inp))
     assert stats["mismatches"] <= 1
+
+
+def test_cuda_graph_capture_and_replay():
+    """A verification call captured in a CUDA graph (its programmatic launches
+    become graph edges) and replayed on new inputs copied into the captured
+    buffers gives the oracle's results each time."""
+    cfg = synth.custom_config(9, 4, 6007, "bf16", "mix", temp=0.9)
+    inps = [synth.make_inputs(cfg, seed=40 + k) for k in range(3)]
+    d = to_dev(inps[0])
+    B, g = inps[0].B, inps[0].gamma
+    tok = torch.full((B, g + 1), -7, dtype=torch.int32, device=DEV)
+    n = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = binding.make_workspace(B, g, inps[0].V, DEV)
+    binding.spec_verify(d["Lt"], d["Ld"], d["x"], d["u_acc"], d["u_res"], d["temp"], tok, n, ws,
+                        st)  # first call outside the capture (per-device set-up)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            binding.spec_verify(d["Lt"], d["Ld"], d["x"], d["u_acc"], d["u_res"], d["temp"], tok,
+                                n, ws, st)
+    torch.cuda.synchronize()
+    for inp in inps:
+        nd = to_dev(inp)
+        for k in d:
+            d[k].copy_(nd[k])
+        graph.replay()
+        torch.cuda.synchronize()
+        got = dict(tokens=tok.cpu().numpy(), n=n.cpu().numpy(),
+                   p=np.zeros((B, g, 2), np.float32), Z=np.zeros(B, np.float32),
+                   status=int(st.item()))
+        ref = oracle_sampling(inp)
+        near = (ref["flags"] & oracle.NEAR_ANY) != 0
+        same = np.all(got["tokens"] == ref["tokens"], axis=1) & (got["n"] == ref["n"])
+        assert np.all(same | near), np.argwhere(~(same | near)).ravel()
+        assert got["status"] == 0
