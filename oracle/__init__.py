@@ -1,6 +1,6 @@
 """fp64 CPU oracle for the speculative-decoding verification step and the
 steps around it (draft-row sampling, KV commit on a sink + ring cache, the
-draft KV window's block table).
+draft KV window's block table) and of token-tree verification.
 
 TEST INFRASTRUCTURE.  Only the tests, the smoke check and the CPU-baseline leg
 of the benchmark may import this package; the product path never does.  It
@@ -15,7 +15,10 @@ tiny V, textbook softmax and argmax; for the draft side a u-grid brute force,
 the ln p closed form and losslessness of draft sampling followed by
 verification; for the KV steps the slot formula's permutation property, the
 cache content against a plain sink + sliding-window model, and the draft
-window page's unit-test example with the clone's gather invariant), and
+window page's unit-test example with the clone's gather invariant; for token
+trees the reduction of a chain to the pinned chain rule, the single-node
+inverse CDF, multi-draft losslessness and the never-re-accepted rejected
+token), and
 tests/test_oracle_mutants.py shows that planted mistakes fail those pins.
 """
 from __future__ import annotations
@@ -78,6 +81,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.svo_greedy.restype = I
         lib.svo_draft_sample.argtypes = [I, P, P, P, I, I, I, P, P, P, P, P, ctypes.c_double, I]
         lib.svo_draft_sample.restype = I
+        lib.svo_tree_verify.argtypes = [I, P, P, P, P, P, P, P, I, I, I, P, P, P, P,
+                                        ctypes.c_double, I]
+        lib.svo_tree_verify.restype = I
         lib.kvo_slot_of.argtypes = [ctypes.c_int64, I, I]
         lib.kvo_slot_of.restype = ctypes.c_int64
         lib.kvo_commit.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
@@ -167,6 +173,33 @@ def draft_sample(L, u, temp, dtype: int, near_eps: float = NEAR_EPS,
                               _threads(nthreads))
     if rc != 0:
         raise RuntimeError(f"svo_draft_sample failed with {rc}")
+    return out
+
+
+TREE_MAX_N = 256  # sv_oracle.c: nodes per token tree
+
+
+def tree_verify(Lt, Ld, parent, tokens, u_acc, u_res, temp, dtype: int,
+                near_eps: float = NEAR_EPS, nthreads: int | None = None,
+                lib: ctypes.CDLL | None = None) -> dict:
+    """Token-tree verification oracle (readings T1-T3 of sv_oracle.c).
+    Lt, Ld [B][N][V] (float32, or uint16 bf16 bits); parent, tokens [B][N]
+    int32; u_acc, u_res [B][N]; temp [B].  Returns tokens [B][N], n [B],
+    nodes [B][N] and flags [B]."""
+    lib = lib or load()
+    Lt, Ld = np.ascontiguousarray(Lt), np.ascontiguousarray(Ld)
+    B, N, V = Lt.shape
+    assert Ld.shape == Lt.shape and Ld.dtype == Lt.dtype
+    arr = [np.ascontiguousarray(a, dtype=t).reshape(B, N) for a, t in
+           ((parent, np.int32), (tokens, np.int32), (u_acc, np.float32), (u_res, np.float32))]
+    temp = np.ascontiguousarray(temp, dtype=np.float32).reshape(B)
+    out = dict(tokens=np.empty((B, N), np.int32), n=np.empty(B, np.int32),
+               nodes=np.empty((B, N), np.int32), flags=np.zeros(B, np.int32))
+    rc = lib.svo_tree_verify(int(dtype), _ptr(Lt), _ptr(Ld), *(_ptr(a) for a in arr), _ptr(temp),
+                             B, N, V, _ptr(out["tokens"]), _ptr(out["n"]), _ptr(out["nodes"]),
+                             _ptr(out["flags"]), float(near_eps), _threads(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"svo_tree_verify failed with {rc}")
     return out
 
 

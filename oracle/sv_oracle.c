@@ -61,6 +61,8 @@
 #define SVO_NEAR_SAMPLE 32    /* |C_{v-1}/Z - u| or |C_v/Z - u| < near_eps */
 #define SVO_DEGENERATE 64     /* reading R6 was used */
 
+#define SVO_TREE_MAX_N 256    /* nodes per token tree */
+
 #ifndef SVO_MUTANT
 #define SVO_MUTANT 0 /* the mutation tests rebuild this file with planted mistakes */
 #endif
@@ -527,3 +529,209 @@ int svo_draft_sample(int dtype, const void* L, const float* u, const float* temp
 
 /* Build-identity hook for the mutation tests. */
 int svo_mutant_id(void) { return SVO_MUTANT; }
+
+/* ---------------------------------------------------------------- token tree
+ * Token-tree (multi-branch) verification.  The pages name candidate token
+ * trees ([Deferred-SD], opening section: the draft "emits a candidate token
+ * tree" into the proposal queue; [SD-overview] 考点3: tree attention checks
+ * several branches in one forward pass) but give no acceptance rule for
+ * sibling drafts.  Readings:
+ *   T1  the rejection rule of 考点2 applied to the siblings of a node in
+ *       index order, the target distribution replaced after every rejected
+ *       sibling by the residual of 考点2 -- the multi-draft form of the same
+ *       rejection sampling, lossless when the siblings were drawn
+ *       independently from the node's draft distribution.  At node n:
+ *       r = P_t[n]; for each child c of n, with token x = tokens[c] and
+ *       Q = P_d[n]: accept iff u_acc[c] <= min(1, r(x) / Q(x)) (Q(x) = 0
+ *       accepts, reading R2); an accepted child is emitted and the walk
+ *       moves to it; a rejected one replaces r by
+ *       max(0, r - Q) / sum_v max(0, r - Q).  When no child is accepted (or
+ *       n is a leaf) one token is drawn from r by the inverse CDF of reading
+ *       R5 with u_res[n] and the walk ends.  A residual that vanishes is
+ *       replaced by P_t[n] (reading R6, flagged).
+ *   T2  only the rows the walk reads decide validity: the target row of
+ *       every node it visits and the draft row of every visited node that
+ *       has children.  NaN / +inf in one of them, or one that is all -inf,
+ *       makes the request invalid (reading R8); rows off the walk are never
+ *       read.
+ *   T3  layout: nodes 0..N-1 per request, node 0 the root (parent -1),
+ *       0 <= parent[n] < n otherwise, so a node's children follow it; the
+ *       children of n are the nodes naming n as parent, in index order.
+ *       target row n = the target distribution after the path to n; draft
+ *       row n = the distribution n's children were drawn from.  A malformed
+ *       parent array or a token outside [0, V) makes the request invalid.
+ * Arrays: Lt, Ld [B][N][V]; parent, tokens, u_acc, u_res [B][N] (entry 0 of
+ * tokens and u_acc unused); temp [B].  Outputs: out_tokens [B][N] (tokens of
+ * the accepted nodes, then the drawn token, then -1), out_n [B] (accepted
+ * nodes), out_nodes [B][N] (the accepted nodes, then -1; may be NULL),
+ * out_flags [B] (SVO_* bits).
+ * The loop applies the definition one residual at a time; no closed form of
+ * the repeated residual is used. */
+typedef struct {
+  int dtype;
+  const void *Lt, *Ld;
+  const int32_t *parent, *tokens;
+  const float *u_acc, *u_res, *temp;
+  int B, N, V;
+  int32_t *out_tokens, *out_n, *out_nodes, *out_flags;
+  double near_eps;
+  int b0, b1;
+} tree_job;
+
+static void tree_request(const tree_job* J, int b, double* P, double* Q, double* r, double* w) {
+  const int N = J->N, V = J->V;
+  int32_t* tok = J->out_tokens + (size_t)b * N;
+  int32_t* nodes = J->out_nodes ? J->out_nodes + (size_t)b * N : NULL;
+  const int32_t* par = J->parent + (size_t)b * N;
+  const int32_t* xt = J->tokens + (size_t)b * N;
+  int32_t flags = 0;
+  for (int i = 0; i < N; ++i) {
+    tok[i] = -1;
+    if (nodes) nodes[i] = -1;
+  }
+  J->out_n[b] = 0;
+  const double T = (double)J->temp[b];
+  if (!(isfinite(T) && T >= 0x1p-126)) flags |= SVO_INVALID_TEMP;
+  if (par[0] != -1) flags |= SVO_INVALID_TOKEN;
+  for (int n = 1; n < N; ++n)
+    if (par[n] < 0 || par[n] >= n || xt[n] < 0 || xt[n] >= V) flags |= SVO_INVALID_TOKEN;
+  if (flags) {
+    J->out_flags[b] = flags;
+    return;
+  }
+  int n = 0, k = 0;
+  int32_t emitted[SVO_TREE_MAX_N], path[SVO_TREE_MAX_N];
+  for (;;) {
+    int has_child = 0;
+    for (int c = n + 1; c < N; ++c) has_child |= (par[c] == n);
+    if (!softmax_row(J->Lt, J->dtype, ((size_t)b * N + n) * V, V, T, P) ||
+        (has_child && !softmax_row(J->Ld, J->dtype, ((size_t)b * N + n) * V, V, T, Q))) {
+      J->out_flags[b] = flags | SVO_INVALID_NONFINITE; /* reading T2 */
+      return;
+    }
+    for (int v = 0; v < V; ++v) r[v] = P[v];
+    int next = -1;
+    for (int c = n + 1; c < N && next < 0; ++c) {
+      if (par[c] != n) continue;
+      const int x = xt[c];
+      const double ratio = (Q[x] > 0.0) ? fmin(1.0, r[x] / Q[x]) : 1.0; /* reading R2 */
+      const double u = (double)J->u_acc[(size_t)b * N + c];
+      if (fabs(u - ratio) < J->near_eps) flags |= SVO_NEAR_ACCEPT;
+#if SVO_MUTANT == 16
+      const int accept = u <= ((Q[x] > 0.0) ? fmin(1.0, P[x] / Q[x]) : 1.0); /* planted: r unused */
+#else
+      const int accept = u <= ratio;
+#endif
+      if (accept) {
+        next = c;
+        break;
+      }
+      double Z = 0.0;
+      for (int v = 0; v < V; ++v) {
+#if SVO_MUTANT == 17
+        r[v] = fmax(0.0, P[v] - Q[v]); /* planted: the residual restarts from P_t */
+#else
+        r[v] = fmax(0.0, r[v] - Q[v]);
+#endif
+        Z += r[v];
+      }
+      if (!(Z > 0.0)) { /* reading R6 */
+        flags |= SVO_DEGENERATE;
+        for (int v = 0; v < V; ++v) r[v] = P[v];
+      } else {
+        for (int v = 0; v < V; ++v) r[v] /= Z;
+      }
+    }
+    if (next < 0) {
+      double Z = 0.0;
+      for (int v = 0; v < V; ++v) {
+        w[v] = r[v];
+        Z += w[v];
+      }
+      int near = 0;
+      double dist = INFINITY;
+      emitted[k] = inverse_cdf(w, V, Z, (double)J->u_res[(size_t)b * N + n], J->near_eps, &near,
+                               &dist);
+      if (near) flags |= SVO_NEAR_SAMPLE;
+      break;
+    }
+    emitted[k] = xt[next];
+    path[k] = next;
+    ++k;
+    n = next;
+  }
+  for (int i = 0; i <= k; ++i) tok[i] = emitted[i];
+  if (nodes)
+    for (int i = 0; i < k; ++i) nodes[i] = path[i];
+  J->out_n[b] = k;
+  J->out_flags[b] = flags;
+}
+
+static void* tree_worker(void* arg) {
+  const tree_job* J = (const tree_job*)arg;
+  const size_t V = (size_t)J->V;
+  double* P = (double*)malloc(V * sizeof(double));
+  double* Q = (double*)malloc(V * sizeof(double));
+  double* r = (double*)malloc(V * sizeof(double));
+  double* w = (double*)malloc(V * sizeof(double));
+  for (int b = J->b0; b < J->b1; ++b) {
+    if (!P || !Q || !r || !w)
+      J->out_flags[b] = -1;
+    else
+      tree_request(J, b, P, Q, r, w);
+  }
+  free(P);
+  free(Q);
+  free(r);
+  free(w);
+  return NULL;
+}
+
+/* Token-tree verification (readings T1-T3 above).  Returns 0, -1 on a bad
+ * argument (N outside [1, SVO_TREE_MAX_N]), -2 when out of memory. */
+int svo_tree_verify(int dtype, const void* Lt, const void* Ld, const int32_t* parent,
+                    const int32_t* tokens, const float* u_acc, const float* u_res,
+                    const float* temp, int B, int N, int V, int32_t* out_tokens, int32_t* out_n,
+                    int32_t* out_nodes, int32_t* out_flags, double near_eps, int nthreads) {
+  if (B < 0 || N < 1 || N > SVO_TREE_MAX_N || V < 1 || (dtype != SVO_F32 && dtype != SVO_BF16))
+    return -1;
+  if (B == 0) return 0;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > B) nthreads = B;
+  tree_job* jobs = (tree_job*)calloc((size_t)nthreads, sizeof(tree_job));
+  pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  if (!jobs || !th) {
+    free(jobs);
+    free(th);
+    return -2;
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    tree_job* J = &jobs[t];
+    J->dtype = dtype;
+    J->Lt = Lt;
+    J->Ld = Ld;
+    J->parent = parent;
+    J->tokens = tokens;
+    J->u_acc = u_acc;
+    J->u_res = u_res;
+    J->temp = temp;
+    J->B = B;
+    J->N = N;
+    J->V = V;
+    J->out_tokens = out_tokens;
+    J->out_n = out_n;
+    J->out_nodes = out_nodes;
+    J->out_flags = out_flags;
+    J->near_eps = near_eps;
+    J->b0 = (int)((long long)B * t / nthreads);
+    J->b1 = (int)((long long)B * (t + 1) / nthreads);
+  }
+  for (int t = 1; t < nthreads; ++t) pthread_create(&th[t], NULL, tree_worker, &jobs[t]);
+  tree_worker(&jobs[0]);
+  for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
+  free(jobs);
+  free(th);
+  for (int b = 0; b < B; ++b)
+    if (out_flags[b] < 0) return -2;
+  return 0;
+}

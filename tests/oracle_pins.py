@@ -628,3 +628,157 @@ def pin_window_block_table(lib):
 
 ALL_PINS += [pin_draft_sample_grid, pin_draft_then_verify_lossless, pin_draft_sample_invalid,
              pin_kv_slot_closed_form, pin_kv_commit_content, pin_window_block_table]
+
+
+# ------------------------------------------------------------ token trees
+# Readings T1-T3 of the oracle (multi-branch verification): the pages name
+# token trees but give no rule for siblings; the pins below hold for any
+# correct multi-draft rejection sampler and reduce to the pinned chain rule.
+
+def _tree_batch(B, Lt_rows, Ld_rows, parent, tokens, temp):
+    N, V = np.asarray(Lt_rows).shape
+    Lt = np.ascontiguousarray(np.broadcast_to(np.asarray(Lt_rows, np.float32), (B, N, V)))
+    Ld = np.ascontiguousarray(np.broadcast_to(np.asarray(Ld_rows, np.float32), (B, N, V)))
+    par = np.ascontiguousarray(np.broadcast_to(np.asarray(parent, np.int32), (B, N)))
+    tok = np.ascontiguousarray(np.broadcast_to(np.asarray(tokens, np.int32), (B, N)))
+    return Lt, Ld, par, tok, np.full(B, temp, np.float32)
+
+
+def pin_tree_chain_is_verify(lib):
+    """A chain (parent[n] = n - 1) is the plain verification of 考点2 / 第三章:
+    node n's target row is position n, its draft row position n, its token
+    the draft token n - 1; the leaf's draft row is never read (NaN there
+    changes nothing).  Every output equals the pinned chain oracle's."""
+    rng = np.random.default_rng(41)
+    B, gamma, V = 300, 4, 11
+    T = np.float32(0.8)
+    Lt = rng.normal(0, 1.5, size=(B, gamma + 1, V)).astype(np.float32)
+    Ld = (Lt[:, :gamma] + rng.normal(0, 0.8, size=(B, gamma, V))).astype(np.float32)
+    x = rng.integers(0, V, size=(B, gamma)).astype(np.int32)
+    ua = rng.random((B, gamma), dtype=np.float32)
+    ur = rng.random((B, gamma + 1), dtype=np.float32)
+    temp = np.full(B, T, np.float32)
+    ref = oracle.verify(Lt, Ld, x, ua, ur, temp, F32, lib=lib)
+    Ldt = np.concatenate([Ld, np.full((B, 1, V), np.nan, np.float32)], axis=1)
+    par = np.broadcast_to(np.arange(-1, gamma, dtype=np.int32), (B, gamma + 1))
+    tok = np.concatenate([np.zeros((B, 1), np.int32), x], axis=1)
+    uat = np.concatenate([np.zeros((B, 1), np.float32), ua], axis=1)
+    out = oracle.tree_verify(Lt, Ldt, par, tok, uat, ur, temp, F32, lib=lib)
+    assert np.array_equal(out["n"], ref["n"])
+    assert np.array_equal(out["tokens"], ref["tokens"])
+    assert np.array_equal(out["flags"], ref["flags"])
+    for b in range(B):  # a chain's accepted nodes are 1 .. n
+        assert list(out["nodes"][b, :out["n"][b]]) == list(range(1, out["n"][b] + 1))
+
+
+def pin_tree_single_node(lib):
+    """N = 1: the walk ends at the root and draws from softmax(Lt[0] / T) by
+    the index-order inverse CDF (np.searchsorted on the cumulative sum,
+    side='right')."""
+    rng = np.random.default_rng(42)
+    V, m = 13, 4000
+    T = float(np.float32(1.3))
+    lt = rng.normal(0, 2, size=(1, V)).astype(np.float32)
+    u = _midgrid(m)
+    Lt, Ld, par, tok, temp = _tree_batch(m, lt, np.zeros((1, V)), [-1], [0], T)
+    out = oracle.tree_verify(Lt, Ld, par, tok, np.zeros((m, 1), np.float32), u[:, None], temp,
+                             F32, lib=lib)
+    p = softmax(lt[0].astype(np.float64) / T)
+    cum = np.cumsum(p)
+    want = np.searchsorted(cum, u.astype(np.float64) * cum[-1], side="right")
+    far = np.min(np.abs(cum[None, :] / cum[-1] - u.astype(np.float64)[:, None]), 1) >= 1e-6
+    assert np.all(out["n"] == 0) and np.all(out["tokens"][:, 0] >= 0)
+    assert np.array_equal(out["tokens"][far, 0], want[far])
+
+
+def pin_tree_rejected_token_stays_rejected(lib):
+    """After sibling c is rejected with token x (u > P_t(x) / P_d(x), so
+    P_t(x) < P_d(x)), every later residual has r(x) = 0: a later sibling with
+    the same token is rejected whenever its u is positive.  Tree: root with
+    four siblings all carrying the token whose target / draft ratio is
+    smallest."""
+    rng = np.random.default_rng(43)
+    B, V = 2000, 6
+    lt = rng.normal(0, 1, size=(5, V)).astype(np.float32)
+    ld = rng.normal(0, 1, size=(5, V)).astype(np.float32)
+    p0 = softmax(lt[0].astype(np.float64))
+    q0 = softmax(ld[0].astype(np.float64))
+    x = int(np.argmin(p0 / q0))
+    a = p0[x] / q0[x]
+    assert a < 0.9
+    Lt, Ld, par, tok, temp = _tree_batch(B, lt, ld, [-1, 0, 0, 0, 0], [0, x, x, x, x], 1.0)
+    ua = rng.random((B, 5), dtype=np.float32) * np.float32(0.999) + np.float32(1e-4)
+    out = oracle.tree_verify(Lt, Ld, par, tok, ua, rng.random((B, 5), dtype=np.float32), temp,
+                             F32, lib=lib)
+    first = ua[:, 1].astype(np.float64) <= a
+    assert np.all(out["nodes"][first, 0] == 1)  # the first sibling is tested by P_t / P_d
+    assert np.all(out["n"][~first] == 0)        # later copies of x are never accepted
+    assert np.all(out["tokens"][~first, 0] != x)
+
+
+def pin_tree_losslessness(lib, trials=400_000):
+    """Multi-draft form of the 考点2 identity: the root has three siblings and
+    each of them two children, every sibling drawn independently from its
+    parent's draft distribution; the first emitted token follows P_t[root]
+    and, given that a depth-1 node was accepted, the second follows that
+    node's target row (all depth-1 nodes share their rows).  Chi-square, 7
+    degrees of freedom, rejected above 24.32 (p = 0.001)."""
+    rng = np.random.default_rng(44)
+    V = 8
+    T = float(np.float32(0.9))
+    lt0, lt1 = (rng.normal(0, 1.5, size=V).astype(np.float32) for _ in range(2))
+    ld0, ld1 = (rng.normal(0, 1.5, size=V).astype(np.float32) for _ in range(2))
+    parent = [-1, 0, 0, 0, 1, 1, 2, 2, 3, 3]
+    N = len(parent)
+    rows_t = np.stack([lt0] + [lt1] * 3 + [lt0] * 6)
+    rows_d = np.stack([ld0] + [ld1] * 3 + [ld0] * 6)
+    Pt0, Pt1 = (softmax(r.astype(np.float64) / T) for r in (lt0, lt1))
+    Q0, Q1 = (softmax(r.astype(np.float64) / T) for r in (ld0, ld1))
+    tok = np.zeros((trials, N), np.int32)
+    for n in range(1, 4):
+        tok[:, n] = rng.choice(V, size=trials, p=Q0)
+    for n in range(4, N):
+        tok[:, n] = rng.choice(V, size=trials, p=Q1)
+    Lt, Ld, par, _, temp = _tree_batch(trials, rows_t, rows_d, parent, np.zeros(N), T)
+    out = oracle.tree_verify(Lt, Ld, par, tok, rng.random((trials, N), dtype=np.float32),
+                             rng.random((trials, N), dtype=np.float32), temp, F32, lib=lib)
+    assert np.all(out["tokens"][:, 0] >= 0)
+    for pos, P, sel in ((0, Pt0, np.ones(trials, bool)), (1, Pt1, out["n"] >= 1)):
+        obs = np.bincount(out["tokens"][sel, pos], minlength=V)
+        exp_ = P * sel.sum()
+        chi2 = float(((obs - exp_) ** 2 / exp_).sum())
+        assert chi2 < 24.32, (pos, chi2)
+
+
+def pin_tree_invalid(lib):
+    """Readings T2/T3: a malformed parent array or an out-of-range token makes
+    the request invalid; NaN in a row the walk reads invalidates it, NaN in a
+    row off the walk does not."""
+    V = 5
+    lt = np.zeros((4, V), np.float32)
+    lt[:, 2] = 3.0  # every target row puts nearly all mass on token 2
+    ld = np.zeros((4, V), np.float32)
+    ld[:, 2] = 3.0
+    parent = [-1, 0, 0, 1]
+    Lt, Ld, par, tok, temp = _tree_batch(6, lt, ld, parent, [0, 2, 1, 2], 1.0)
+    Lt, Ld, par, tok = Lt.copy(), Ld.copy(), par.copy(), tok.copy()
+    ua = np.full((6, 4), 0.01, np.float32)  # node 1 (token 2, ratio 1) is always accepted
+    ur = np.full((6, 4), 0.5, np.float32)
+    par[1, 2] = 2     # parent not before the node
+    tok[2, 3] = V     # token out of range
+    Lt[3, 2, 0] = np.nan  # node 2 is never visited: its row is not read
+    Ld[3, 3, 1] = np.nan  # node 3 is a leaf: its draft row is not read
+    Lt[4, 3, 4] = np.inf  # node 3's target row is read (the walk ends there)
+    temp[5] = 0.0
+    out = oracle.tree_verify(Lt, Ld, par, tok, ua, ur, temp, F32, lib=lib)
+    assert out["flags"][1] & oracle.INVALID_TOKEN and out["flags"][2] & oracle.INVALID_TOKEN
+    assert out["flags"][4] & oracle.INVALID_NONFINITE and out["flags"][5] & oracle.INVALID_TEMP
+    for b in (1, 2, 4, 5):
+        assert out["n"][b] == 0 and np.all(out["tokens"][b] == -1) and np.all(out["nodes"][b] == -1)
+    for b in (0, 3):
+        assert out["flags"][b] & oracle.INVALID_ANY == 0
+        assert list(out["nodes"][b, :2]) == [1, 3] and list(out["tokens"][b, :3]) == [2, 2, 2]
+
+
+ALL_PINS += [pin_tree_chain_is_verify, pin_tree_single_node,
+             pin_tree_rejected_token_stays_rejected, pin_tree_losslessness, pin_tree_invalid]

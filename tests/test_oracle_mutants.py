@@ -8,7 +8,9 @@ from the wrong row, swapped residual operands, no max shift in the softmax, a
 dropped softmax term, a greedy tie broken to the last index, a draft sample
 without the temperature, a ring slot without the sink offset, a KV commit
 that drops the last emitted token's entry, a draft window start not aligned
-to a block, and a block-table clone not zeroed past `needed`.
+to a block, a block-table clone not zeroed past `needed`, a token-tree
+sibling tested against the target row instead of the current residual, and a
+token-tree residual that restarts from the target row at every rejection.
 """
 import pytest
 
@@ -31,6 +33,8 @@ MUTANTS = {
     13: "KV commit drops the last emitted token's entry",
     14: "draft window start not block-aligned",
     15: "block-table clone not zeroed past needed",
+    16: "tree sibling tested against P_t instead of the residual",
+    17: "tree residual restarts from P_t at every rejection",
 }
 
 
