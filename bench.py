@@ -322,6 +322,79 @@ def measure_kv_side(binding, torch, dev, stream, B, g, num_accepted, steps, warm
     }
 
 
+def measure_tree_side(binding, torch, dev, stream, steps, warmup, peak, sets=3) -> dict:
+    """Token-tree verification (sv_tree_verify) on its workload: 64 requests,
+    22-node trees (3, 2, 1, 1 children per level), V = 151936 bf16.  `sets`
+    device copies of one batch at distinct addresses rotate between calls,
+    so no call finds its rows in L2.  The algorithmic bytes of a call are the
+    rows its walks must read once: each visited node's target row and the
+    draft row of each visited node with children."""
+    cfg = synth.TREE_WORKLOAD
+    parent = synth.tree_parents(cfg["branching"])
+    ti = synth.make_tree_inputs(cfg, parent)
+    B, N, V = ti.B, ti.N, ti.V
+
+    def dev_set():
+        t = {k: torch.from_numpy(np.ascontiguousarray(getattr(ti, k))).to(dev)
+             for k in ("Lt", "Ld", "parent", "tokens", "u_acc", "u_res", "temp")}
+        t["Lt"], t["Ld"] = t["Lt"].view(torch.bfloat16), t["Ld"].view(torch.bfloat16)
+        return t
+
+    ds = [dev_set() for _ in range(sets)]
+    tok = torch.empty(B, N, dtype=torch.int32, device=dev)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    nodes = torch.empty(B, N, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call(i):
+        t = ds[i % sets]
+        binding.sv_tree_verify(t["Lt"], t["Ld"], t["parent"], t["tokens"], t["u_acc"],
+                               t["u_res"], t["temp"], tok, n, nodes, st, stream)
+
+    for i in range(warmup):
+        call(i)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for i in range(steps):
+        call(i)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / steps
+    n_h, nodes_h = n.cpu().numpy(), nodes.cpu().numpy()
+    has_child = np.zeros(N, bool)
+    has_child[parent[1:]] = True
+    row = V * 2
+    rows = 0
+    for r in range(B):
+        for v in [0] + [int(c) for c in nodes_h[r, :n_h[r]]]:
+            rows += 1 + int(has_child[v])
+    moved = rows * row
+    del ds
+    return {"workload": cfg["name"], "B": B, "N": N, "V": V, "ms_per_call": ms,
+            "requests_per_s": B / (ms / 1e3), "accepted_per_request": float(n_h.mean()),
+            "emitted_tokens_per_s": float((n_h + 1).sum()) / (ms / 1e3),
+            "rows_read_per_call": rows, "algorithmic_bytes": moved,
+            "all_rows_bytes": int((ti.Lt.nbytes + ti.Ld.nbytes)),
+            "achieved_gbs": moved / (ms / 1e3) / 1e9,
+            "frac_of_peak": moved / (ms / 1e3) / 1e9 / peak,
+            "l2": f"{sets} device copies at distinct addresses, rotated", "kernels": 1,
+            "status": int(st.item())}
+
+
+def run_tree_only(args) -> None:
+    """Token-tree verification alone (for profiling captures): one JSON dict."""
+    import torch
+
+    from speculative_decoding_verification_09_gb300 import binding
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    binding.lib()
+    peak, _ = read_peaks()
+    print(json.dumps(measure_tree_side(binding, torch, dev, torch.cuda.current_stream(dev),
+                                       args.steps, args.warmup, peak, sets=args.tree_sets)))
+
+
 def run_ours(args) -> None:
     import torch
 
@@ -443,6 +516,9 @@ def run_ours(args) -> None:
     draft_side = None if (greedy or args.no_draft_side) else measure_draft_side(
         binding, torch, dev, stream, sets, host_sets, B, g, V, ws, out_tok, out_n, status,
         args.steps, args.warmup, peak)
+    tree_side = None
+    if not args.no_tree_side:
+        tree_side = measure_tree_side(binding, torch, dev, stream, args.steps, args.warmup, peak)
     kv_side = None
     if not args.no_kv_side:
         step(sets[0])  # the accepted counts of one verification drive the commit
@@ -556,7 +632,7 @@ def run_ours(args) -> None:
         "stages_ms_extra_calls": stage_ms, "call_ms": launch_ms,
         "single_call_latency_ms": latency_ms,
         "call_equivalent_gbs": logit_bytes / (launch_ms / 1e3) / 1e9,
-        "draft_side": draft_side, "kv_side": kv_side,
+        "draft_side": draft_side, "kv_side": kv_side, "tree_side": tree_side,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_kern * args.steps, "clocks": clk,
         "status": st, "wall_s_timed": t_wall,
         "tuning": {"chunk": args.chunk},
@@ -585,6 +661,11 @@ def main():
                     help="skip timing sv_draft_sample and spec_verify_cached")
     ap.add_argument("--no-kv-side", action="store_true",
                     help="skip timing the KV commit, valid slots and block-table window")
+    ap.add_argument("--no-tree-side", action="store_true",
+                    help="skip timing token-tree verification")
+    ap.add_argument("--tree-only", action="store_true",
+                    help="time token-tree verification alone (profiling captures)")
+    ap.add_argument("--tree-sets", type=int, default=3)
     ap.add_argument("--kv-window", type=int, default=KV_MODEL["window"],
                     help="ring slots of the KV-commit measurement (smaller for profiling captures)")
     ap.add_argument("--cpu-requests", type=int, default=256)
@@ -595,7 +676,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.impl == "reference":
+    if args.tree_only:
+        run_tree_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

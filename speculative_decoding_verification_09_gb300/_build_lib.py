@@ -7,8 +7,8 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRCS = [os.path.join(PKG, "csrc", f) for f in ("specverify.cu", "kvcache.cu")]
-HEADERS = [os.path.join(ROOT, "include", f) for f in ("specverify.h", "svkv.h")]
+SRCS = [os.path.join(PKG, "csrc", f) for f in ("specverify.cu", "kvcache.cu", "tree.cu")]
+HEADERS = [os.path.join(ROOT, "include", f) for f in ("specverify.h", "svkv.h", "svtree.h")]
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libspecverify.so")
 

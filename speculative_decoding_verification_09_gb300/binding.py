@@ -26,7 +26,8 @@ EXPORTED = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_veri
             "sv_draft_workspace_bytes", "sv_draft_sample", "sv_set_tuning",
             "sv_set_stage_events", "sv_test_withhold_slot", "sv_error_string", "sv_version",
             "sv_kv_commit", "sv_kv_valid_slots", "sv_window_cols", "sv_window_block_table",
-            "sv_window_seq_lens_host")
+            "sv_window_seq_lens_host", "sv_tree_verify", "sv_tree_set_cluster")
+SV_TREE_MAX_N = 256
 SV_NOALLOC_MAX_WORKSPACE = 16 << 20
 
 _lib = None
@@ -60,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.sv_window_cols.argtypes = [I, I]
         L.sv_window_block_table.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
         L.sv_window_seq_lens_host.argtypes = [P, I, I, I, I, P]
+        L.sv_tree_verify.argtypes = [I, P, P, P, P, P, P, P, I, I, I, P, P, P, P, P]
+        L.sv_tree_set_cluster.argtypes = [I]
         L.sv_set_tuning.argtypes = [I]
         L.sv_set_stage_events.argtypes = [P, I]
         L.sv_test_withhold_slot.argtypes = [I]
@@ -70,7 +73,8 @@ def lib() -> ctypes.CDLL:
                      "sv_draft_sample", "sv_set_tuning", "sv_set_stage_events", "sv_version",
                      "sv_test_withhold_slot",
                      "sv_kv_commit", "sv_kv_valid_slots", "sv_window_cols",
-                     "sv_window_block_table", "sv_window_seq_lens_host"):
+                     "sv_window_block_table", "sv_window_seq_lens_host", "sv_tree_verify",
+                     "sv_tree_set_cluster"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -337,3 +341,34 @@ def sv_window_seq_lens_host(seq_lens, window: int, block_size: int, future_offse
         src.ctypes.data_as(ctypes.c_void_p), int(src.size), window, block_size, future_offset,
         out.ctypes.data_as(ctypes.c_void_p)))
     return out
+
+
+def sv_tree_verify(target_logits, draft_logits, parent, tokens, u_accept, u_residual,
+                   temperature, out_tokens, out_num_accepted, out_nodes=None, dev_status=None,
+                   stream=None) -> None:
+    """Token-tree verification.  target_logits / draft_logits [B][N][V]
+    (float32 or bfloat16; draft_logits may be None when N == 1), parent /
+    tokens [B][N] int32, u_accept / u_residual [B][N] and temperature [B]
+    float32; outputs out_tokens [B][N], out_num_accepted [B], out_nodes
+    [B][N] (optional), all int32."""
+    if target_logits.dim() != 3:
+        raise SpecVerifyError("target_logits must be [B][N][V]")
+    B, N, V = target_logits.shape
+    dt = _dtype_code(target_logits)
+    if draft_logits is not None and (draft_logits.dtype != target_logits.dtype
+                                     or tuple(draft_logits.shape) != (B, N, V)):
+        raise SpecVerifyError("draft_logits must match target_logits in shape and dtype")
+    _check(lib().sv_tree_verify(
+        dt, _dev(target_logits, None, "target_logits"), _dev(draft_logits, None, "draft_logits"),
+        _dev(parent, torch.int32, "parent"), _dev(tokens, torch.int32, "tokens"),
+        _dev(u_accept, torch.float32, "u_accept"), _dev(u_residual, torch.float32, "u_residual"),
+        _dev(temperature, torch.float32, "temperature"), B, N, V,
+        _dev(out_tokens, torch.int32, "out_tokens"),
+        _dev(out_num_accepted, torch.int32, "out_num_accepted"),
+        _dev(out_nodes, torch.int32, "out_nodes"), _dev(dev_status, torch.int32, "dev_status"),
+        _stream(stream, target_logits.device)))
+
+
+def sv_tree_set_cluster(ctas: int = 0) -> None:
+    """CTAs per request for sv_tree_verify: 0 = automatic, 1..8 forced."""
+    _check(lib().sv_tree_set_cluster(int(ctas)))

@@ -118,35 +118,42 @@ def _gumbel_argmax(rng: np.random.Generator, logits64: np.ndarray, T: float) -> 
     return int(np.argmax(logits64 / T + rng.gumbel(size=logits64.shape[0])))
 
 
+def _target_row(cfg: dict, rt: np.random.Generator, V: int) -> np.ndarray:
+    kind = cfg["kind"]
+    if kind in ("normal", "greedy"):
+        return cfg["sigma_t"] * rt.standard_normal(V)
+    if kind == "zipf":
+        return _zipf_row(rt, V, cfg["zipf_s"], cfg["zipf_noise"])
+    if kind == "mix":
+        return cfg["sigma"] * rt.standard_normal(V)
+    raise ValueError(kind)
+
+
+def _draft_row(cfg: dict, rd: np.random.Generator, lt: np.ndarray, b: int, B: int) -> np.ndarray:
+    kind, V = cfg["kind"], lt.shape[0]
+    if kind in ("normal", "greedy"):
+        return lt + cfg["sigma_noise"] * rd.standard_normal(V)
+    if kind == "zipf":
+        rho = cfg["rho"]
+        return rho * lt + np.sqrt(1.0 - rho * rho) * _zipf_row(rd, V, cfg["zipf_s"],
+                                                               cfg["zipf_noise"])
+    # mix: draft distribution = w * softmax(target) + (1-w) * softmax(Q)
+    from scipy.special import log_softmax
+    w = cfg["weights"][min(len(cfg["weights"]) - 1, (len(cfg["weights"]) * b) // B)]
+    q = cfg["sigma"] * rd.standard_normal(V)
+    ld = np.logaddexp(np.log(w) + log_softmax(lt), np.log1p(-w) + log_softmax(q))
+    return ld - ld.max()  # shift so the stored bf16 values keep their precision
+
+
 def _draw_request(cfg: dict, seed: int, set_index: int, b: int, B: int, gamma: int, V: int,
                   dtype: int, T: float, Lt: np.ndarray, Ld: np.ndarray, x: np.ndarray) -> None:
     kind = cfg["kind"]
     for i in range(gamma + 1):
-        rt = rng_for(seed, set_index, _TAG_TARGET, b, i)
-        if kind in ("normal", "greedy"):
-            lt = cfg["sigma_t"] * rt.standard_normal(V)
-        elif kind == "zipf":
-            lt = _zipf_row(rt, V, cfg["zipf_s"], cfg["zipf_noise"])
-        elif kind == "mix":
-            lt = cfg["sigma"] * rt.standard_normal(V)
-        else:
-            raise ValueError(kind)
+        lt = _target_row(cfg, rng_for(seed, set_index, _TAG_TARGET, b, i), V)
         Lt[b, i] = round_to_dtype(lt, dtype)
         if i == gamma:
             break
-        rd = rng_for(seed, set_index, _TAG_DRAFT, b, i)
-        if kind in ("normal", "greedy"):
-            ld = lt + cfg["sigma_noise"] * rd.standard_normal(V)
-        elif kind == "zipf":
-            rho = cfg["rho"]
-            ld = rho * lt + np.sqrt(1.0 - rho * rho) * _zipf_row(rd, V, cfg["zipf_s"],
-                                                                  cfg["zipf_noise"])
-        else:  # mix: draft distribution = w * softmax(target) + (1-w) * softmax(Q)
-            from scipy.special import log_softmax
-            w = cfg["weights"][min(len(cfg["weights"]) - 1, (len(cfg["weights"]) * b) // B)]
-            q = cfg["sigma"] * rd.standard_normal(V)
-            ld = np.logaddexp(np.log(w) + log_softmax(lt), np.log1p(-w) + log_softmax(q))
-            ld -= ld.max()  # shift so the stored bf16 values keep their precision
+        ld = _draft_row(cfg, rng_for(seed, set_index, _TAG_DRAFT, b, i), lt, b, B)
         Ld[b, i] = round_to_dtype(ld, dtype)
         rx = rng_for(seed, set_index, _TAG_TOKEN, b, i)
         ld_stored = widen(Ld[b, i], dtype)
@@ -215,3 +222,136 @@ def custom_config(B: int, gamma: int, V: int, dtype: str = "bf16", kind: str = "
 def draft_uniforms(B: int, n: int, seed: int, set_index: int = 0) -> np.ndarray:
     """u_draft [B][n]: fp32 uniforms in [0, 1) for sampling the draft rows."""
     return rng_for(seed, set_index, _TAG_DRAFT_UNIFORM).random((B, n), dtype=np.float32)
+
+
+# ---------------------------------------------------------------- token trees
+
+_TAG_TREE_TARGET, _TAG_TREE_DRAFT, _TAG_TREE_TOKEN, _TAG_TREE_UNIFORM, _TAG_TREE_SHAPE = (
+    8, 9, 10, 11, 12)
+
+# the token-tree workload: 64 requests, a tree with 3 root children, 2 below
+# each of them, then two single-child levels (22 nodes, depth 4), the c4
+# vocabulary and row model
+TREE_WORKLOAD = dict(name="tree_b3211_B64_N22_V151936_bf16", B=64, branching=(3, 2, 1, 1),
+                     V=151936, dtype="bf16", kind="mix", sigma=2.5, weights=(0.3, 0.6, 0.9),
+                     temp=1.0)
+
+
+def tree_parents(branching) -> np.ndarray:
+    """Parent array (node order: level by level) of a tree whose nodes at
+    depth d have branching[d] children each; the root's parent is -1."""
+    parent, level = [-1], [0]
+    for k in branching:
+        nxt = []
+        for p in level:
+            for _ in range(k):
+                parent.append(p)
+                nxt.append(len(parent) - 1)
+        level = nxt
+    return np.array(parent, np.int32)
+
+
+def random_parents(N: int, seed: int, max_children: int = 4) -> np.ndarray:
+    """A random tree on N nodes with parent[n] < n and at most max_children
+    children per node."""
+    rng = rng_for(seed, _TAG_TREE_SHAPE)
+    parent = np.full(N, -1, np.int32)
+    kids = np.zeros(N, np.int64)
+    for n in range(1, N):
+        while True:
+            p = int(rng.integers(max(0, n - 8), n))
+            if kids[p] < max_children:
+                break
+        parent[n] = p
+        kids[p] += 1
+    return parent
+
+
+@dataclasses.dataclass
+class TreeInputs:
+    """One batch of token-tree verification inputs, host-resident.
+
+    Lt, Ld [B][N][V]  target / draft logits (float32, or uint16 bf16 bits);
+                      the draft rows of leaves are never read (filled with
+                      `leaf_fill`)
+    parent [B][N], tokens [B][N]  int32 (tokens[b][0] = 0, unused)
+    u_acc, u_res [B][N]  float32 uniforms in [0, 1)
+    temp [B]          float32
+    """
+    Lt: np.ndarray
+    Ld: np.ndarray
+    parent: np.ndarray
+    tokens: np.ndarray
+    u_acc: np.ndarray
+    u_res: np.ndarray
+    temp: np.ndarray
+    dtype: int
+    B: int
+    N: int
+    V: int
+    name: str = "tree"
+
+    def visited_bytes_bound(self) -> int:
+        return (self.Lt.size + self.Ld.size) * ELEM_BYTES[self.dtype]
+
+
+def _draw_tree_request(cfg, seed, set_index, b, B, parent, V, dtype, T, leaf_fill, Lt, Ld, tok):
+    N = parent.shape[0]
+    has_child = np.zeros(N, bool)
+    has_child[parent[1:]] = True
+    for n in range(N):
+        lt = _target_row(cfg, rng_for(seed, set_index, _TAG_TREE_TARGET, b, n), V)
+        Lt[b, n] = round_to_dtype(lt, dtype)
+        if has_child[n]:
+            ld = _draft_row(cfg, rng_for(seed, set_index, _TAG_TREE_DRAFT, b, n), lt, b, B)
+            Ld[b, n] = round_to_dtype(ld, dtype)
+        else:
+            Ld[b, n] = round_to_dtype(np.full(V, leaf_fill), dtype)
+    # every child's token is drawn from its parent's stored draft row
+    # (Gumbel-max at the request's temperature), independently per sibling
+    for n in range(1, N):
+        rx = rng_for(seed, set_index, _TAG_TREE_TOKEN, b, n)
+        tok[b, n] = _gumbel_argmax(rx, widen(Ld[b, parent[n]], dtype), T)
+
+
+def make_tree_inputs(cfg: dict, parent, seed: int = BASE_SEED, set_index: int = 0,
+                     B: int | None = None, leaf_fill: float = 0.0,
+                     threads: int | None = None) -> TreeInputs:
+    """Draw one batch of token-tree inputs: `cfg` a row model (the keys of
+    custom_config or TREE_WORKLOAD), `parent` one parent array [N] shared by
+    all requests or one per request [B][N]."""
+    B = cfg["B"] if B is None else B
+    V = cfg["V"]
+    dtype = DTYPE_CODE[cfg["dtype"]] if isinstance(cfg["dtype"], str) else cfg["dtype"]
+    parent = np.asarray(parent, np.int32)
+    if parent.ndim == 1:
+        parent = np.broadcast_to(parent, (B, parent.shape[0]))
+    parent = np.ascontiguousarray(parent)
+    N = parent.shape[1]
+    st = np.float32 if dtype == F32 else np.uint16
+    Lt = np.empty((B, N, V), dtype=st)
+    Ld = np.empty((B, N, V), dtype=st)
+    tok = np.zeros((B, N), dtype=np.int32)
+    ru = rng_for(seed, set_index, _TAG_TREE_UNIFORM)
+    u_acc = ru.random((B, N), dtype=np.float32)
+    u_res = ru.random((B, N), dtype=np.float32)
+    tcfg = cfg.get("temp", 1.0)
+    if isinstance(tcfg, tuple):
+        _, lo, hi = tcfg
+        temp = rng_for(seed, set_index, _TAG_TEMP).uniform(lo, hi, B).astype(np.float32)
+    else:
+        temp = np.full(B, tcfg, dtype=np.float32)
+    threads = threads or min(32, os.cpu_count() or 1)
+
+    def one(b):
+        _draw_tree_request(cfg, seed, set_index, b, B, parent[b], V, dtype, float(temp[b]),
+                           leaf_fill, Lt, Ld, tok)
+    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
+        if threads > 1 and B > 1:
+            with ThreadPoolExecutor(threads) as ex:
+                list(ex.map(one, range(B)))
+        else:
+            for b in range(B):
+                one(b)
+    return TreeInputs(Lt, Ld, parent, tok, u_acc, u_res, temp, dtype, B, N, V,
+                      cfg.get("name", "tree"))

@@ -11,7 +11,7 @@ import __graft_entry__
 from speculative_decoding_verification_09_gb300 import binding
 from speculative_decoding_verification_09_gb300._build_lib import LIB_PATH, ROOT
 
-HEADERS = [os.path.join(ROOT, "include", f) for f in ("specverify.h", "svkv.h")]
+HEADERS = [os.path.join(ROOT, "include", f) for f in ("specverify.h", "svkv.h", "svtree.h")]
 
 
 @pytest.fixture(scope="module")
@@ -164,6 +164,33 @@ def test_kv_and_window_validation(L):
                                    None) == binding.SV_ERR_INVALID_ARG
     assert L.sv_window_block_table(FAKE, FAKE, 2, 0, 64, 16, 3, FAKE, FAKE, None, None,
                                    None) == binding.SV_ERR_INVALID_ARG
+
+
+def test_tree_validation(L):
+    """sv_tree_verify rejects bad arguments before any CUDA call."""
+    def tree(**kw):
+        a = dict(dt=binding.SV_BF16, lt=FAKE, ld=FAKE, par=FAKE, tok=FAKE, ua=FAKE, ur=FAKE,
+                 temp=FAKE, B=3, N=5, V=100, ot=FAKE, on=FAKE)
+        a.update(kw)
+        return L.sv_tree_verify(a["dt"], a["lt"], a["ld"], a["par"], a["tok"], a["ua"], a["ur"],
+                                a["temp"], a["B"], a["N"], a["V"], a["ot"], a["on"], None, None,
+                                None)
+    assert tree(dt=2) == binding.SV_ERR_DTYPE
+    assert tree(N=0) == binding.SV_ERR_INVALID_ARG
+    assert tree(N=binding.SV_TREE_MAX_N + 1) == binding.SV_ERR_INVALID_ARG
+    assert tree(V=0) == binding.SV_ERR_INVALID_ARG and tree(B=-1) == binding.SV_ERR_INVALID_ARG
+    for k in ("lt", "par", "tok", "ur", "temp", "ot", "on", "ld", "ua"):
+        assert tree(**{k: None}) == binding.SV_ERR_INVALID_ARG, k
+    assert tree(lt=FAKE + 1) == binding.SV_ERR_INVALID_ARG        # bf16 needs 2-byte alignment
+    assert tree(dt=binding.SV_F32, ld=FAKE + 2) == binding.SV_ERR_INVALID_ARG
+    assert tree(B=0) == binding.SV_OK
+    if not __import__("torch").cuda.is_available():
+        # a single-node tree reads no draft row and no accept uniform: these
+        # arguments are valid and fail only at the device query
+        assert tree(N=1, ld=None, ua=None) == binding.SV_ERR_CUDA
+    assert L.sv_tree_set_cluster(9) == binding.SV_ERR_INVALID_ARG
+    assert L.sv_tree_set_cluster(-1) == binding.SV_ERR_INVALID_ARG
+    assert L.sv_tree_set_cluster(0) == binding.SV_OK
 
 
 def test_window_host_mirror_matches_oracle():
