@@ -39,7 +39,13 @@ namespace {
 constexpr int TW = 16;            // warps per CTA
 constexpr int TTHR = 32 * TW;
 constexpr int TMAXC = 8;          // CTAs per cluster (the portable limit)
-constexpr int TU = 4;             // 16-byte vectors in flight per lane and row
+constexpr int TU = 4;             // 16-byte vectors per lane and row in a batch
+constexpr int NS = 3;             // ring slots per warp
+constexpr int CHV = 32 * TU;      // 16-byte vectors of one row in a slot
+constexpr int CHB = CHV * 16;     // bytes of one row in a slot
+constexpr size_t RING_BYTES = size_t(TW) * NS * 2 * CHB;  // 192 KB of dynamic shared memory
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;  // one second
+constexpr int RB = 8;             // elements per lane loaded together in the final rescan
 constexpr double LOG2E_D = 1.4426950408889634;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -56,6 +62,80 @@ __device__ __forceinline__ float warp_max_nan(float v) {
   float r;
   asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
   return r;
+}
+__device__ __forceinline__ uint32_t bmax_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// Packed fp32 pairs (one 64-bit register pair) for the f32x2 instructions.
+__device__ __forceinline__ unsigned long long pk2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(unsigned long long* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(unsigned long long* bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+// One-dimensional bulk copy global -> this CTA's shared memory, completion
+// counted on `bar`; addresses and size multiples of 16 bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes,
+                                         unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
 }
 
 // Float pairs (h + l): sums with about 48 significant bits.
@@ -125,31 +205,33 @@ template <int DT>
 struct TE;
 template <>
 struct TE<SV_F32> {
-  static constexpr int ES = 4, VEC = 4;
+  static constexpr int ES = 4, VEC = 4, PAIRS = 2;
   __device__ static float at(const unsigned char* row, long long i) {
     return __ldg(reinterpret_cast<const float*>(row) + i);
   }
-  __device__ static void unpack(const uint4& v, float* f) {
-    f[0] = __uint_as_float(v.x);
-    f[1] = __uint_as_float(v.y);
-    f[2] = __uint_as_float(v.z);
-    f[3] = __uint_as_float(v.w);
+  __device__ static unsigned long long pair(const uint4& v, int q) {
+    return q == 0 ? pk2(__uint_as_float(v.x), __uint_as_float(v.y))
+                  : pk2(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
+  __device__ static float vmax(const uint4& v) {  // NaN if any element is NaN
+    return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                    fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
   }
 };
 template <>
 struct TE<SV_BF16> {
-  static constexpr int ES = 2, VEC = 8;
+  static constexpr int ES = 2, VEC = 8, PAIRS = 4;
   __device__ static float at(const unsigned char* row, long long i) {
     return __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short*>(row) + i))
                            << 16);
   }
-  __device__ static void unpack(const uint4& v, float* f) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      f[2 * q] = __uint_as_float(w[q] << 16);
-      f[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
-    }
+  __device__ static unsigned long long pair(const uint4& v, int q) {
+    const uint32_t w = q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+    return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+  __device__ static float vmax(const uint4& v) {
+    const uint32_t m = bmax_nan(bmax_nan(v.x, v.y), bmax_nan(v.z, v.w));
+    return fmax_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
   }
 };
 
@@ -180,6 +262,10 @@ struct TreeSmem {
   int32_t token[SV_TREE_MAX_N];
   int32_t path_tok[SV_TREE_MAX_N];
   int32_t path_node[SV_TREE_MAX_N];
+  float xl_t[SV_TREE_MAX_N];  // target / draft logit of each child's token at the current node
+  float xl_d[SV_TREE_MAX_N];
+  float ua[SV_TREE_MAX_N];    // accept uniform of each child of the current node
+  float ur;                   // residual uniform of the current node
   Part part[2][2][TW];    // [buffer][target, draft][warp], alternating per pass
   FF seg_incl[TW * TMAXC];  // running mass after each segment (index order)
   FF seg_tot[TW * TMAXC];
@@ -188,6 +274,8 @@ struct TreeSmem {
   FF St, Sd, Z;
   float K;
   int accept, seg_pick, degenerate;
+  int abort;                      // a ring wait gave up (the call's results are void)
+  unsigned long long bar[TW][NS];  // per-warp ring slots: bytes arrived
 };
 
 // Element range of segment g of a row split into nseg contiguous segments.
@@ -210,25 +298,96 @@ __device__ __forceinline__ void split16(const unsigned char* row, long long a, l
   nvec = (e - head_end) / E::VEC;
 }
 
+__device__ __forceinline__ void set_status(int32_t* status, int bits) {
+  if (status && bits) atomicOr(status, bits);
+}
+
+// A warp's ring: NS slots of CHB bytes of the target row and CHB of the
+// draft row, filled by bulk copies that lane 0 issues, each slot's arrival
+// counted on its mbarrier.  Fill f (counted over the kernel) goes to slot
+// f % NS and completes phase (f / NS) & 1 of its barrier.
+struct Ring {
+  unsigned char* base;
+  unsigned long long* bar;
+  unsigned seq;     // fills consumed
+  unsigned issued;  // fills issued
+};
+
+// Bounded wait for a ring slot: false after one second (recording
+// SV_ST_TIMEOUT and the CTA's abort flag) or once another warp gave up.
+__device__ bool ring_wait(unsigned long long* bar, unsigned parity, TreeSmem& sm,
+                          int32_t* status) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    if (mbar_try(bar, parity)) return true;
+    if (*(volatile int*)&sm.abort) return false;
+    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+      *(volatile int*)&sm.abort = 1;
+      set_status(status, SV_ST_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Stream nvec 16-byte vectors of a row body (and of the draft body when bd
+// is not null) through the warp's ring; consume(ct, cd, nv) sees each slot's
+// nv <= CHV vectors in order.
+template <class F>
+__device__ __forceinline__ void stream_body(Ring& R, TreeSmem& sm, int32_t* status,
+                                            const unsigned char* bt, const unsigned char* bd,
+                                            long long nvec, int lane, F&& consume) {
+  if (*(volatile int*)&sm.abort) return;
+  const long long nch = (nvec + CHV - 1) / CHV;
+  const unsigned base = R.seq;
+  auto issue = [&](long long k) {
+    const int sl = int((base + unsigned(k)) % NS);
+    const unsigned nb = unsigned(min((long long)CHV, nvec - k * CHV)) * 16u;
+    unsigned char* dst = R.base + size_t(sl) * 2 * CHB;
+    mbar_arrive_tx(&R.bar[sl], bd ? 2 * nb : nb);
+    bulk_g2s(dst, bt + k * CHB, nb, &R.bar[sl]);
+    if (bd) bulk_g2s(dst + CHB, bd + k * CHB, nb, &R.bar[sl]);
+  };
+  if (lane == 0)
+    for (long long k = 0; k < nch && k < NS; ++k) issue(k);
+  R.issued = base + unsigned(min(nch, (long long)NS));
+  for (long long k = 0; k < nch; ++k) {
+    const unsigned f = base + unsigned(k);
+    const int sl = int(f % NS);
+    if (!ring_wait(&R.bar[sl], (f / NS) & 1u, sm, status)) {
+      R.seq = f;  // fills f .. issued - 1 may still be in flight
+      return;
+    }
+    const uint4* ct = reinterpret_cast<const uint4*>(R.base + size_t(sl) * 2 * CHB);
+    consume(ct, ct + CHV, int(min((long long)CHV, nvec - k * CHV)));
+    __syncwarp();
+    if (k + NS < nch) {
+      if (lane == 0) issue(k + NS);
+      R.issued = base + unsigned(k + NS + 1);
+    }
+  }
+  R.seq = base + unsigned(nch);
+}
+
 // Statistics of one warp's segment: running max m and exp-sum s relative to
-// it per lane (the sum is rescaled when the max grows; each vector's terms are
-// summed in fp32 and added to a float pair), then the warp's (max, sum).  NaN
-// propagates through the max; an all -inf segment gives (-inf, 0).
+// it per lane, then the warp's (max, sum).  Each batch of TU vectors per lane
+// first moves the running max (rescaling the sum once), then adds its terms
+// 2^((x - m) kf), computed on packed pairs and summed in fp32, to a float
+// pair.  NaN propagates through the max; an all -inf segment gives (-inf, 0).
 struct MS {
   float m;
   FF s;
 };
-__device__ __forceinline__ void ms_add(MS& a, float vm, const float* f, int n, float kf) {
+__device__ __forceinline__ void ms_rescale(MS& a, float vm, float kf) {
   const float mn = fmax_nan(a.m, vm);
   if (mn != a.m) {
     a.s = ff_scale(a.s, ex2((a.m - mn) * kf));
     a.m = mn;
   }
-  if (a.m > -INFINITY) {
-    float v = 0.f;
-    for (int i = 0; i < n; ++i) v += ex2((f[i] - a.m) * kf);
-    a.s = ff_addf(a.s, v);
-  }
+}
+__device__ __forceinline__ void ms_add1(MS& a, float x, float kf) {
+  ms_rescale(a, x, kf);
+  if (a.m > -INFINITY) a.s = ff_addf(a.s, ex2((x - a.m) * kf));
 }
 __device__ __forceinline__ Part ms_warp(MS a, float kf) {
   const float M = warp_max_nan(a.m);
@@ -238,70 +397,92 @@ __device__ __forceinline__ Part ms_warp(MS a, float kf) {
   s = warp_sum(s);
   return Part{M, s.h, s.l, 0.f};
 }
+// sum over a vector of 2^((x - m) kf), the subtraction and product on pairs
+template <int DT>
+__device__ __forceinline__ unsigned long long vec_exp(const uint4& v, unsigned long long mm,
+                                                      unsigned long long kk,
+                                                      unsigned long long acc) {
+#pragma unroll
+  for (int q = 0; q < TE<DT>::PAIRS; ++q) {
+    float x, y;
+    upk2(mul2(sub2(TE<DT>::pair(v, q), mm), kk), x, y);
+    acc = add2(acc, pk2(ex2(x), ex2(y)));
+  }
+  return acc;
+}
+__device__ __forceinline__ float sum2(unsigned long long acc) {
+  float x, y;
+  upk2(acc, x, y);
+  return x + y;
+}
 
 template <int DT>
-__device__ void stats_pass(const TreeParams& P, const unsigned char* rt, const unsigned char* rd,
-                           bool with_draft, long long a, long long e, float kf, int lane,
-                           Part& pt, Part& pd) {
+__device__ void stats_pass(const TreeParams& P, TreeSmem& sm, Ring& R, const unsigned char* rt,
+                           const unsigned char* rd, bool with_draft, long long a, long long e,
+                           float kf, int lane, Part& pt, Part& pd) {
   using E = TE<DT>;
   MS st{-INFINITY, {0.f, 0.f}}, sd{-INFINITY, {0.f, 0.f}};
   const bool vec = !with_draft || P.same_align;
   long long hend = e, nvec = 0;
   if (vec) split16<DT>(rt, a, e, hend, nvec);
+  if (lane == 0 && nvec > CHV * NS) {  // the body past the ring's first fills, into L2
+    const long long off = (long long)CHV * NS * 16;
+    prefetch_l2(rt + hend * E::ES + off, unsigned(nvec * 16 - off));
+    if (with_draft) prefetch_l2(rd + hend * E::ES + off, unsigned(nvec * 16 - off));
+  }
   // scalar head (or the whole segment when the rows' alignments differ)
   for (long long i = a + lane; i < hend; i += 32) {
-    float f = E::at(rt, i);
-    ms_add(st, f, &f, 1, kf);
-    if (with_draft) {
-      float d = E::at(rd, i);
-      ms_add(sd, d, &d, 1, kf);
-    }
+    ms_add1(st, E::at(rt, i), kf);
+    if (with_draft) ms_add1(sd, E::at(rd, i), kf);
   }
-  const uint4* vt = reinterpret_cast<const uint4*>(rt + hend * E::ES);
-  const uint4* vd = reinterpret_cast<const uint4*>(rd + hend * E::ES);
-  for (long long j0 = 0; j0 < nvec; j0 += 32 * TU) {
-    uint4 xt[TU], xd[TU];
+  const unsigned long long kk = pk2(kf, kf);
+  stream_body(R, sm, P.status, rt + hend * E::ES, with_draft ? rd + hend * E::ES : nullptr, nvec,
+              lane, [&](const uint4* ct, const uint4* cd, int nv) {
+                uint4 xt[TU], xd[TU];
+                float bt = -INFINITY, bd = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < TU; ++u) {
-      const long long j = j0 + lane + 32 * u;
-      if (j < nvec) {
-        xt[u] = __ldg(vt + j);
-        if (with_draft) xd[u] = __ldg(vd + j);
-      }
-    }
+                for (int u = 0; u < TU; ++u) {
+                  if (lane + 32 * u < nv) {
+                    xt[u] = ct[lane + 32 * u];
+                    bt = fmax_nan(bt, E::vmax(xt[u]));
+                    if (with_draft) {
+                      xd[u] = cd[lane + 32 * u];
+                      bd = fmax_nan(bd, E::vmax(xd[u]));
+                    }
+                  }
+                }
+                ms_rescale(st, bt, kf);
+                if (st.m > -INFINITY) {
+                  const unsigned long long mm = pk2(st.m, st.m);
+                  unsigned long long acc = 0ull;
 #pragma unroll
-    for (int u = 0; u < TU; ++u) {
-      if (j0 + lane + 32 * u < nvec) {
-        float f[E::VEC];
-        E::unpack(xt[u], f);
-        float vm = f[0];
+                  for (int u = 0; u < TU; ++u)
+                    if (lane + 32 * u < nv) acc = vec_exp<DT>(xt[u], mm, kk, acc);
+                  st.s = ff_addf(st.s, sum2(acc));
+                }
+                if (with_draft) {
+                  ms_rescale(sd, bd, kf);
+                  if (sd.m > -INFINITY) {
+                    const unsigned long long mm = pk2(sd.m, sd.m);
+                    unsigned long long acc = 0ull;
 #pragma unroll
-        for (int i = 1; i < E::VEC; ++i) vm = fmax_nan(vm, f[i]);
-        ms_add(st, vm, f, E::VEC, kf);
-        if (with_draft) {
-          E::unpack(xd[u], f);
-          vm = f[0];
-#pragma unroll
-          for (int i = 1; i < E::VEC; ++i) vm = fmax_nan(vm, f[i]);
-          ms_add(sd, vm, f, E::VEC, kf);
-        }
-      }
-    }
-  }
+                    for (int u = 0; u < TU; ++u)
+                      if (lane + 32 * u < nv) acc = vec_exp<DT>(xd[u], mm, kk, acc);
+                    sd.s = ff_addf(sd.s, sum2(acc));
+                  }
+                }
+              });
   for (long long i = hend + nvec * E::VEC + lane; i < e; i += 32) {
-    float f = E::at(rt, i);
-    ms_add(st, f, &f, 1, kf);
-    if (with_draft) {
-      float d = E::at(rd, i);
-      ms_add(sd, d, &d, 1, kf);
-    }
+    ms_add1(st, E::at(rt, i), kf);
+    if (with_draft) ms_add1(sd, E::at(rd, i), kf);
   }
   pt = ms_warp(st, kf);
   pd = with_draft ? ms_warp(sd, kf) : Part{-INFINITY, 0.f, 0.f, 0.f};
 }
 
 // Residual weight of one element: max(0, e_t - K e_d) with e = 2^((l - m) kf),
-// or e_t alone when K == 0 (a draw from the target row).
+// or e_t alone when K == 0 (a draw from the target row).  The packed path
+// below performs the same operations, so both give the same values.
 __device__ __forceinline__ float weight(float lt, float ld, float mt, float md, float kf,
                                         float K) {
   const float et = ex2((lt - mt) * kf);
@@ -310,11 +491,11 @@ __device__ __forceinline__ float weight(float lt, float ld, float mt, float md, 
 }
 
 // Lane sum of the residual weights over [a, e) (lanes interleaved; each
-// vector's weights summed in fp32 and added to a float pair).
+// batch of vectors summed in fp32 on pairs and added to a float pair).
 template <int DT>
-__device__ FF mass_lane(const TreeParams& P, const unsigned char* rt, const unsigned char* rd,
-                        long long a, long long e, float mt, float md, float kf, float K,
-                        int lane) {
+__device__ FF mass_lane(const TreeParams& P, TreeSmem& sm, Ring& R, const unsigned char* rt,
+                        const unsigned char* rd, long long a, long long e, float mt, float md,
+                        float kf, float K, int lane) {
   using E = TE<DT>;
   const bool with_draft = K != 0.f;
   const bool vec = !with_draft || P.same_align;
@@ -323,43 +504,66 @@ __device__ FF mass_lane(const TreeParams& P, const unsigned char* rt, const unsi
   FF s{0.f, 0.f};
   for (long long i = a + lane; i < hend; i += 32)
     s = ff_addf(s, weight(E::at(rt, i), with_draft ? E::at(rd, i) : 0.f, mt, md, kf, K));
-  const uint4* vt = reinterpret_cast<const uint4*>(rt + hend * E::ES);
-  const uint4* vd = reinterpret_cast<const uint4*>(rd + hend * E::ES);
-  for (long long j0 = 0; j0 < nvec; j0 += 32 * TU) {
-    uint4 xt[TU], xd[TU];
+  const unsigned long long kk = pk2(kf, kf), mmt = pk2(mt, mt), mmd = pk2(md, md),
+                           nk = pk2(-K, -K);
+  stream_body(R, sm, P.status, rt + hend * E::ES, with_draft ? rd + hend * E::ES : nullptr, nvec,
+              lane, [&](const uint4* ct, const uint4* cd, int nv) {
+                unsigned long long acc = 0ull;
 #pragma unroll
-    for (int u = 0; u < TU; ++u) {
-      const long long j = j0 + lane + 32 * u;
-      if (j < nvec) {
-        xt[u] = __ldg(vt + j);
-        if (with_draft) xd[u] = __ldg(vd + j);
-      }
-    }
+                for (int u = 0; u < TU; ++u) {
+                  if (lane + 32 * u < nv) {
+                    const uint4 xt = ct[lane + 32 * u];
+                    if (!with_draft) {
+                      acc = vec_exp<DT>(xt, mmt, kk, acc);
+                    } else {
+                      const uint4 xd = cd[lane + 32 * u];
 #pragma unroll
-    for (int u = 0; u < TU; ++u) {
-      if (j0 + lane + 32 * u < nvec) {
-        float f[E::VEC], d[E::VEC];
-        E::unpack(xt[u], f);
-        if (with_draft) {
-          E::unpack(xd[u], d);
-        } else {
-#pragma unroll
-          for (int i = 0; i < E::VEC; ++i) d[i] = 0.f;
-        }
-        float v = 0.f;
-#pragma unroll
-        for (int i = 0; i < E::VEC; ++i) v += weight(f[i], d[i], mt, md, kf, K);
-        s = ff_addf(s, v);
-      }
-    }
-  }
+                      for (int q = 0; q < E::PAIRS; ++q) {
+                        float t0, t1, d0, d1;
+                        upk2(mul2(sub2(E::pair(xt, q), mmt), kk), t0, t1);
+                        upk2(mul2(sub2(E::pair(xd, q), mmd), kk), d0, d1);
+                        // e_t - K e_d on the pair (one rounding each, as fmaf)
+                        upk2(fma2(pk2(ex2(d0), ex2(d1)), nk, pk2(ex2(t0), ex2(t1))), t0, t1);
+                        acc = add2(acc, pk2(fmaxf(0.f, t0), fmaxf(0.f, t1)));
+                      }
+                    }
+                  }
+                }
+                s = ff_addf(s, sum2(acc));
+              });
   for (long long i = hend + nvec * E::VEC + lane; i < e; i += 32)
     s = ff_addf(s, weight(E::at(rt, i), with_draft ? E::at(rd, i) : 0.f, mt, md, kf, K));
   return s;
 }
 
-__device__ __forceinline__ void set_status(const TreeParams& P, int bits) {
-  if (P.status && bits) atomicOr(P.status, bits);
+// Combine of a mass pass (warp 0): the partials of all 16 c segments, read
+// from every CTA of the cluster in index order (lane l holds segments
+// 4 l .. 4 l + 3), into the segment totals, their running sums and the total.
+__device__ void combine_mass(cg::cluster_group& cluster, TreeSmem& sm, int buf, int nseg,
+                             int lane) {
+  FF t[4], run{0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int g = 4 * lane + j;
+    t[j] = FF{0.f, 0.f};
+    if (g < nseg) {
+      const Part* src = cluster.map_shared_rank(&sm.part[buf][0][0], g / TW);
+      const Part p = src[g % TW];
+      t[j] = FF{p.h, p.l};
+    }
+    run = ff_add(run, t[j]);
+  }
+  const FF incl = warp_scan(run, lane);
+  FF before = ff_shfl_up(incl, 1);
+  if (lane == 0) before = FF{0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    before = ff_add(before, t[j]);
+    sm.seg_tot[4 * lane + j] = t[j];
+    sm.seg_incl[4 * lane + j] = before;
+  }
+  const FF Z = ff_shfl(incl, 31);
+  if (lane == 0) sm.Z = Z;
 }
 
 // The walk of one request by one cluster.  Every CTA of the cluster runs the
@@ -369,6 +573,7 @@ template <int DT>
 __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
   using E = TE<DT>;
   __shared__ TreeSmem sm;
+  extern __shared__ __align__(128) unsigned char ring_mem[];
   cg::cluster_group cluster = cg::this_cluster();
   const int c = int(cluster.num_blocks());
   const int q = int(cluster.block_rank());
@@ -377,6 +582,11 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
   const int N = P.N;
   const long long V = P.V;
   const int nseg = TW * c;
+
+  if (lane == 0)
+    for (int sl = 0; sl < NS; ++sl) mbar_init(&sm.bar[warp][sl], 1);
+  if (tid == 0) sm.abort = 0;
+  Ring R{ring_mem + size_t(warp) * NS * 2 * CHB, sm.bar[warp], 0u, 0u};
 
   // tree structure and its validity (every node, before any row is read)
   int bad = 0;
@@ -400,24 +610,19 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
       }
       if (tid == 0) {
         P.out_n[b] = 0;
-        set_status(P, (bad ? SV_ST_BAD_TOKEN : 0) | (bad_temp ? SV_ST_BAD_TEMP : 0));
+        set_status(P.status, (bad ? SV_ST_BAD_TOKEN : 0) | (bad_temp ? SV_ST_BAD_TEMP : 0));
       }
     }
     return;  // no pass ran: no peer reads this CTA's shared memory
   }
   const float kf = float(LOG2E_D / double(T));
-  const double kd = double(kf);
   const size_t row_bytes = size_t(V) * E::ES;
 
   int n = 0, k = 0, buf = 0;
   bool invalid = false;
-  int drawn = -1;
-  int owner = -1;       // rank of the CTA that rescans the drawn segment
-  FF tau_seg{0.f, 0.f};  // u * Z less the mass before that segment
-  int gpick = 0;
-  float Kdraw = 0.f;
-  // scalar state of the walk, thread 0 only
-  double C = 0.0, S = 1.0;
+  float Kseg = 0.f;  // K of the residual whose segment totals are in sm.seg_*
+  // scalar state of the walk (thread 0): r = max(0, P_t - C P_d) / S
+  float C = 0.f, S = 1.f;
   int status_bits = 0;
 
   for (;;) {
@@ -426,13 +631,22 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
     const bool has_child = __syncthreads_or(hc) != 0;
     const unsigned char* rt = P.Lt + ((long long)b * N + n) * row_bytes;
     const unsigned char* rd = has_child ? P.Ld + ((long long)b * N + n) * row_bytes : nullptr;
+    // the children's logits at their tokens, for the accept tests
+    for (int i = n + 1 + tid; i < N; i += TTHR) {
+      if (sm.parent[i] == n) {
+        sm.xl_t[i] = E::at(rt, sm.token[i]);
+        sm.xl_d[i] = E::at(rd, sm.token[i]);
+        sm.ua[i] = P.u_acc[(long long)b * N + i];
+      }
+    }
+    if (tid == TTHR - 1) sm.ur = P.u_res[(long long)b * N + n];
 
     // pass 1: the rows' max and exp-sum
     {
       long long a, e;
       seg_range(V, q * TW + warp, nseg, a, e);
       Part pt, pd;
-      stats_pass<DT>(P, rt, rd, has_child, a, e, kf, lane, pt, pd);
+      stats_pass<DT>(P, sm, R, rt, rd, has_child, a, e, kf, lane, pt, pd);
       if (lane == 0) {
         sm.part[buf][0][warp] = pt;
         sm.part[buf][1][warp] = pd;
@@ -445,7 +659,7 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
         float M = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int g = lane + 32 * j;
+          const int g = 4 * lane + j;
           p[j] = Part{-INFINITY, 0.f, 0.f, 0.f};
           if (g < nseg) {
             const Part* src = cluster.map_shared_rank(&sm.part[buf][r][0], g / TW);
@@ -454,20 +668,36 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
           M = fmax_nan(M, p[j].m);
         }
         M = warp_max_nan(M);
-        FF s{0.f, 0.f};
-        if (M > -INFINITY && M < INFINITY) {
+        const bool fin = M > -INFINITY && M < INFINITY;
+        FF t[4], run{0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (p[j].m > -INFINITY) s = ff_add(s, ff_scale(FF{p[j].h, p[j].l}, ex2((p[j].m - M) * kf)));
+        for (int j = 0; j < 4; ++j) {
+          t[j] = FF{0.f, 0.f};
+          if (fin && p[j].m > -INFINITY) t[j] = ff_scale(FF{p[j].h, p[j].l}, ex2((p[j].m - M) * kf));
+          run = ff_add(run, t[j]);
         }
-        s = warp_sum(s);
+        if (r == 0 && !has_child && fin) {
+          // a leaf: its draw is from P_t, whose segment totals are these
+          const FF incl = warp_scan(run, lane);
+          FF before = ff_shfl_up(incl, 1);
+          if (lane == 0) before = FF{0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            before = ff_add(before, t[j]);
+            sm.seg_tot[4 * lane + j] = t[j];
+            sm.seg_incl[4 * lane + j] = before;
+          }
+          const FF Z = ff_shfl(incl, 31);
+          if (lane == 0) sm.Z = Z;
+        }
+        const FF tot = warp_sum(run);
         if (lane == 0) {
           if (r == 0) {
             sm.mt = M;
-            sm.St = s;
+            sm.St = tot;
           } else {
             sm.md = M;
-            sm.Sd = s;
+            sm.Sd = tot;
           }
         }
       }
@@ -484,24 +714,35 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
       break;
     }
     if (tid == 0) {
-      C = 0.0;
-      S = 1.0;
+      C = 0.f;
+      S = 1.f;
     }
-    bool mass_current = false;  // the last mass pass matches the current residual
+    bool seg_ready = !has_child;  // a leaf's segment totals came with pass 1
+    Kseg = 0.f;
     int next = -1;
     for (int cc = n + 1; cc < N; ++cc) {
       if (sm.parent[cc] != n) continue;
       if (tid == 0) {
-        const int x = sm.token[cc];
-        const double pt = exp2((double(E::at(rt, x)) - double(mt)) * kd) / ff_d(St);
-        const double pq = exp2((double(E::at(rd, x)) - double(md)) * kd) / ff_d(Sd);
-        double ratio = 1.0;
-        if (pq > 0.0) ratio = fmin(1.0, fmax(0.0, pt - C * pq) / (S * pq));
-        const int acc = double(P.u_acc[(long long)b * N + cc]) <= ratio;
+        // r(x) / P_d(x) with P = 2^((l - m) kf) / S_row, the same terms the
+        // passes summed; where a term underflows fp32 it is taken in fp64
+        const float et = ex2((sm.xl_t[cc] - mt) * kf);
+        const float ed = ex2((sm.xl_d[cc] - md) * kf);
+        float ratio = 1.f;
+        if (et > 0.f && ed > 0.f) {
+          const float pt = et / St.h, pq = ed / Sd.h;
+          ratio = fminf(1.f, fmaxf(0.f, pt - C * pq) / (S * pq));
+        } else {
+          const double kd = double(kf);
+          const double pt = exp2((double(sm.xl_t[cc]) - double(mt)) * kd) / ff_d(St);
+          const double pq = exp2((double(sm.xl_d[cc]) - double(md)) * kd) / ff_d(Sd);
+          if (pq > 0.0)
+            ratio = float(fmin(1.0, fmax(0.0, pt - double(C) * pq) / (double(S) * pq)));
+        }
+        const int acc = sm.ua[cc] <= ratio;
         sm.accept = acc;
         if (!acc) {
           C += S;
-          sm.K = float(C * ff_d(St) / ff_d(Sd));
+          sm.K = C * (St.h / Sd.h);
         }
       }
       __syncthreads();
@@ -514,54 +755,27 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
       {
         long long a, e;
         seg_range(V, q * TW + warp, nseg, a, e);
-        const FF s = warp_sum(mass_lane<DT>(P, rt, rd, a, e, mt, md, kf, K, lane));
+        const FF s = warp_sum(mass_lane<DT>(P, sm, R, rt, rd, a, e, mt, md, kf, K, lane));
         if (lane == 0) sm.part[buf][0][warp] = Part{0.f, s.h, s.l, 0.f};
       }
       cluster.sync();
-      if (warp == 0) {
-        // segment totals in index order: lane holds segments 4 lane .. 4 lane + 3
-        FF t[4], run{0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int g = 4 * lane + j;
-          t[j] = FF{0.f, 0.f};
-          if (g < nseg) {
-            const Part* src = cluster.map_shared_rank(&sm.part[buf][0][0], g / TW);
-            const Part p = src[g % TW];
-            t[j] = FF{p.h, p.l};
-          }
-          run = ff_add(run, t[j]);
-        }
-        const FF incl = warp_scan(run, lane);
-        FF before = ff_shfl_up(incl, 1);
-        if (lane == 0) before = FF{0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int g = 4 * lane + j;
-          before = ff_add(before, t[j]);
-          if (g < TW * TMAXC) {
-            sm.seg_tot[g] = t[j];
-            sm.seg_incl[g] = before;
-          }
-        }
-        const FF Z = ff_shfl(incl, 31);
-        if (lane == 0) sm.Z = Z;
-      }
+      if (warp == 0) combine_mass(cluster, sm, buf, nseg, lane);
       buf ^= 1;
       __syncthreads();
       if (tid == 0) {
-        const double Snew = ff_d(sm.Z) / ff_d(St);
-        sm.degenerate = !(Snew > 0.0);
-        if (Snew > 0.0) {
+        const float Snew = (sm.Z.h + sm.Z.l) / St.h;
+        sm.degenerate = !(Snew > 0.f);
+        if (Snew > 0.f) {
           S = Snew;
         } else {  // the residual vanished: continue from P_t[n]
-          C = 0.0;
-          S = 1.0;
+          C = 0.f;
+          S = 1.f;
           status_bits |= SV_ST_DEGENERATE;
         }
       }
       __syncthreads();
-      mass_current = !sm.degenerate;
+      seg_ready = !sm.degenerate;
+      Kseg = K;
     }
     if (next >= 0) {
       if (tid == 0) {
@@ -573,48 +787,21 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
       continue;
     }
     // the draw from the current residual (or from P_t[n])
-    Kdraw = mass_current ? sm.K : 0.f;
-    if (!mass_current) {
+    if (!seg_ready) {
+      Kseg = 0.f;
       long long a, e;
       seg_range(V, q * TW + warp, nseg, a, e);
-      const FF s = warp_sum(mass_lane<DT>(P, rt, rd, a, e, mt, md, kf, 0.f, lane));
+      const FF s = warp_sum(mass_lane<DT>(P, sm, R, rt, rd, a, e, mt, md, kf, 0.f, lane));
       if (lane == 0) sm.part[buf][0][warp] = Part{0.f, s.h, s.l, 0.f};
       cluster.sync();
-      if (warp == 0) {
-        FF t[4], run{0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int g = 4 * lane + j;
-          t[j] = FF{0.f, 0.f};
-          if (g < nseg) {
-            const Part* src = cluster.map_shared_rank(&sm.part[buf][0][0], g / TW);
-            const Part p = src[g % TW];
-            t[j] = FF{p.h, p.l};
-          }
-          run = ff_add(run, t[j]);
-        }
-        const FF incl = warp_scan(run, lane);
-        FF before = ff_shfl_up(incl, 1);
-        if (lane == 0) before = FF{0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int g = 4 * lane + j;
-          before = ff_add(before, t[j]);
-          if (g < TW * TMAXC) {
-            sm.seg_tot[g] = t[j];
-            sm.seg_incl[g] = before;
-          }
-        }
-        const FF Z = ff_shfl(incl, 31);
-        if (lane == 0) sm.Z = Z;
-      }
+      if (warp == 0) combine_mass(cluster, sm, buf, nseg, lane);
       buf ^= 1;
       __syncthreads();
     }
     // the segment holding tau = u * Z: the first with positive mass whose
     // running total exceeds tau (else the last with positive mass)
     if (warp == 0) {
-      const float u = P.u_res[(long long)b * N + n];
+      const float u = sm.ur;
       const FF Z = sm.Z;
       const float p = u * Z.h;
       FF tau;
@@ -643,10 +830,17 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
       }
     }
     __syncthreads();
-    gpick = sm.seg_pick;
-    tau_seg = sm.piece[0];
-    owner = gpick / TW;
     break;
+  }
+  const int gpick = invalid ? 0 : sm.seg_pick;
+  const FF tau_seg = sm.piece[0];
+  // after a ring wait gave up, wait (bounded) for this warp's copies still in
+  // flight before the shared memory they target is released
+  if (*(volatile int*)&sm.abort) {
+    const unsigned long long t0 = globaltimer();
+    for (unsigned f = R.seq; f < R.issued; ++f)
+      while (!mbar_try(&R.bar[f % NS], (f / NS) & 1u) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+      }
   }
   // no CTA leaves while a peer may still read its partials
   cluster.sync();
@@ -659,33 +853,45 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
       }
       if (tid == 0) {
         P.out_n[b] = 0;
-        set_status(P, SV_ST_NONFINITE | status_bits);
+        set_status(P.status, SV_ST_NONFINITE | status_bits);
       }
     }
     return;
   }
-  if (q != owner) return;
+  if (q != gpick / TW) return;
 
   // rescan the picked segment: 16 pieces, one per warp, then one warp scans
   // the piece holding the remaining tau element by element
   const unsigned char* rt = P.Lt + ((long long)b * N + n) * row_bytes;
-  const unsigned char* rd = P.Ld ? P.Ld + ((long long)b * N + n) * row_bytes : nullptr;
-  const float mt = sm.mt, md = Kdraw != 0.f ? sm.md : 0.f;
+  const unsigned char* rd = Kseg != 0.f ? P.Ld + ((long long)b * N + n) * row_bytes : nullptr;
+  const float mt = sm.mt, md = Kseg != 0.f ? sm.md : 0.f;
   long long sa, se;
   seg_range(V, gpick, nseg, sa, se);
   {
     long long a, e;
     seg_range(se - sa, warp, TW, a, e);
     FF s{0.f, 0.f};
-    for (long long i = sa + a + lane; i < sa + e; i += 32)
-      s = ff_addf(s, weight(E::at(rt, i), Kdraw != 0.f ? E::at(rd, i) : 0.f, mt, md, kf, Kdraw));
+    for (long long i0 = sa + a; i0 < sa + e; i0 += 32 * RB) {
+      float lt[RB], ld[RB];
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {  // all of the batch's loads first
+        const long long i = i0 + 32 * r + lane;
+        lt[r] = i < sa + e ? E::at(rt, i) : -INFINITY;
+        ld[r] = (rd && i < sa + e) ? E::at(rd, i) : 0.f;
+      }
+      float v = 0.f;
+#pragma unroll
+      for (int r = 0; r < RB; ++r)
+        if (i0 + 32 * r + lane < sa + e) v += weight(lt[r], ld[r], mt, md, kf, Kseg);
+      s = ff_addf(s, v);
+    }
     const FF t = warp_sum(s);
-    __syncthreads();  // sm.piece[0] was read by every thread above
-    if (lane == 0) sm.piece[warp] = t;
+    if (lane == 0) sm.piece[warp] = t;  // every thread read sm.piece[0] before the cluster barrier
   }
   __syncthreads();
+  int drawn = 0;
   if (warp == 0) {
-    FF t = lane < TW ? sm.piece[lane] : FF{0.f, 0.f};
+    const FF t = lane < TW ? sm.piece[lane] : FF{0.f, 0.f};
     const FF incl = warp_scan(t, lane);
     const bool pos = t.h > 0.f;
     const unsigned hits = __ballot_sync(0xffffffffu, pos && ff_gt(incl, tau_seg));
@@ -699,33 +905,39 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
     seg_range(se - sa, j, TW, a, e);
     FF run{0.f, 0.f};
     long long found = -1, lastpos = -1;
-    for (long long i0 = sa + a; i0 < sa + e && found < 0; i0 += 32) {
-      const long long i = i0 + lane;
-      const float w = i < sa + e ? weight(E::at(rt, i), Kdraw != 0.f ? E::at(rd, i) : 0.f, mt, md,
-                                          kf, Kdraw)
-                                 : 0.f;
-      const FF inc = ff_add(run, warp_scan(FF{w, 0.f}, lane));
-      const unsigned h = __ballot_sync(0xffffffffu, w > 0.f && ff_gt(inc, tau));
-      const unsigned pv = __ballot_sync(0xffffffffu, w > 0.f);
-      if (h) found = i0 + __ffs(h) - 1;
-      if (pv) lastpos = i0 + 31 - __clz(pv);
-      run = ff_shfl(inc, 31);
+    for (long long i0 = sa + a; i0 < sa + e && found < 0; i0 += 32 * RB) {
+      float w[RB];
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {  // the batch's loads first, then its tiles in order
+        const long long i = i0 + 32 * r + lane;
+        w[r] = i < sa + e ? weight(E::at(rt, i), rd ? E::at(rd, i) : 0.f, mt, md, kf, Kseg) : 0.f;
+      }
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        if (found < 0) {
+          const long long t0 = i0 + 32 * r;
+          const FF inc = ff_add(run, warp_scan(FF{w[r], 0.f}, lane));
+          const unsigned h = __ballot_sync(0xffffffffu, w[r] > 0.f && ff_gt(inc, tau));
+          const unsigned pv = __ballot_sync(0xffffffffu, w[r] > 0.f);
+          if (h) found = t0 + __ffs(h) - 1;
+          if (pv) lastpos = t0 + 31 - __clz(pv);
+          run = ff_shfl(inc, 31);
+        }
+      }
     }
     drawn = int(found >= 0 ? found : (lastpos >= 0 ? lastpos : sa));
+    if (lane == 0) sm.seg_pick = drawn;
   }
-  // outputs: the accepted path, the drawn token, -1 after
-  if (warp == 0) drawn = __shfl_sync(0xffffffffu, drawn, 0);
-  __syncthreads();
-  if (warp == 0 && lane == 0) sm.seg_pick = drawn;
   __syncthreads();
   drawn = sm.seg_pick;
+  // outputs: the accepted path, the drawn token, -1 after
   for (int i = tid; i < N; i += TTHR) {
     otok[i] = i < k ? sm.path_tok[i] : (i == k ? drawn : -1);
     if (onode) onode[i] = i < k ? sm.path_node[i] : -1;
   }
   if (tid == 0) {
     P.out_n[b] = k;
-    set_status(P, status_bits);
+    set_status(P.status, status_bits);
   }
 }
 
@@ -737,9 +949,16 @@ int sms_of_device(int& sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SV_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_tree_mu);
-  if (!g_sms[dev] &&
-      cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return SV_ERR_CUDA;
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(sv_tree_walk<SV_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(RING_BYTES)) != cudaSuccess ||
+        cudaFuncSetAttribute(sv_tree_walk<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(RING_BYTES)) != cudaSuccess)
+      return SV_ERR_CUDA;
+    g_sms[dev] = n;
+  }
   sms = g_sms[dev];
   return SV_OK;
 }
@@ -797,7 +1016,7 @@ extern "C" int sv_tree_verify(int dtype, const void* target_logits, const void* 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(B) * unsigned(c));
   cfg.blockDim = dim3(TTHR);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = RING_BYTES;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
