@@ -93,8 +93,9 @@ constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;  // one second
 // ------------------------------------------------------------ workspace
 
 struct Ctrl {                 // 64 bytes at the start of the workspace
-  // both 0 between calls (the ready state); state is 1 while a call runs
-  unsigned long long state, reserved;
+  // both 0 between calls (the ready state); state is 1 while a call runs,
+  // claims counts the reduce's claims of pool units (reset by the call's last kernel)
+  unsigned long long state, claims;
   unsigned long long pad[6];  // pad[0]: the residual kernel's chunk-claim counter
 };
 struct Partial {              // per (request, position, chunk, consumer warp)
@@ -288,6 +289,14 @@ __device__ __forceinline__ void wait_previous_kernel() {
 
 __device__ __forceinline__ void set_status(const Params& P, int bits) {
   if (bits && P.status) atomicOr(P.status, bits);
+}
+
+// The control block's ready state, written by the last kernel of a call
+// (the reduce of this call has completed; the next call's reduce reads it
+// only after this kernel has completed).
+__device__ __forceinline__ void ready_for_next_call(const Params& P) {
+  P.ctrl->state = 0ull;
+  P.ctrl->claims = 0ull;
 }
 
 // Bounded wait for phase `parity` of an mbarrier (the reduce kernel's waits are
@@ -944,43 +953,87 @@ __device__ void end_markers(const Params& P, SmemCtl<G>& C, long long seq) {
   }
 }
 
-// First task of CTA x of nb, splitting the reduce's tasks so that every CTA
-// streams about the same bytes: a chunk of a row that also streams its draft
-// row weighs 2, a target-only chunk 1.  A request's tasks weigh
-// w_req = nch1 * (R + gs): its first gs rows 2 * nch1 each, the rest nch1.
-// The CTA starts at the smallest task whose weight before it reaches
-// ceil(x / nb) of the total, found in closed form.
-__device__ __forceinline__ long long tasks_split(const Params& P, long long x, long long nb) {
+// Task weights: a chunk of a row that also streams its draft row weighs 2,
+// a target-only chunk 1, so weight counts streamed bytes.  A request's tasks
+// weigh w_req = nch1 * (R + gs): its first gs rows 2 * nch1 each, the rest
+// nch1.  The smallest task whose weight before it reaches w, in closed form.
+__device__ __forceinline__ long long task_at_weight(const Params& P, long long w) {
   const long long per_req = (long long)P.R * P.nch1;
   const long long w_req = (long long)P.nch1 * (P.R + P.gs);
   const long long w2 = 2LL * P.gs * P.nch1;  // weight of a request's two-row chunks
-  const long long target = (w_req * P.B * x + nb - 1) / nb;
-  const long long b = target / w_req, rem = target - b * w_req;
+  const long long b = w / w_req, rem = w - b * w_req;
   const long long t_in = rem <= w2 ? (rem + 1) / 2 : P.gs * (long long)P.nch1 + (rem - w2);
   return b * per_req + t_in;
 }
 
-// Producer (one lane): this CTA's contiguous range of chunks, in order, into
-// the slot ring.  Chunk t is chunk t % nch1 of row t / nch1 (row = b * R + i).
-// A slot holds a target chunk and the same span of the draft row; where no
-// draft rows are streamed (greedy verification, given draft normalisers,
-// draft sampling) it holds two consecutive target chunks instead (a pair),
-// so every slot still carries up to two half-slots of logits.
+// Work split of the reduce.  The first (POOL_DIV - 1) / POOL_DIV of the
+// weight is split statically: CTA x of nb streams the contiguous tasks from
+// task_at_weight(ceil(Ws x / nb)) on, so every CTA starts with the same
+// bytes.  The rest, tasks [ts, tasks) (the last requests' rows), is a pool
+// of units of `unit` consecutive tasks that the CTAs claim one at a time
+// from a counter in the control block once their static range is nearly
+// done; CTAs whose copies are served faster take more units, so the grid
+// ends together (a static split alone left the last CTA 2-18 us behind the
+// median on the sampling workloads).
+constexpr int POOL_DIV = 8;
+struct Split {
+  long long t0, t1;    // this CTA's static range
+  long long ts;        // first pool task
+  long long unit, nunits;
+};
+__device__ __forceinline__ Split reduce_split(const Params& P, long long x, long long nb) {
+  const long long W = (long long)P.nch1 * (P.R + P.gs) * P.B;
+  const long long Ws = W - W / POOL_DIV;
+  Split sp;
+  sp.t0 = task_at_weight(P, (Ws * x + nb - 1) / nb);
+  sp.t1 = task_at_weight(P, (Ws * (x + 1) + nb - 1) / nb);
+  sp.ts = task_at_weight(P, Ws);
+  const long long pool = P.tasks - sp.ts;
+  sp.unit = max(1LL, (pool + 4 * nb - 1) / (4 * nb));  // about four units per CTA
+  sp.nunits = (pool + sp.unit - 1) / sp.unit;
+  return sp;
+}
+
+// Producer (one lane): this CTA's static range of chunks, then the pool
+// units it claims, each in order, into the slot ring.  Chunk t is chunk
+// t % nch1 of row t / nch1 (row = b * R + i).  A slot holds a target chunk
+// and the same span of the draft row; where no draft rows are streamed
+// (greedy verification, given draft normalisers, draft sampling) it holds
+// two consecutive target chunks of one range instead (a pair), so every
+// slot still carries up to two half-slots of logits.
 template <int DT, bool GREEDY, bool PAIRS>
 __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* slots) {
   using E = Elem<DT>;
   using G = GeoReduce;
   constexpr int NS = G::NS, SLOT = G::SLOT, HALF = G::HALF;
-  const long long nb = gridDim.x;
-  const long long t0 = tasks_split(P, blockIdx.x, nb), t1 = tasks_split(P, blockIdx.x + 1, nb);
-  const long long row0 = t0 / P.nch1;
-  int c = int(t0 - row0 * P.nch1);
-  int b = int(row0 / P.R), i = int(row0 - (long long)b * P.R);
-  float T = GREEDY ? 1.f : __ldg(P.temp + b);
-  float T_next = (!GREEDY && b + 1 < P.B) ? __ldg(P.temp + b + 1) : 1.f;
-  const unsigned char* trow = P.Lt + (size_t(b) * P.R + i) * size_t(P.V) * E::ES;
-  const unsigned char* drow =
-      (!GREEDY && i < P.gs) ? P.Ld + (size_t(b) * P.gamma + i) * size_t(P.V) * E::ES : nullptr;
+  const Split sp = reduce_split(P, blockIdx.x, gridDim.x);
+  long long t = sp.t0, tend = sp.t1;  // the range being streamed
+  // a claim is issued while the current range still has NS tasks to go, so
+  // its round trip is hidden behind the slots in flight
+  long long claimed = 0;
+  bool pending = false;
+  auto claim = [&]() {
+    if (sp.nunits > 0) {
+      claimed = (long long)atomicAdd(&P.ctrl->claims, 1ull);
+      pending = true;
+    }
+  };
+  int c = 0, b = 0, i = 0;
+  float T = 1.f, T_next = 1.f;
+  const unsigned char* trow = nullptr;
+  const unsigned char* drow = nullptr;
+  auto seek = [&](long long tt) {  // to chunk tt
+    const long long row = tt / P.nch1;
+    c = int(tt - row * P.nch1);
+    b = int(row / P.R);
+    i = int(row - (long long)b * P.R);
+    T = (!GREEDY && b < P.B) ? __ldg(P.temp + b) : 1.f;  // b == B: an empty range at the end
+    T_next = (!GREEDY && b + 1 < P.B) ? __ldg(P.temp + b + 1) : 1.f;
+    trow = P.Lt + (size_t(b) * P.R + i) * size_t(P.V) * E::ES;
+    drow = (!GREEDY && i < P.gs) ? P.Ld + (size_t(b) * P.gamma + i) * size_t(P.V) * E::ES
+                                 : nullptr;
+  };
+  seek(t);
   auto advance = [&]() {  // to the next chunk
     if (++c == P.nch1) {
       c = 0;
@@ -995,10 +1048,22 @@ __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* 
                                    : nullptr;
     }
   };
-  for (long long t = t0, seq = 0; t <= t1; ++seq) {
+  for (long long seq = 0;; ++seq) {
     const int s = int(seq % NS);
     const unsigned use = unsigned(seq / NS);
-    if (t == t1 || C.abort) {
+    if (!pending && tend - t <= NS) claim();
+    if (t == tend) {  // on to the claimed unit, if the pool has one left
+      if (pending && claimed < sp.nunits) {
+        t = sp.ts + claimed * sp.unit;
+        tend = min(t + sp.unit, P.tasks);
+        pending = false;
+        seek(t);
+      } else {
+        end_markers(P, C, seq);
+        return;
+      }
+    }
+    if (C.abort) {
       end_markers(P, C, seq);
       return;
     }
@@ -1018,7 +1083,7 @@ __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* 
     const unsigned char* dseg = drow ? drow + size_t(d.e0) * E::ES : nullptr;
     split<DT>(tseg, d.n, d.head_t, d.nb_t);
     ++t;
-    if (PAIRS && t < t1) {  // the next target chunk into the second half
+    if (PAIRS && t < tend) {  // the next target chunk of the range into the second half
       advance();
       const int e0b = c * P.ch1;
       d.pair = 1;
@@ -1141,9 +1206,8 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
   if (threadIdx.x == 0) {
     // the workspace is in its ready state between calls; mark this call
     if (blockIdx.x == 0) {
-      if (P.ctrl->state != 0ull || P.ctrl->reserved != 0ull) set_status(P, SV_ST_WORKSPACE);
+      if (P.ctrl->state != 0ull || P.ctrl->claims != 0ull) set_status(P, SV_ST_WORKSPACE);
       P.ctrl->state = 1ull;
-      P.ctrl->reserved = 0ull;
       P.ctrl->pad[0] = 0ull;  // the residual kernel's chunk claims
     }
   }
@@ -1454,7 +1518,7 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
     if (threadIdx.x == 0) write_record(P, b, mode_k.x, mode_k.y, rows, cand);
   }
   // greedy verification ends here: the workspace is ready for the next call
-  if (last && b == 0 && threadIdx.x == 0) P.ctrl->state = 0ull;
+  if (last && b == 0 && threadIdx.x == 0) ready_for_next_call(P);
   // only now: the residual kernel's CTAs need whole SMs, which this grid's
   // CTAs still waiting to be placed must not lose to them
   allow_next_kernel();
@@ -1777,7 +1841,7 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
     }
   }
   if (r.mode == MODE_INVALID) {
-    if (last_cta && threadIdx.x == 0) P.ctrl->state = 0ull;
+    if (last_cta && threadIdx.x == 0) ready_for_next_call(P);
     return;
   }
   const float u = __shfl_sync(0xffffffffu, u_lane, r.k & 31) ;
@@ -1984,7 +2048,7 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
     }
   }
   // the last kernel of a sampling call: the workspace is ready for the next one
-  if (last_cta && threadIdx.x == 0) P.ctrl->state = 0ull;
+  if (last_cta && threadIdx.x == 0) ready_for_next_call(P);
 }
 
 // ---------------------------------------------------------- draft sampling
@@ -2098,7 +2162,7 @@ __global__ void __launch_bounds__(32 * SAMPLE_WARPS) sv_sample(const Params P) {
       P.out_stats[2 * o] = NAN;
       P.out_stats[2 * o + 1] = NAN;
       set_status(P, t_ok ? SV_ST_NONFINITE : SV_ST_BAD_TEMP);
-      if (r == 0) P.ctrl->state = 0ull;
+      if (r == 0) ready_for_next_call(P);
     }
     return;
   }
@@ -2186,7 +2250,7 @@ __global__ void __launch_bounds__(32 * SAMPLE_WARPS) sv_sample(const Params P) {
   if (tid == 0) {
     P.out_stats[2 * o] = m;
     P.out_stats[2 * o + 1] = float(Sd);
-    if (r == 0) P.ctrl->state = 0ull;
+    if (r == 0) ready_for_next_call(P);
   }
 }
 

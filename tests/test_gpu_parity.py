@@ -200,13 +200,13 @@ def test_repeated_calls_reuse_workspace_and_streams():
     assert np.array_equal(again["tokens"], first["tokens"]) and again["status"] == 0
 
 
-# Workspace layout facts used to poison it: the control block starts at byte 0
-# (task counter, u64); per-request words start at byte 256, 16 bytes each
-# (u32 decision flag, padding), followed by records and epoch-tagged partials.
+# Workspace layout facts used to poison it: the control block takes bytes
+# 0..63 (the call-state word at byte 0, the reduce's pool-claim counter at
+# byte 8, both 0 between calls); the partials start at byte 256.
 def test_garbage_request_words_are_harmless():
-    """Decision flags and published values are tagged with the launch epoch, so
-    leftover or garbage per-request words (another shape's records, a stale
-    flag) cannot change the result."""
+    """Every workspace region past the control block is written before it is
+    read within a call, so leftover or garbage words there (another shape's
+    partials or records) cannot change the result."""
     cfg = synth.custom_config(8, 3, 6000, "bf16", "normal")
     inp = synth.make_inputs(cfg, seed=12)
     d = to_dev(inp)
@@ -226,6 +226,10 @@ def test_poisoned_task_counter_is_detected_and_repaired():
     ws = binding.make_workspace(inp.B, inp.gamma, inp.V, DEV)
     ref = oracle_sampling(inp)
     ws[0:8].view(torch.int64).fill_(1 << 40)  # the control block is not in its ready state
+    bad = run_sampling(inp, d, ws)
+    assert bad["status"] & binding.SV_ST_WORKSPACE
+    compare_sampling(inp, run_sampling(inp, d, ws), ref)
+    ws[8:16].view(torch.int64).fill_(5)  # a stale pool-claim count
     bad = run_sampling(inp, d, ws)
     assert bad["status"] & binding.SV_ST_WORKSPACE
     compare_sampling(inp, run_sampling(inp, d, ws), ref)
