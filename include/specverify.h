@@ -217,10 +217,24 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
 int sv_set_tuning(int chunk_elems);
 
 /*
+ * Process-wide choice of the kernels that follow the reduce in a sampling
+ * call (spec_verify, spec_verify_diag, spec_verify_cached, spec_verify_noalloc),
+ * for tests and benchmarking: 0 (the default) picks the fused tail when the
+ * batch leaves at least two SMs per request (B * 2 <= SMs) and the
+ * decide / residual / draw kernels otherwise; 1 forces the three kernels;
+ * 2 forces the fused tail (one kernel, one cluster of up to 8 CTAs per
+ * request).  Both compute the same decision and draw the token by the same
+ * rule.  Not thread-safe, like sv_set_tuning().  Returns SV_OK, or
+ * SV_ERR_INVALID_ARG for a mode outside [0, 2].
+ */
+int sv_set_tail(int mode);
+
+/*
  * Profiling aid: the next calls record the caller's CUDA events (cudaEvent_t
  * handles, created on the device the calls run on) on their stream: events[0]
  * before the first kernel and events[j] after the j-th (sampling runs four
- * kernels: reduce, decide, residual, draw; greedy runs two), for j < n.
+ * kernels: reduce, decide, residual, draw, or two with the fused tail: reduce
+ * and the fused kernel; greedy runs two), for j < n.
  * n = 0 turns it off.  n outside [0, 5] or a NULL handle: SV_ERR_INVALID_ARG.
  * Not thread-safe, like sv_set_tuning().
  */

@@ -24,7 +24,8 @@ SV_MAX_GAMMA = 32
 EXPORTED = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_verify_diag",
             "spec_verify_greedy", "spec_verify_noalloc", "spec_verify_cached",
             "sv_draft_workspace_bytes", "sv_draft_sample", "sv_set_tuning",
-            "sv_set_stage_events", "sv_test_withhold_slot", "sv_error_string", "sv_version",
+            "sv_set_stage_events", "sv_set_tail", "sv_test_withhold_slot", "sv_error_string",
+            "sv_version",
             "sv_kv_commit", "sv_kv_valid_slots", "sv_window_cols", "sv_window_block_table",
             "sv_window_seq_lens_host", "sv_tree_verify", "sv_tree_set_cluster")
 SV_TREE_MAX_N = 256
@@ -64,13 +65,15 @@ def lib() -> ctypes.CDLL:
         L.sv_tree_verify.argtypes = [I, P, P, P, P, P, P, P, I, I, I, P, P, P, P, P]
         L.sv_tree_set_cluster.argtypes = [I]
         L.sv_set_tuning.argtypes = [I]
+        L.sv_set_tail.argtypes = [I]
         L.sv_set_stage_events.argtypes = [P, I]
         L.sv_test_withhold_slot.argtypes = [I]
         L.sv_error_string.argtypes = [I]
         L.sv_error_string.restype = ctypes.c_char_p
         for name in ("sv_workspace_init", "spec_verify", "spec_verify_diag",
                      "spec_verify_greedy", "spec_verify_noalloc", "spec_verify_cached",
-                     "sv_draft_sample", "sv_set_tuning", "sv_set_stage_events", "sv_version",
+                     "sv_draft_sample", "sv_set_tuning", "sv_set_stage_events", "sv_set_tail",
+                     "sv_version",
                      "sv_test_withhold_slot",
                      "sv_kv_commit", "sv_kv_valid_slots", "sv_window_cols",
                      "sv_window_block_table", "sv_window_seq_lens_host", "sv_tree_verify",
@@ -136,6 +139,12 @@ def sv_test_withhold_slot(enable: bool) -> None:
     """Failure-handling test aid: the next calls' streaming kernel leaves one
     slot unfilled, so its bounded wait runs out (SV_ST_TIMEOUT)."""
     _check(lib().sv_test_withhold_slot(1 if enable else 0))
+
+
+def sv_set_tail(mode: int = 0) -> None:
+    """Kernels after the reduce in sampling calls: 0 automatic, 1 the
+    decide / residual / draw kernels, 2 the fused tail."""
+    _check(lib().sv_set_tail(mode))
 
 
 def sv_set_stage_events(events) -> None:

@@ -32,6 +32,7 @@
 // Greedy verification runs reduce (chunk argmax) and decide only; draft
 // sampling runs reduce (contiguous warp shares) and sample (one CTA per draft
 // row: the crossing partial's span, scanned in index order).
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <limits.h>
 #include <math.h>
@@ -1386,8 +1387,8 @@ __device__ int2 decide_sample(const Params& P, int b, const RowStat* rows, float
 
 // The decision record of request b (one thread): the draw's row k and its
 // normalisers, read by the residual and draw kernels.
-__device__ void write_record(const Params& P, int b, int mode, int k, const RowStat* rows,
-                             const Cand* cand) {
+__device__ Record make_record(const Params& P, int b, int mode, int k, const RowStat* rows,
+                              const Cand* cand) {
   Record r;
   r.k = k;
   r.mode = mode;
@@ -1404,6 +1405,11 @@ __device__ void write_record(const Params& P, int b, int mode, int k, const RowS
       r.c0_lo = cand[k].c0_lo;
     }
   }
+  return r;
+}
+__device__ void write_record(const Params& P, int b, int mode, int k, const RowStat* rows,
+                             const Cand* cand) {
+  const Record r = make_record(P, b, mode, k, rows, cand);
   int4* d = reinterpret_cast<int4*>(P.rec + b);
   const int4* src = reinterpret_cast<const int4*>(&r);
   d[0] = src[0]; d[1] = src[1]; d[2] = src[2];
@@ -1844,7 +1850,9 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
     if (last_cta && threadIdx.x == 0) ready_for_next_call(P);
     return;
   }
-  const float u = __shfl_sync(0xffffffffu, u_lane, r.k & 31) ;
+  // k is the same in every thread; k = 32 (gamma = 32, all accepted) is past the lanes
+  const float u = r.k < 32 ? __shfl_sync(0xffffffffu, u_lane, r.k)
+                           : __ldg(P.u_res + size_t(b) * R + r.k);
   const int rowk = (r.mode == MODE_BONUS) ? P.gamma : r.k;
   const unsigned char* trow = P.Lt + (size_t(b) * R + rowk) * size_t(V) * E::ES;
   bool two = (r.mode == MODE_REJECT);
@@ -2049,6 +2057,262 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
   }
   // the last kernel of a sampling call: the workspace is ready for the next one
   if (last_cta && threadIdx.x == 0) ready_for_next_call(P);
+}
+
+// ------------------------------------------- decide + residual + draw, fused
+
+// The decision, the residual mass and the draw of one request in one kernel,
+// for batches small enough that each request can have a cluster of CTAs:
+// at a few dozen requests the three kernels above cost more in launches and
+// hand-offs than in streaming the row pair.  One cluster of c CTAs per request:
+//   1. every CTA combines the request's partials and takes the decision (the
+//      same values in the same order in every CTA, so the same decision; the
+//      outputs other than token k are written by each, with equal values);
+//   2. the row token k is drawn from (with the draft row after a rejection)
+//      is split into FIN_WARPS * c contiguous segments of whole 8-element
+//      runs, one per warp of the cluster, each warp the mass of its segment
+//      (the residual kernel's arithmetic), into shared memory;
+//   3. after a cluster barrier every CTA reads all segment masses through
+//      distributed shared memory in index order: Z, the segment where the
+//      running mass crosses tau = u * Z (the last with mass if none), and what
+//      remains of tau inside it;
+//   4. the CTA owning that segment splits it over its warps, finds the
+//      crossing slice by a block prefix, and that slice's warp scans it in
+//      index order.
+// A residual that sums to 0 is replaced by target row k (steps 2 and 3 again,
+// SV_ST_DEGENERATE).
+constexpr int FIN_WARPS = 16;
+constexpr int FIN_MAXC = 8;  // CTAs per cluster (the portable limit)
+
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int DT>
+__global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
+  using E = Elem<DT>;
+  __shared__ RowStat rows[MAXR];
+  __shared__ Cand cand[MAXR];
+  __shared__ float2 dst_sh[MAXR];
+  __shared__ int2 mode_k;
+  __shared__ Record rec;
+  __shared__ FF seg_mass[2][FIN_WARPS];  // [pass][warp]: read by every CTA of the cluster
+  __shared__ FF wsum[FIN_WARPS];
+  __shared__ FF sh_rest, sh_before, sh_Z;
+  __shared__ int sh_seg, sh_wsel, sh_degen;
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int c = int(cluster.num_blocks()), q = int(cluster.block_rank());
+  const int b = int(blockIdx.x) / c;
+  const int warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int g = P.gamma, R = P.R, V = P.V;
+  const int nseg = FIN_WARPS * c;
+  // the call's inputs, before the wait
+  float lt = 0.f, ld = 0.f, u = 0.f;
+  bool tok_ok = true;
+  int xi = -1;
+  if (warp == 0 && lane < g) {
+    xi = __ldg(P.x + size_t(b) * g + lane);
+    u = __ldg(P.u_acc + size_t(b) * g + lane);
+    tok_ok = xi >= 0 && xi < V;
+    if (tok_ok) {
+      lt = E::load(P.Lt, (long long)(size_t(b) * R + lane) * V + xi);
+      ld = E::load(P.Ld, (long long)(size_t(b) * g + lane) * V + xi);
+    }
+  }
+  const float kf = LOG2E_F / __ldg(P.temp + b);
+  const bool cached = P.dstats != nullptr;
+  if (cached && int(threadIdx.x) < g)
+    dst_sh[threadIdx.x] = __ldg(reinterpret_cast<const float2*>(P.dstats) + size_t(b) * g +
+                                threadIdx.x);
+  // the next call's reduce may be placed as SMs free up: it waits for this
+  // grid's completion before it reads anything
+  allow_next_kernel();
+  wait_previous_kernel();  // the partials
+  // the reduce has completed: the control block is ready for the next call
+  if (blockIdx.x == 0 && threadIdx.x == 0) ready_for_next_call(P);
+  __syncthreads();
+
+  // 1. rows and decision
+  for (int i = warp; i < R; i += FIN_WARPS) {
+    const Partial* pp = P.part + (size_t(b) * R + i) * size_t(P.np1);
+    float mt, md;
+    FF St, Sd;
+    row_combine(pp, P.np1, kf, i < P.gs, mt, St, md, Sd);
+    if (cached && i < g) {  // the draft row's normaliser, as given
+      md = dst_sh[i].x;
+      Sd = ff(dst_sh[i].y);
+    }
+    if (lane == 0) {
+      RowStat r;
+      r.mt = mt; r.md = md;
+      r.St_h = St.h; r.St_l = St.l; r.Sd_h = Sd.h; r.Sd_l = Sd.l;
+      r.bad = (!row_ok_ff(mt, St.h) || (i < g && !row_ok_ff(md, Sd.h))) ? SV_ST_NONFINITE : 0;
+      r.amax = -1;
+      rows[i] = r;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) record_candidates(P, b, rows, cand);
+  if (warp == 0) {
+    const int2 mk = decide_sample<DT>(P, b, rows, lt, ld, u, tok_ok, xi);
+    if (lane == 0) mode_k = mk;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) rec = make_record(P, b, mode_k.x, mode_k.y, rows, cand);
+  __syncthreads();
+  Record r = rec;
+  if (r.mode == MODE_INVALID) return;  // the same in every CTA: none reaches a cluster barrier
+
+  const float ur = __ldg(P.u_res + size_t(b) * R + r.k);
+  const int rowk = (r.mode == MODE_BONUS) ? g : r.k;
+  const unsigned char* trow = P.Lt + (size_t(b) * R + rowk) * size_t(V) * E::ES;
+  const unsigned char* drow =
+      (r.mode == MODE_REJECT) ? P.Ld + (size_t(b) * g + r.k) * size_t(V) * E::ES : nullptr;
+  const long long nrun = (V + 7) / 8;
+  auto seg_lo = [&](int s) { return int(min((long long)V, nrun * s / nseg * 8)); };
+
+  // 2 and 3 (twice if the residual vanished)
+  bool degenerate = false;
+  for (int pass = 0; pass < 2; ++pass) {
+    {
+      const int s = q * FIN_WARPS + warp;
+      const int lo = seg_lo(s), hi = seg_lo(s + 1);
+      float h = 0.f, l = 0.f;
+      if (lo < hi) span_mass<DT>(r, trow, drow, lo, hi, h, l);
+      if (lane == 0) seg_mass[pass][warp] = ff(h, l);
+    }
+    cluster.sync();
+    if (warp == 0) {
+      // lane j holds segments 4 j .. 4 j + 3 (nseg <= 4 * 32)
+      FF t[4], run = ff(0.f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int s = 4 * lane + j;
+        t[j] = ff(0.f);
+        if (s < nseg) {
+          const FF* src = cluster.map_shared_rank(&seg_mass[pass][0], s / FIN_WARPS);
+          t[j] = src[s % FIN_WARPS];
+        }
+        run = run + t[j];
+      }
+      FF incl = run;
+      warp_scan_ff(incl.h, incl.l, lane);
+      const FF Z = ff_shfl(incl, 31);
+      const bool degen = !ff_pos(Z);
+      const FF tau = ff_mul(ur, Z);
+      // the first segment with mass whose running total exceeds tau, else
+      // the last segment with mass
+      FF before = incl - run;  // mass of the segments before this lane's four
+      int hit = INT_MAX, lastpos = -1;
+      FF hit_before = ff(0.f), last_before = ff(0.f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int s = 4 * lane + j;
+        if (s < nseg && ff_pos(t[j])) {
+          if (hit == INT_MAX && ff_gt(before + t[j], tau)) {
+            hit = s;
+            hit_before = before;
+          }
+          lastpos = s;
+          last_before = before;
+        }
+        before = before + t[j];
+      }
+      const unsigned hits = __ballot_sync(0xffffffffu, hit != INT_MAX);
+      const unsigned poss = __ballot_sync(0xffffffffu, lastpos >= 0);
+      const int src_lane = hits ? __ffs(hits) - 1 : (poss ? 31 - __clz(poss) : 0);
+      const int seg = __shfl_sync(0xffffffffu, hits ? hit : (lastpos >= 0 ? lastpos : 0), src_lane);
+      const FF bef = ff_shfl(hits ? hit_before : last_before, src_lane);
+      if (lane == 0) {
+        sh_degen = degen && pass == 0;
+        sh_seg = seg;
+        sh_Z = Z;
+        // past the last segment's total: aim at its last element with mass
+        sh_rest = hits ? tau - bef : ff(INFINITY);
+      }
+    }
+    __syncthreads();
+    if (!sh_degen) break;
+    // the residual vanished in fp32: draw from target row k instead
+    degenerate = true;
+    r.mode = MODE_TARGET;
+    drow = nullptr;
+  }
+  // no CTA leaves while a peer may still read its segment masses
+  cluster_arrive();
+
+  // 4. the owner of the crossing segment finds the token
+  const int sg = sh_seg;
+  if (q == sg / FIN_WARPS) {
+    const int lo = seg_lo(sg), hi = seg_lo(sg + 1);
+    const int nr = (hi - lo + 7) / 8;
+    const int per = (nr + FIN_WARPS - 1) / FIN_WARPS;
+    const int a = min(hi, lo + min(nr, warp * per) * 8);
+    const int e = min(hi, lo + min(nr, warp * per + per) * 8);
+    FF s = ff(0.f);
+    for (int i0 = a; i0 < e; i0 += 32 * 8) {
+      float w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {  // the batch's loads first
+        const int i = i0 + lane + 32 * j;
+        w[j] = i < e ? weight(r, E::load(trow, i), drow ? E::load(drow, i) : 0.f) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ff_add(s.h, s.l, w[j]);
+    }
+    warp_sum_ff(s.h, s.l);
+    if (lane == 0) wsum[warp] = s;
+    __syncthreads();
+    const FF rest = sh_rest;
+    if (threadIdx.x == 0) {
+      FF base = ff(0.f), before = ff(0.f), before_last = ff(0.f);
+      int sel = -1, last = -1;
+      for (int w = 0; w < FIN_WARPS; ++w) {
+        const FF z = wsum[w];
+        if (ff_pos(z)) {
+          last = w;
+          before_last = base;
+          if (sel < 0 && ff_gt(base + z, rest)) { sel = w; before = base; }
+        }
+        base = base + z;
+      }
+      if (sel < 0) { sel = last < 0 ? 0 : last; before = before_last; }
+      sh_wsel = sel;
+      sh_before = before;
+    }
+    __syncthreads();
+    if (warp == sh_wsel) {
+      const FF tau_s = rest - sh_before;
+      FF base = ff(0.f);
+      int tok = -1, last_pos = -1;
+      for (int i0 = a; i0 < e && tok < 0; i0 += 32) {
+        const int i = i0 + lane;
+        const float w = i < e ? weight(r, E::load(trow, i), drow ? E::load(drow, i) : 0.f) : 0.f;
+        FF incl = ff(w);
+        warp_scan_ff(incl.h, incl.l, lane);
+        incl = base + incl;
+        const unsigned h = __ballot_sync(0xffffffffu, w > 0.f && ff_gt(incl, tau_s));
+        const unsigned pv = __ballot_sync(0xffffffffu, w > 0.f);
+        if (h) tok = i0 + __ffs(h) - 1;
+        if (pv) last_pos = i0 + 31 - __clz(pv);
+        base = ff_shfl(incl, 31);
+      }
+      if (tok < 0) tok = last_pos < 0 ? lo : last_pos;  // rounding: the last element with mass
+      if (lane == 0) {
+        P.out_tokens[size_t(b) * R + r.k] = tok;
+        // the masses leave out the row's 1/S_t (a common factor)
+        const FF Z = sh_Z;
+        if (P.out_Z) P.out_Z[b] = float((double(Z.h) + double(Z.l)) *
+                                        (double(r.ist_hi) + double(r.ist_lo)));
+        if (degenerate) set_status(P, SV_ST_DEGENERATE);
+      }
+    }
+  }
+  cluster_wait();
 }
 
 // ---------------------------------------------------------- draft sampling
@@ -2258,6 +2522,7 @@ __global__ void __launch_bounds__(32 * SAMPLE_WARPS) sv_sample(const Params P) {
 
 struct Tuning {
   int chunk = 0;
+  int tail = 0;                  // 0: automatic, 1: decide/residual/draw, 2: fused (sv_set_tail)
   int withhold_slot = 0;         // failure-handling test (sv_test_withhold_slot)
   cudaEvent_t stage_ev[5] = {};  // profiling: events recorded around the kernels
   int stage_n = 0;
@@ -2323,6 +2588,26 @@ cudaError_t launch_after(void (*kern)(KArgs...), unsigned grid, unsigned block, 
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+// The same, in clusters of `cluster` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after_cluster(void (*kern)(KArgs...), unsigned grid, unsigned block,
+                                 unsigned cluster, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = cluster;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
@@ -2446,7 +2731,15 @@ int launch(const Call& a) {
   };
   mark(0);
   cudaError_t e = cudaSuccess;
-  auto run = [&](auto reduce_k, auto decide_k, auto residual_k, auto draw_k, auto sample_k) {
+  // the tail after the reduce: for batches that leave at least two SMs per
+  // request, one fused kernel with a cluster of fc CTAs per request
+  int fc = 0;
+  if (!greedy && !draft) {
+    const int per = min(FIN_MAXC, sms / B);
+    if (g_tune.tail == 2 || (g_tune.tail == 0 && per >= 2)) fc = max(1, per);
+  }
+  auto run = [&](auto reduce_k, auto decide_k, auto residual_k, auto draw_k, auto sample_k,
+                 auto finish_k) {
     // programmatic launch: the reduce's CTAs may be placed while the previous
     // kernel in the stream finishes; it waits for that kernel on the device
     e = launch_after(reduce_k, grid, NTHR, smem_bytes<GeoReduce>(), st, P);
@@ -2454,6 +2747,13 @@ int launch(const Call& a) {
     if (draft) {
       if (e == cudaSuccess)
         e = launch_after(sample_k, unsigned(units), 32 * SAMPLE_WARPS, 0, st, P);
+      mark(2);
+      return;
+    }
+    if (fc > 0) {
+      if (e == cudaSuccess)
+        e = launch_after_cluster(finish_k, unsigned(B) * unsigned(fc), 32 * FIN_WARPS,
+                                 unsigned(fc), st, P);
       mark(2);
       return;
     }
@@ -2476,9 +2776,9 @@ int launch(const Call& a) {
     constexpr int D = decltype(dt)::value;
     auto go = [&](auto reduce_k, auto decide_k) {
       if (aligned_rows)
-        run(reduce_k, decide_k, sv_residual<D, true>, sv_draw<D>, sv_sample<D>);
+        run(reduce_k, decide_k, sv_residual<D, true>, sv_draw<D>, sv_sample<D>, sv_finish<D>);
       else
-        run(reduce_k, decide_k, sv_residual<D, false>, sv_draw<D>, sv_sample<D>);
+        run(reduce_k, decide_k, sv_residual<D, false>, sv_draw<D>, sv_sample<D>, sv_finish<D>);
     };
     if (greedy)
       go(sv_reduce<D, true, true, false>, sv_decide<D, true>);
@@ -2660,6 +2960,12 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
 
 int sv_set_tuning(int chunk_elems) {
   g_tune.chunk = chunk_elems > 0 ? chunk_elems : 0;
+  return SV_OK;
+}
+
+int sv_set_tail(int mode) {
+  if (mode < 0 || mode > 2) return SV_ERR_INVALID_ARG;
+  g_tune.tail = mode;
   return SV_OK;
 }
 

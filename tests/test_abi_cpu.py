@@ -9,15 +9,14 @@ import pytest
 
 import __graft_entry__
 from speculative_decoding_verification_09_gb300 import binding
-from speculative_decoding_verification_09_gb300._build_lib import LIB_PATH, ROOT
+from speculative_decoding_verification_09_gb300._build_lib import ROOT
 
 HEADERS = [os.path.join(ROOT, "include", f) for f in ("specverify.h", "svkv.h", "svtree.h")]
 
 
 @pytest.fixture(scope="module")
 def L():
-    if not os.path.exists(LIB_PATH):
-        __graft_entry__.build()
+    __graft_entry__.build()  # rebuilds only what is out of date
     return binding.lib()
 
 
@@ -100,6 +99,13 @@ def test_stage_events_validation(L):
     nul = (ctypes.c_void_p * 2)(FAKE, None)
     assert L.sv_set_stage_events(nul, 2) == binding.SV_ERR_INVALID_ARG   # a NULL handle
     assert L.sv_set_stage_events(None, 0) == binding.SV_OK               # off
+
+
+def test_tail_selection_validation(L):
+    assert L.sv_set_tail(3) == binding.SV_ERR_INVALID_ARG
+    assert L.sv_set_tail(-1) == binding.SV_ERR_INVALID_ARG
+    for mode in (1, 2, 0):
+        assert L.sv_set_tail(mode) == binding.SV_OK
 
 
 def test_draft_and_cached_validation(L):

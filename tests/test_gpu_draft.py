@@ -17,11 +17,17 @@ from speculative_decoding_verification_09_gb300 import binding, synth
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", autouse=True)
-def _gpu():
+@pytest.fixture(scope="module", autouse=True, params=[1, 2], ids=["tail3", "fused"])
+def _gpu(request):
+    """Every test of the module runs twice: with the decide / residual / draw
+    kernels after the reduce, and with the fused tail (one cluster per
+    request), whatever the batch size."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     binding.lib()
+    binding.sv_set_tail(request.param)
+    yield
+    binding.sv_set_tail(0)
 
 
 def _draft_case(B, n, V, dtype, kind="normal", temp=0.85, seed=0):

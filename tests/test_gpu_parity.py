@@ -12,11 +12,17 @@ from speculative_decoding_verification_09_gb300 import binding, synth
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", autouse=True)
-def _gpu():
+@pytest.fixture(scope="module", autouse=True, params=[1, 2], ids=["tail3", "fused"])
+def _gpu(request):
+    """Every test of the module runs twice: with the decide / residual / draw
+    kernels after the reduce, and with the fused tail (one cluster per
+    request), whatever the batch size."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     binding.lib()
+    binding.sv_set_tail(request.param)
+    yield
+    binding.sv_set_tail(0)
 
 
 NEAR_LOG = []
@@ -283,6 +289,22 @@ def test_maximum_gamma(dtype):
     stats = compare_sampling(inp, run_sampling(inp), oracle_sampling(inp))
     assert stats["mismatches"] <= 1
     compare_greedy(run_greedy(inp), oracle.greedy(inp.Lt, inp.x, inp.dtype))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_maximum_gamma_all_accepted(dtype):
+    """gamma = SV_MAX_GAMMA with u_accept = 0, so every draft is accepted and
+    the bonus token is drawn from target row 32 with u_resample[b][32] (the
+    one uniform past the first 32 lanes)."""
+    cfg = synth.custom_config(6, binding.SV_MAX_GAMMA, 2003, dtype, "normal", temp=0.9)
+    inp = synth.make_inputs(cfg, seed=24)
+    inp.u_acc[:] = 0.0
+    ref = oracle_sampling(inp)
+    assert np.all(ref["n"] == binding.SV_MAX_GAMMA)
+    got = run_sampling(inp)
+    assert np.all(got["n"] == binding.SV_MAX_GAMMA)
+    stats = compare_sampling(inp, got, ref)
+    assert stats["mismatches"] == 0
 
 
 def test_vocabulary_of_a_million():
