@@ -2084,6 +2084,11 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
 constexpr int FIN_WARPS = 16;
 constexpr int FIN_MAXC = 8;  // CTAs per cluster (the portable limit)
 
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
@@ -2181,6 +2186,16 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
     {
       const int s = q * FIN_WARPS + warp;
       const int lo = seg_lo(s), hi = seg_lo(s + 1);
+      // the segment into L2 at once, so that the warp's later load batches hit it
+      const unsigned pf = unsigned(hi - lo) * E::ES & ~15u;
+      if (pass == 0 && lane == 0 && pf > 0) {
+        const unsigned char* pt = trow + size_t(lo) * E::ES;
+        if ((reinterpret_cast<uintptr_t>(pt) & 15u) == 0) prefetch_l2(pt, pf);
+        if (drow) {
+          const unsigned char* pd = drow + size_t(lo) * E::ES;
+          if ((reinterpret_cast<uintptr_t>(pd) & 15u) == 0) prefetch_l2(pd, pf);
+        }
+      }
       float h = 0.f, l = 0.f;
       if (lo < hi) span_mass<DT>(r, trow, drow, lo, hi, h, l);
       if (lane == 0) seg_mass[pass][warp] = ff(h, l);
@@ -2253,7 +2268,10 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
     const int per = (nr + FIN_WARPS - 1) / FIN_WARPS;
     const int a = min(hi, lo + min(nr, warp * per) * 8);
     const int e = min(hi, lo + min(nr, warp * per + per) * 8);
+    // the slice's weights in batches of 32 * 8 elements (element i0 + lane +
+    // 32 j in w[j]); the first batch stays in registers for the scan below
     FF s = ff(0.f);
+    float w0[8];
     for (int i0 = a; i0 < e; i0 += 32 * 8) {
       float w[8];
 #pragma unroll
@@ -2262,7 +2280,10 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
         w[j] = i < e ? weight(r, E::load(trow, i), drow ? E::load(drow, i) : 0.f) : 0.f;
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) ff_add(s.h, s.l, w[j]);
+      for (int j = 0; j < 8; ++j) {
+        ff_add(s.h, s.l, w[j]);
+        if (i0 == a) w0[j] = w[j];
+      }
     }
     warp_sum_ff(s.h, s.l);
     if (lane == 0) wsum[warp] = s;
@@ -2289,9 +2310,8 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
       const FF tau_s = rest - sh_before;
       FF base = ff(0.f);
       int tok = -1, last_pos = -1;
-      for (int i0 = a; i0 < e && tok < 0; i0 += 32) {
-        const int i = i0 + lane;
-        const float w = i < e ? weight(r, E::load(trow, i), drow ? E::load(drow, i) : 0.f) : 0.f;
+      // tiles of 32 elements in index order: the first eight from registers
+      auto tile = [&](int i0, float w) {
         FF incl = ff(w);
         warp_scan_ff(incl.h, incl.l, lane);
         incl = base + incl;
@@ -2300,6 +2320,15 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
         if (h) tok = i0 + __ffs(h) - 1;
         if (pv) last_pos = i0 + 31 - __clz(pv);
         base = ff_shfl(incl, 31);
+      };
+      if (a < e) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (tok < 0) tile(a + 32 * j, w0[j]);
+      }
+      for (int i0 = a + 32 * 8; i0 < e && tok < 0; i0 += 32) {  // slices past 256 elements
+        const int i = i0 + lane;
+        tile(i0, i < e ? weight(r, E::load(trow, i), drow ? E::load(drow, i) : 0.f) : 0.f);
       }
       if (tok < 0) tok = last_pos < 0 ? lo : last_pos;  // rounding: the last element with mass
       if (lane == 0) {
