@@ -436,6 +436,7 @@ def run_ours(args) -> None:
     ws = binding.make_workspace(B, g, V, dev)
     if args.chunk:
         binding.sv_set_tuning(args.chunk)
+    binding.sv_set_tail(args.tail)
 
     def step(t):
         if greedy:
@@ -460,8 +461,15 @@ def run_ours(args) -> None:
     # library records an event before its first kernel and one after the
     # reduce kernel (an event between two kernels stops the next one from
     # being launched early, so the headline loop has none)
-    n_kern = 2 if greedy else 4
-    kernel_names = ["reduce", "decide"] if greedy else ["reduce", "decide", "residual", "draw"]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fused = not greedy and (args.tail == 2 or (args.tail == 0 and min(8, sms // B) >= 2))
+    if greedy:
+        kernel_names = ["reduce", "decide"]
+    elif fused:  # small batches: one fused kernel after the reduce
+        kernel_names = ["reduce", "finish"]
+    else:
+        kernel_names = ["reduce", "decide", "residual", "draw"]
+    n_kern = len(kernel_names)
 
     def make_events(n):
         es = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -611,7 +619,7 @@ def run_ours(args) -> None:
 
     if rank != 0:
         return
-    traffic = read_traffic() if cid == 4 else None
+    traffic = read_traffic() if (cid == 4 and not args.batch and args.tail != 2) else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -635,7 +643,7 @@ def run_ours(args) -> None:
         "draft_side": draft_side, "kv_side": kv_side, "tree_side": tree_side,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_kern * args.steps, "clocks": clk,
         "status": st, "wall_s_timed": t_wall,
-        "tuning": {"chunk": args.chunk},
+        "tuning": {"chunk": args.chunk, "tail": args.tail},
     }
     print(json.dumps(line))
     if pg:
@@ -673,6 +681,8 @@ def main():
                     help="approximate seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-requests", type=int, default=32)
     ap.add_argument("--chunk", type=int, default=0, help="phase-1 chunk elements (0 = auto)")
+    ap.add_argument("--tail", type=int, default=0, choices=[0, 1, 2],
+                    help="kernels after the reduce: 0 automatic, 1 decide/residual/draw, 2 fused")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
