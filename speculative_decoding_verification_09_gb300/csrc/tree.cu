@@ -39,6 +39,7 @@ namespace {
 constexpr int TW = 16;            // warps per CTA
 constexpr int TTHR = 32 * TW;
 constexpr int TMAXC = 8;          // CTAs per cluster (the portable limit)
+static_assert(SV_TREE_MAX_N <= 32 * TW, "one child per thread at every node");
 constexpr int TU = 4;             // 16-byte vectors per lane and row in a batch
 constexpr int NS = 3;             // ring slots per warp
 constexpr int CHV = 32 * TU;      // 16-byte vectors of one row in a slot
@@ -631,15 +632,19 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
     const bool has_child = __syncthreads_or(hc) != 0;
     const unsigned char* rt = P.Lt + ((long long)b * N + n) * row_bytes;
     const unsigned char* rd = has_child ? P.Ld + ((long long)b * N + n) * row_bytes : nullptr;
-    // the children's logits at their tokens, for the accept tests
-    for (int i = n + 1 + tid; i < N; i += TTHR) {
-      if (sm.parent[i] == n) {
-        sm.xl_t[i] = E::at(rt, sm.token[i]);
-        sm.xl_d[i] = E::at(rd, sm.token[i]);
-        sm.ua[i] = P.u_acc[(long long)b * N + i];
-      }
+    // the children's logits at their tokens and uniforms, for the accept
+    // tests: loaded into registers now and stored after the pass, so that no
+    // warp waits for them before it starts streaming (child ci of thread tid
+    // is node n + 1 + tid: N <= TTHR)
+    const int ci = n + 1 + tid;
+    const bool mine = ci < N && sm.parent[ci] == n;
+    float cxt = 0.f, cxd = 0.f, cua = 0.f, cur = 0.f;
+    if (mine) {
+      cxt = E::at(rt, sm.token[ci]);
+      cxd = E::at(rd, sm.token[ci]);
+      cua = P.u_acc[(long long)b * N + ci];
     }
-    if (tid == TTHR - 1) sm.ur = P.u_res[(long long)b * N + n];
+    if (tid == TTHR - 1) cur = P.u_res[(long long)b * N + n];
 
     // pass 1: the rows' max and exp-sum
     {
@@ -652,9 +657,17 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
         sm.part[buf][1][warp] = pd;
       }
     }
+    if (mine) {
+      sm.xl_t[ci] = cxt;
+      sm.xl_d[ci] = cxd;
+      sm.ua[ci] = cua;
+    }
+    if (tid == TTHR - 1) sm.ur = cur;
     cluster.sync();
-    if (warp == 0) {
-      for (int r = 0; r < (has_child ? 2 : 1); ++r) {
+    // warp 0 combines the target row's partials, warp 1 the draft row's
+    if (warp < (has_child ? 2 : 1)) {
+      {
+        const int r = warp;
         Part p[4];
         float M = -INFINITY;
 #pragma unroll
