@@ -21,8 +21,18 @@ def _gpu(request):
         pytest.skip("no CUDA device")
     binding.lib()
     binding.sv_set_tail(request.param)
+    _TAIL[0] = request.param
     yield
     binding.sv_set_tail(0)
+    _TAIL[0] = 0
+
+
+_TAIL = [0]
+
+
+def _gpu_tail() -> int:
+    """The tail the module fixture selected for the running tests."""
+    return _TAIL[0]
 
 
 NEAR_LOG = []
@@ -321,6 +331,21 @@ def test_many_requests_small_rows():
     cfg = synth.custom_config(3000, 3, 257, "f32", "normal", temp=("uniform", 0.5, 1.5))
     inp = synth.make_inputs(cfg, seed=23)
     stats = compare_sampling(inp, run_sampling(inp), oracle_sampling(inp))
+    assert stats["mismatches"] <= 1
+
+
+@pytest.mark.parametrize("B", [75, 76, 77, 152, 153])
+def test_automatic_tail_around_its_boundary(B):
+    """The automatic choice (fused tail while B * 2 <= SMs, so up to B = 76 on
+    152 SMs; three kernels above), checked on both sides of the boundary and
+    where one SM per request is left or fewer, against the oracle."""
+    cfg = synth.custom_config(B, 3, 3001, "bf16", "normal", temp=("uniform", 0.6, 1.4))
+    inp = synth.make_inputs(cfg, seed=50 + B)
+    binding.sv_set_tail(0)
+    try:
+        stats = compare_sampling(inp, run_sampling(inp), oracle_sampling(inp))
+    finally:
+        binding.sv_set_tail(_gpu_tail())
     assert stats["mismatches"] <= 1
 
 
