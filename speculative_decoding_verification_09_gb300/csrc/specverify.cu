@@ -13,7 +13,8 @@
 // the device for the previous kernel's memory):
 //   reduce   one CTA per SM, each streaming a contiguous range of row chunks
 //            (chunk c of target row i and draft row i of request b; or two
-//            target chunks when no draft rows are streamed) from HBM into a
+//            target chunks when no draft rows are streamed), then units of
+//            the last requests' chunks claimed from a counter, from HBM into a
 //            ring of shared-memory slots with TMA bulk copies (cp.async.bulk,
 //            completion counted on an mbarrier) issued by one producer lane;
 //            consumer warps reduce each slot from registers and publish one
@@ -29,6 +30,10 @@
 //            bonus): the mass of each warp's contiguous sub-range.
 //   draw     one CTA per request: the sub-range where the running mass
 //            crosses u * Z, scanned in index order: token k.
+// Batches that leave at least two SMs per request replace decide, residual
+// and draw by one kernel, finish, with a cluster of CTAs per request (the
+// decision in every CTA, segment masses shared through distributed shared
+// memory, the token found by the CTA owning the crossing segment).
 // Greedy verification runs reduce (chunk argmax) and decide only; draft
 // sampling runs reduce (contiguous warp shares) and sample (one CTA per draft
 // row: the crossing partial's span, scanned in index order).
