@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import subprocess
@@ -43,8 +44,14 @@ WORKLOADS = {f"c{i}": i for i in synth.CONFIGS}
 
 
 def kernel_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256/16 of the kernel code: the source with comments and blank lines
+    removed, so that an edit of a comment does not void recorded counters."""
+    with open(KERNEL_SRC, encoding="utf-8") as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    code = "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+    return hashlib.sha256(code.encode("utf-8")).hexdigest()[:16]
 
 
 def read_peaks() -> tuple[float, str]:
@@ -66,7 +73,7 @@ def read_traffic() -> float | None:
                 if ":" in line:
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_sha256_16") != kernel_hash():
+        if kv.get("kernel_code_sha256_16") != kernel_hash():
             return None
         return float(kv["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
