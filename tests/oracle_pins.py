@@ -149,6 +149,36 @@ def pin_expected_tokens(lib):
     assert np.all(out["tokens"][:, 0] < 4)
 
 
+def pin_mixture_acceptance(lib):
+    """考点2 / 考点4: a draft token x ~ P_d is accepted with probability
+    sum_v min(P_t, P_d).  The softmax-mix draft rows of the large-batch
+    workload, P_d = w P_t + (1 - w) q, make that at least w.  The oracle's
+    acceptance frequency over draws from P_d must match the closed form within
+    4 sigma for w = 0.3, 0.6, 0.9, with the rows stored as T ln p at T = 0.7
+    (so the temperature must reach both rows)."""
+    rng = np.random.default_rng(45)
+    V, N, T = 40, 60000, np.float32(0.7)
+    for w in (0.3, 0.6, 0.9):
+        p_t = rng.dirichlet(np.full(V, 0.5))
+        q = rng.dirichlet(np.full(V, 0.5))
+        p_d = w * p_t + (1 - w) * q
+        lt = (T * _ln(p_t)).astype(np.float32)
+        ld = (T * _ln(p_d)).astype(np.float32)
+        # the stored rows' own distributions (after fp32 rounding), in fp64
+        pt = softmax(lt.astype(np.float64) / float(T))
+        pd = softmax(ld.astype(np.float64) / float(T))
+        alpha = float(np.minimum(pt, pd).sum())
+        assert alpha >= w - 1e-6, (w, alpha)
+        x = rng.choice(V, size=(N, 1), p=pd).astype(np.int32)
+        Lt, Ld, _, _, _, temp = _batch(N, [lt, lt], [ld], [0], 0.0, [0.0, 0.0], T)
+        ua = rng.random((N, 1), dtype=np.float32)
+        ur = rng.random((N, 2), dtype=np.float32)
+        out = oracle.verify(Lt, Ld, x, ua, ur, temp, F32, lib=lib)
+        f = float(out["n"].mean())
+        sd = np.sqrt(alpha * (1 - alpha) / N)
+        assert abs(f - alpha) < 4 * sd, (w, f, alpha)
+
+
 # ------------------------------------------------------------- mathematics
 
 def pin_losslessness_chisq(lib, trials=1_000_000):
@@ -395,6 +425,7 @@ def pin_greedy(lib):
 
 
 ALL_PINS = [pin_worked_example, pin_numpy_operator_vectors, pin_expected_tokens,
+            pin_mixture_acceptance,
             pin_losslessness_chisq, pin_brute_force_tiny, pin_accept_boundary,
             pin_inverse_cdf_strict, pin_softmax_textbook, pin_degenerate_shapes,
             pin_invalid_inputs, pin_greedy]
