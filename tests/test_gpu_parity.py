@@ -216,6 +216,39 @@ def test_repeated_calls_reuse_workspace_and_streams():
     assert np.array_equal(again["tokens"], first["tokens"]) and again["status"] == 0
 
 
+def test_overlapping_calls_on_three_streams():
+    """Calls that overlap on the GPU (three streams, one workspace each, all
+    queued before any is waited for, different batches and shapes per
+    stream) each give the oracle's results."""
+    cfgs = [synth.custom_config(12, 3, 9001, "bf16", "mix"),
+            synth.custom_config(100, 2, 4099, "f32", "normal", temp=("uniform", 0.5, 1.5)),
+            synth.custom_config(7, 5, 20011, "bf16", "zipf", temp=0.8)]
+    inps = [synth.make_inputs(c, seed=60 + j) for j, c in enumerate(cfgs)]
+    refs = [oracle_sampling(x) for x in inps]
+    streams = [torch.cuda.Stream() for _ in inps]
+    devs = [to_dev(x) for x in inps]
+    wss = [binding.make_workspace(x.B, x.gamma, x.V, DEV) for x in inps]
+    outs = []
+    for x in inps:
+        outs.append(dict(tok=torch.full((x.B, x.gamma + 1), -7, dtype=torch.int32, device=DEV),
+                         n=torch.full((x.B,), -7, dtype=torch.int32, device=DEV),
+                         st=torch.zeros(1, dtype=torch.int32, device=DEV)))
+    torch.cuda.synchronize()
+    for rep in range(4):  # each stream's calls queue behind one another
+        for x, d, ws, o, s in zip(inps, devs, wss, outs, streams):
+            binding.spec_verify(d["Lt"], d["Ld"], d["x"], d["u_acc"], d["u_res"], d["temp"],
+                                o["tok"], o["n"], ws, o["st"], s)
+    torch.cuda.synchronize()
+    for x, o, ref in zip(inps, outs, refs):
+        got = dict(tokens=o["tok"].cpu().numpy(), n=o["n"].cpu().numpy(),
+                   p=np.zeros((x.B, x.gamma, 2), np.float32), Z=np.zeros(x.B, np.float32),
+                   status=int(o["st"].item()))
+        near = (ref["flags"] & oracle.NEAR_ANY) != 0
+        same = np.all(got["tokens"] == ref["tokens"], axis=1) & (got["n"] == ref["n"])
+        assert np.all(same | near), np.argwhere(~(same | near)).ravel()
+        assert got["status"] == 0
+
+
 # Workspace layout facts used to poison it: the control block takes bytes
 # 0..63 (the call-state word at byte 0, the reduce's pool-claim counter at
 # byte 8, both 0 between calls); the partials start at byte 256.
