@@ -89,8 +89,8 @@ constexpr int CH2_F32 = GeoResidual::HALF / 4;  // phase-2 chunk for fp32 (the w
 constexpr unsigned SUSPEND_HINT_NS = 1000000u;  // a waiting warp sleeps until the phase completes
 constexpr int SMS_CAP = 256;           // the chunk heuristic assumes at most this many SMs
 constexpr int MAXR = SV_MAX_GAMMA + 1;
-constexpr int DECIDE_WARPS = 8;        // decide: warps per request
-constexpr int DRAW_WARPS = 8;          // draw: warps per request
+constexpr int DECIDE_WARPS = 16;       // decide: warps per request
+constexpr int DRAW_WARPS = 4;          // draw: warps per request
 constexpr int SAMPLE_WARPS = 4;        // draft sampling: warps per draft row
 constexpr float LOG2E_F = 1.4426950408889634f;
 constexpr double LOG2E_D = 1.4426950408889634;
