@@ -1454,19 +1454,20 @@ __device__ void decide_greedy(const Params& P, int b, const RowStat* rows) {
 // i % DECIDE_WARPS), then warp 0 decides.  The draft tokens, their logits and
 // the uniforms are loaded by warp 0 before its rows; given draft normalisers
 // (dstats) replace the draft rows' combine.
-template <int DT, bool GREEDY>
-__global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, bool last) {
+// The decision's per-position inputs of request b (warp 0, lane i < gamma
+// takes position i): draft token, accept uniform, and the target and draft
+// logits at the token.  They are the call's inputs, so they are loaded before
+// the wait for the partials.
+template <int DT>
+__device__ __forceinline__ void load_decision_inputs(const Params& P, int b, float& lt, float& ld,
+                                                     float& u, bool& tok_ok, int& xi) {
   using E = Elem<DT>;
-  __shared__ RowStat rows[MAXR];
-  __shared__ Cand cand[MAXR];
-  __shared__ float2 dst_sh[MAXR];
-  __shared__ int2 mode_k;
-  const int b = blockIdx.x, warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int g = P.gamma, R = P.R, V = P.V;
-  float lt = 0.f, ld = 0.f, u = 0.f;
-  bool tok_ok = true;
-  int xi = -1;
-  if (!GREEDY && warp == 0 && lane < g) {
+  const int lane = threadIdx.x & 31;
+  lt = ld = u = 0.f;
+  tok_ok = true;
+  xi = -1;
+  if ((threadIdx.x >> 5) == 0 && lane < g) {
     xi = __ldg(P.x + size_t(b) * g + lane);
     u = __ldg(P.u_acc + size_t(b) * g + lane);
     tok_ok = xi >= 0 && xi < V;
@@ -1475,6 +1476,49 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
       ld = E::load(P.Ld, (long long)(size_t(b) * g + lane) * V + xi);
     }
   }
+}
+
+// Every row's statistics of request b for the sampling decision, the warps of
+// the CTA taking rows in turn: the partials combined (row_combine), or the
+// draft row's normaliser as given (dst_sh, cached verification).
+template <int NWARPS>
+__device__ void combine_rows(const Params& P, int b, float kf, const float2* dst_sh,
+                             RowStat* rows) {
+  const int warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int g = P.gamma, R = P.R;
+  const bool cached = P.dstats != nullptr;
+  for (int i = warp; i < R; i += NWARPS) {
+    const Partial* pp = P.part + (size_t(b) * R + i) * size_t(P.np1);
+    float mt, md;
+    FF St, Sd;
+    row_combine(pp, P.np1, kf, i < P.gs, mt, St, md, Sd);
+    if (cached && i < g) {  // the draft row's normaliser, as given
+      md = dst_sh[i].x;
+      Sd = ff(dst_sh[i].y);
+    }
+    if (lane == 0) {
+      RowStat r;
+      r.mt = mt; r.md = md;
+      r.St_h = St.h; r.St_l = St.l; r.Sd_h = Sd.h; r.Sd_l = Sd.l;
+      r.bad = (!row_ok_ff(mt, St.h) || (i < g && !row_ok_ff(md, Sd.h))) ? SV_ST_NONFINITE : 0;
+      r.amax = -1;
+      rows[i] = r;
+    }
+  }
+}
+
+template <int DT, bool GREEDY>
+__global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, bool last) {
+  __shared__ RowStat rows[MAXR];
+  __shared__ Cand cand[MAXR];
+  __shared__ float2 dst_sh[MAXR];
+  __shared__ int2 mode_k;
+  const int b = blockIdx.x, warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int g = P.gamma, R = P.R;
+  float lt = 0.f, ld = 0.f, u = 0.f;
+  bool tok_ok = true;
+  int xi = -1;
+  if (!GREEDY) load_decision_inputs<DT>(P, b, lt, ld, u, tok_ok, xi);
   const float kf = GREEDY ? 0.f : LOG2E_F / __ldg(P.temp + b);
   const bool cached = !GREEDY && P.dstats != nullptr;
   if (cached && int(threadIdx.x) < g)
@@ -1484,9 +1528,9 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
   // reduce kernel
   wait_previous_kernel();
   if (cached) __syncthreads();
-  for (int i = warp; i < R; i += DECIDE_WARPS) {
-    const Partial* pp = P.part + (size_t(b) * R + i) * size_t(P.np1);
-    if (GREEDY) {
+  if (GREEDY) {
+    for (int i = warp; i < R; i += DECIDE_WARPS) {
+      const Partial* pp = P.part + (size_t(b) * R + i) * size_t(P.np1);
       float best;
       int bi, nan;
       row_argmax(pp, P.np1, best, bi, nan);
@@ -1497,23 +1541,9 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
         r.amax = bi;
         rows[i] = r;
       }
-    } else {
-      float mt, md;
-      FF St, Sd;
-      row_combine(pp, P.np1, kf, i < P.gs, mt, St, md, Sd);
-      if (cached && i < g) {  // the draft row's normaliser, as given
-        md = dst_sh[i].x;
-        Sd = ff(dst_sh[i].y);
-      }
-      if (lane == 0) {
-        RowStat r;
-        r.mt = mt; r.md = md;
-        r.St_h = St.h; r.St_l = St.l; r.Sd_h = Sd.h; r.Sd_l = Sd.l;
-        r.bad = (!row_ok_ff(mt, St.h) || (i < g && !row_ok_ff(md, Sd.h))) ? SV_ST_NONFINITE : 0;
-        r.amax = -1;
-        rows[i] = r;
-      }
     }
+  } else {
+    combine_rows<DECIDE_WARPS>(P, b, kf, dst_sh, rows);
   }
   __syncthreads();
   if (GREEDY) {
@@ -2121,18 +2151,10 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
   const int g = P.gamma, R = P.R, V = P.V;
   const int nseg = FIN_WARPS * c;
   // the call's inputs, before the wait
-  float lt = 0.f, ld = 0.f, u = 0.f;
-  bool tok_ok = true;
-  int xi = -1;
-  if (warp == 0 && lane < g) {
-    xi = __ldg(P.x + size_t(b) * g + lane);
-    u = __ldg(P.u_acc + size_t(b) * g + lane);
-    tok_ok = xi >= 0 && xi < V;
-    if (tok_ok) {
-      lt = E::load(P.Lt, (long long)(size_t(b) * R + lane) * V + xi);
-      ld = E::load(P.Ld, (long long)(size_t(b) * g + lane) * V + xi);
-    }
-  }
+  float lt, ld, u;
+  bool tok_ok;
+  int xi;
+  load_decision_inputs<DT>(P, b, lt, ld, u, tok_ok, xi);
   const float kf = LOG2E_F / __ldg(P.temp + b);
   const bool cached = P.dstats != nullptr;
   if (cached && int(threadIdx.x) < g)
@@ -2147,24 +2169,7 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
   __syncthreads();
 
   // 1. rows and decision
-  for (int i = warp; i < R; i += FIN_WARPS) {
-    const Partial* pp = P.part + (size_t(b) * R + i) * size_t(P.np1);
-    float mt, md;
-    FF St, Sd;
-    row_combine(pp, P.np1, kf, i < P.gs, mt, St, md, Sd);
-    if (cached && i < g) {  // the draft row's normaliser, as given
-      md = dst_sh[i].x;
-      Sd = ff(dst_sh[i].y);
-    }
-    if (lane == 0) {
-      RowStat r;
-      r.mt = mt; r.md = md;
-      r.St_h = St.h; r.St_l = St.l; r.Sd_h = Sd.h; r.Sd_l = Sd.l;
-      r.bad = (!row_ok_ff(mt, St.h) || (i < g && !row_ok_ff(md, Sd.h))) ? SV_ST_NONFINITE : 0;
-      r.amax = -1;
-      rows[i] = r;
-    }
-  }
+  combine_rows<FIN_WARPS>(P, b, kf, dst_sh, rows);
   __syncthreads();
   if (warp == 1) record_candidates(P, b, rows, cand);
   if (warp == 0) {
