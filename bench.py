@@ -43,15 +43,19 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_c4.txt")
 WORKLOADS = {f"c{i}": i for i in synth.CONFIGS}
 
 
-def kernel_hash() -> str:
-    """sha256/16 of the kernel code: the source with comments and blank lines
-    removed, so that an edit of a comment does not void recorded counters."""
-    with open(KERNEL_SRC, encoding="utf-8") as f:
-        src = f.read()
+def code_hash(src: str) -> str:
+    """sha256/16 of C/CUDA source with comments and blank lines removed."""
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     src = re.sub(r"//[^\n]*", "", src)
     code = "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
     return hashlib.sha256(code.encode("utf-8")).hexdigest()[:16]
+
+
+def kernel_hash() -> str:
+    """The kernel code's hash, so that an edit of a comment does not void the
+    recorded counters but any change of code does."""
+    with open(KERNEL_SRC, encoding="utf-8") as f:
+        return code_hash(f.read())
 
 
 def read_peaks() -> tuple[float, str]:
