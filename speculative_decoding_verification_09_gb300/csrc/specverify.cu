@@ -1450,10 +1450,6 @@ __device__ void decide_greedy(const Params& P, int b, const RowStat* rows) {
   }
 }
 
-// One CTA per request: DECIDE_WARPS warps combine the rows (row i by warp
-// i % DECIDE_WARPS), then warp 0 decides.  The draft tokens, their logits and
-// the uniforms are loaded by warp 0 before its rows; given draft normalisers
-// (dstats) replace the draft rows' combine.
 // The decision's per-position inputs of request b (warp 0, lane i < gamma
 // takes position i): draft token, accept uniform, and the target and draft
 // logits at the token.  They are the call's inputs, so they are loaded before
@@ -1507,6 +1503,10 @@ __device__ void combine_rows(const Params& P, int b, float kf, const float2* dst
   }
 }
 
+// One CTA per request: DECIDE_WARPS warps combine the rows (row i by warp
+// i % DECIDE_WARPS), then warp 0 decides.  The draft tokens, their logits and
+// the uniforms are loaded by warp 0 before its rows; given draft normalisers
+// (dstats) replace the draft rows' combine.
 template <int DT, bool GREEDY>
 __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, bool last) {
   __shared__ RowStat rows[MAXR];
