@@ -192,9 +192,12 @@ int spec_verify_cached(const void* target_logits, const void* draft_logits,
  * device) and calls no allocating routine.
  *   - Sizes whose sv_workspace_bytes(B, gamma, V) exceeds
  *     SV_NOALLOC_MAX_WORKSPACE return SV_ERR_WORKSPACE; nothing is launched.
- *   - The first call on a device looks up the scratch array's device
- *     address (cudaGetSymbolAddress) with that device current; make that
- *     first call before any stream capture.
+ *   - Every call looks up the scratch array's device address
+ *     (cudaGetSymbolAddress) with the calling thread's device current; the
+ *     address is not cached, so a context created anew after
+ *     cudaDeviceReset is served correctly.  The first call on a device also
+ *     loads the library's kernels into that context: make it before any
+ *     stream capture.
  *   - Each call resets the scratch's 64-byte control block on `stream`
  *     before its launches; every other byte of the scratch that a call reads
  *     is written earlier in the same call.

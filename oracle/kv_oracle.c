@@ -26,7 +26,7 @@
  *       "两条贯穿始终的不变量" -- every length input is windowed by the same
  *           arithmetic; the slot mapping (writes) is never windowed.
  *
- * Readings (listed in the design doc as well):
+ * Readings taken where the page leaves a step open:
  *   K1  what is committed: the verification step ran the target over R =
  *       gamma + 1 inputs (the last emitted token and the gamma drafts) at
  *       logical positions pos .. pos + gamma and staged their KV; with k drafts

@@ -21,8 +21,7 @@
  *       row, per-position accept test in draft order, stop at the first
  *       rejection ("后续推迟序列作废"), inverse-CDF scan in vocabulary order.
  *
- * Readings taken where the pages are silent or disagree (each is listed in
- * the design doc as well):
+ * Readings taken where the pages are silent or disagree:
  *   R1  accept iff u <= r (the NumPy operator), not u < r.
  *   R2  P_draft(x) == 0 gives r = 1 (the limit of the formula), no epsilon.
  *   R3  the residual is formed from PROBABILITIES (考点2), not from raw

@@ -102,7 +102,8 @@ struct Ctrl {                 // 64 bytes at the start of the workspace
   // both 0 between calls (the ready state); state is 1 while a call runs,
   // claims counts the reduce's claims of pool units (reset by the call's last kernel)
   unsigned long long state, claims;
-  unsigned long long pad[6];  // pad[0]: the residual kernel's chunk-claim counter
+  unsigned long long pad[6];  // pad[0]: the residual kernel's chunk-claim counter;
+                              // pad[1]: pool units the reduce's CTAs took (0 between calls)
 };
 struct Partial {              // per (request, position, chunk, consumer warp)
   float a, b, c, d;           // sampling: m_t, s_t, m_d, s_d; greedy: value, index, nan, 0
@@ -176,6 +177,7 @@ struct Params {
   float* out_Z;
   float* out_stats;           // draft sampling: row normalisers (m, S)
   int withhold_slot;          // failure-handling test: CTA 0 never fills its first reduce slot
+  int reduce_grid;            // CTAs of the call's reduce kernel
   int col, ncols;             // draft sampling: row i of request b goes to column col + i of ncols
   int32_t* status;
   Ctrl* ctrl;
@@ -297,10 +299,19 @@ __device__ __forceinline__ void set_status(const Params& P, int bits) {
   if (bits && P.status) atomicOr(P.status, bits);
 }
 
+// Units of the reduce's claimed pool (see reduce_split).
+__device__ long long reduce_pool_units(const Params& P, long long nb);
+
 // The control block's ready state, written by the last kernel of a call
 // (the reduce of this call has completed; the next call's reduce reads it
-// only after this kernel has completed).
+// only after this kernel has completed).  The pool units the reduce's CTAs
+// took must add up to the pool: a claim counter that did not start the call
+// at 0 would have skipped units, and is reported like a workspace that was
+// not in its ready state.
 __device__ __forceinline__ void ready_for_next_call(const Params& P) {
+  if (P.ctrl->pad[1] != (unsigned long long)reduce_pool_units(P, P.reduce_grid))
+    set_status(P, SV_ST_WORKSPACE);
+  P.ctrl->pad[1] = 0ull;
   P.ctrl->state = 0ull;
   P.ctrl->claims = 0ull;
 }
@@ -999,6 +1010,9 @@ __device__ __forceinline__ Split reduce_split(const Params& P, long long x, long
   sp.nunits = (pool + sp.unit - 1) / sp.unit;
   return sp;
 }
+__device__ long long reduce_pool_units(const Params& P, long long nb) {
+  return reduce_split(P, 0, nb).nunits;
+}
 
 // Producer (one lane): this CTA's static range of chunks, then the pool
 // units it claims, each in order, into the slot ring.  Chunk t is chunk
@@ -1014,6 +1028,10 @@ __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* 
   constexpr int NS = G::NS, SLOT = G::SLOT, HALF = G::HALF;
   const Split sp = reduce_split(P, blockIdx.x, gridDim.x);
   long long t = sp.t0, tend = sp.t1;  // the range being streamed
+  unsigned long long taken = 0;       // pool units this CTA took
+  auto report = [&]() {
+    if (taken) atomicAdd(&P.ctrl->pad[1], taken);
+  };
   // a claim is issued while the current range still has NS tasks to go, so
   // its round trip is hidden behind the slots in flight
   long long claimed = 0;
@@ -1063,17 +1081,23 @@ __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* 
         t = sp.ts + claimed * sp.unit;
         tend = min(t + sp.unit, P.tasks);
         pending = false;
+        ++taken;
         seek(t);
       } else {
+        report();
         end_markers(P, C, seq);
         return;
       }
     }
     if (C.abort) {
+      report();
       end_markers(P, C, seq);
       return;
     }
-    if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, &C.abort)) return;
+    if (use > 0 && !mbar_wait(&C.empty[s], (use - 1) & 1u, P, &C.abort)) {
+      report();
+      return;
+    }
     Desc& d = C.desc[s];
     d.end = 0;
     d.b = b; d.i = i; d.c = c;
@@ -1210,9 +1234,11 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
   // it wrote is read before it has completed
   wait_previous_kernel();
   if (threadIdx.x == 0) {
-    // the workspace is in its ready state between calls; mark this call
+    // the workspace is in its ready state between calls; mark this call.
+    // Only the state word is tested: the other CTAs of this grid may already
+    // be claiming pool units, so the claim counter can be non-zero here.
     if (blockIdx.x == 0) {
-      if (P.ctrl->state != 0ull || P.ctrl->claims != 0ull) set_status(P, SV_ST_WORKSPACE);
+      if (P.ctrl->state != 0ull) set_status(P, SV_ST_WORKSPACE);
       P.ctrl->state = 1ull;
       P.ctrl->pad[0] = 0ull;  // the residual kernel's chunk claims
     }
@@ -2752,6 +2778,7 @@ int launch(const Call& a) {
   P.out_tokens = a.out_tokens; P.out_n = a.out_n; P.out_p = a.out_p; P.out_Z = a.out_Z;
   P.out_stats = a.out_stats; P.col = a.col; P.ncols = a.ncols;
   P.withhold_slot = g_tune.withhold_slot;
+  P.reduce_grid = int(min((long long)sms, P.tasks));
   P.status = a.status;
   unsigned char* w = static_cast<unsigned char*>(a.ws);
   P.ctrl = reinterpret_cast<Ctrl*>(w + L.ctrl);
@@ -2951,21 +2978,15 @@ int sv_draft_sample(const void* draft_logits, const float* u_draft, const float*
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_MAX_WORKSPACE];
 
 namespace {
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {};  // device address of g_noalloc_scratch, per device
-
-// Device address of the scratch on the current device; the lookup runs once
-// per device, with that device current.
+// Device address of the scratch in the current context, looked up on every
+// call with the calling thread's device current.  The lookup allocates
+// nothing and enqueues nothing; it is not cached, because a context that is
+// destroyed and created again (cudaDeviceReset) loads the module anew and
+// the array may then sit at another address.
 int noalloc_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SV_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SV_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SV_ERR_CUDA;
+  *out = p;
   return SV_OK;
 }
 }  // namespace

@@ -81,6 +81,52 @@ def expected_status(flags: np.ndarray) -> int:
     return s
 
 
+def _row_probs(L, dtype: int, T: float) -> np.ndarray:
+    """softmax(l / T) of one stored logit row, in fp64."""
+    w = synth.widen(L, dtype).astype(np.float64) / float(T)
+    m = np.max(w)
+    if not np.isfinite(m):
+        return np.zeros_like(w)
+    p = np.exp(w - m)
+    return p / p.sum()
+
+
+def check_valid_draw(inp: synth.Inputs, got: dict, ref: dict, b: int) -> None:
+    """A request whose GPU result differs from the oracle's at a flagged
+    near-tie must still be a result the rule allows, decided within the
+    1e-6 window:
+      * the outputs have the rule's shape: the accepted drafts, one drawn
+        token, then -1;
+      * where the accepted counts differ, the first position decided
+        differently has |u_accept - r| < 1e-6 (r the oracle's fp64 ratio);
+      * the drawn token's interval of the fp64 CDF it is drawn from (the
+        residual of row k, the target row gamma for the bonus, the target
+        row k when the residual vanishes) contains u_resample[b][k] to
+        within 1e-6."""
+    g, tok = inp.gamma, got["tokens"][b]
+    kg, kr = int(got["n"][b]), int(ref["n"][b])
+    assert 0 <= kg <= g, (b, kg)
+    assert np.array_equal(tok[:kg], inp.x[b, :kg]) and np.all(tok[kg + 1:] == -1), (b, tok)
+    if kg != kr:
+        i = min(kg, kr)
+        pt, pd = float(ref["pt"][b, i]), float(ref["pd"][b, i])
+        r = 1.0 if pd == 0.0 else min(1.0, pt / pd)
+        assert abs(float(inp.u_acc[b, i]) - r) < oracle.NEAR_EPS, (b, i, float(inp.u_acc[b, i]), r)
+    T = float(inp.temp[b])
+    row_t = inp.Lt[b, kg]
+    w = _row_probs(row_t, inp.dtype, T)
+    if kg < g:
+        res = np.maximum(0.0, w - _row_probs(inp.Ld[b, kg], inp.dtype, T))
+        if res.sum() > 0.0:
+            w = res
+    c = np.cumsum(w) / w.sum()
+    v = int(tok[kg])
+    assert 0 <= v < inp.V and w[v] > 0.0, (b, v)
+    lo, hi = (c[v - 1] if v > 0 else 0.0), c[v]
+    u = float(inp.u_res[b, kg])
+    assert lo - oracle.NEAR_EPS <= u < hi + oracle.NEAR_EPS, (b, kg, v, lo, u, hi)
+
+
 def compare_sampling(inp: synth.Inputs, got: dict, ref: dict) -> dict:
     flags = ref["flags"]
     inv = (flags & oracle.INVALID_ANY) != 0
@@ -91,6 +137,9 @@ def compare_sampling(inp: synth.Inputs, got: dict, ref: dict) -> dict:
     assert not bad.any(), (f"{int(bad.sum())} mismatching requests, e.g. b={int(np.argmax(bad))}: "
                            f"gpu {got['tokens'][bad][0]} n={got['n'][bad][0]} vs oracle "
                            f"{ref['tokens'][bad][0]} n={ref['n'][bad][0]}")
+    # a flagged request that differs must still be a valid draw
+    for b in np.flatnonzero(~inv & near & ~same):
+        check_valid_draw(inp, got, ref, int(b))
     ok = ~inv
     if inp.gamma > 0 and ok.any():
         for j, key in ((0, "pt"), (1, "pd")):

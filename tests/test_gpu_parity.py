@@ -5,8 +5,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import (DEV, compare_greedy, compare_sampling, oracle_sampling, run_greedy,
-                      run_sampling, to_dev)
+from gpu_util import (DEV, check_valid_draw, compare_greedy, compare_sampling, oracle_sampling,
+                      run_greedy, run_sampling, to_dev)
 from speculative_decoding_verification_09_gb300 import binding, synth
 
 pytestmark = pytest.mark.gpu
@@ -38,6 +38,16 @@ def _gpu_tail() -> int:
 NEAR_LOG = []
 
 
+def assert_same_or_valid(inp, got, ref):
+    """Tokens and counts as the oracle's, or, at a flagged near-tie, a draw
+    the rule allows within the 1e-6 window (check_valid_draw)."""
+    near = (ref["flags"] & oracle.NEAR_ANY) != 0
+    same = np.all(got["tokens"] == ref["tokens"], axis=1) & (got["n"] == ref["n"])
+    assert np.all(same | near), np.argwhere(~(same | near)).ravel()
+    for b in np.flatnonzero(~same):
+        check_valid_draw(inp, got, ref, int(b))
+
+
 # ------------------------------------------------------------ small sweeps
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -48,6 +58,7 @@ def test_small_sweep(V, gamma, dtype):
     inp = synth.make_inputs(cfg, seed=1000 + V * 7 + gamma)
     stats = compare_sampling(inp, run_sampling(inp), oracle_sampling(inp))
     NEAR_LOG.append(stats)
+    assert stats["mismatches"] <= max(1.0, 1e-4 * stats["positions"])
 
 
 @pytest.mark.parametrize("kind", ["normal", "zipf", "mix"])
@@ -180,9 +191,11 @@ def test_near_identical_rows():
     inp = synth.make_inputs(cfg, seed=9)
     inp.u_acc[:] = 0.999999
     got, ref = run_sampling(inp), oracle_sampling(inp)
-    compare_sampling(inp, got, ref)
+    stats = compare_sampling(inp, got, ref)
+    print(f"\nnear-identical rows: {stats}")
     ok = (ref["flags"] & oracle.INVALID_ANY) == 0
     assert np.all((got["tokens"][ok] >= -1) & (got["tokens"][ok] < inp.V))
+    assert stats["mismatches"] <= max(1.0, 1e-4 * stats["positions"])
 
 
 def test_empty_batch_is_a_noop():
@@ -243,9 +256,7 @@ def test_overlapping_calls_on_three_streams():
         got = dict(tokens=o["tok"].cpu().numpy(), n=o["n"].cpu().numpy(),
                    p=np.zeros((x.B, x.gamma, 2), np.float32), Z=np.zeros(x.B, np.float32),
                    status=int(o["st"].item()))
-        near = (ref["flags"] & oracle.NEAR_ANY) != 0
-        same = np.all(got["tokens"] == ref["tokens"], axis=1) & (got["n"] == ref["n"])
-        assert np.all(same | near), np.argwhere(~(same | near)).ravel()
+        assert_same_or_valid(x, got, ref)
         assert got["status"] == 0
 
 
@@ -282,6 +293,27 @@ def test_poisoned_task_counter_is_detected_and_repaired():
     bad = run_sampling(inp, d, ws)
     assert bad["status"] & binding.SV_ST_WORKSPACE
     compare_sampling(inp, run_sampling(inp, d, ws), ref)
+
+
+def test_small_calls_in_a_loop_report_no_workspace_error():
+    """Many back-to-back calls of the smallest workload (one request of
+    V = 32000: about one reduce task per CTA, so every CTA reaches the pool
+    claims at its first chunk) on one workspace: none may report
+    SV_ST_WORKSPACE (the ready-state check must not race with the claims of
+    the call's own CTAs), and every call gives the oracle's tokens."""
+    inp = synth.make_inputs(1)
+    d = to_dev(inp)
+    ws = binding.make_workspace(inp.B, inp.gamma, inp.V, DEV)
+    ref = oracle_sampling(inp)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tok = torch.full((inp.B, inp.gamma + 1), -7, dtype=torch.int32, device=DEV)
+    n = torch.full((inp.B,), -7, dtype=torch.int32, device=DEV)
+    for _ in range(300):
+        binding.spec_verify(d["Lt"], d["Ld"], d["x"], d["u_acc"], d["u_res"], d["temp"], tok, n,
+                            ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert_same_or_valid(inp, dict(tokens=tok.cpu().numpy(), n=n.cpu().numpy()), ref)
 
 
 def test_bounded_wait_reports_timeout_and_context_recovers():
@@ -415,7 +447,5 @@ def test_cuda_graph_capture_and_replay():
                    p=np.zeros((B, g, 2), np.float32), Z=np.zeros(B, np.float32),
                    status=int(st.item()))
         ref = oracle_sampling(inp)
-        near = (ref["flags"] & oracle.NEAR_ANY) != 0
-        same = np.all(got["tokens"] == ref["tokens"], axis=1) & (got["n"] == ref["n"])
-        assert np.all(same | near), np.argwhere(~(same | near)).ravel()
+        assert_same_or_valid(inp, got, ref)
         assert got["status"] == 0
