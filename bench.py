@@ -99,7 +99,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -165,14 +165,41 @@ def job_throughput(units_per_rank_step: int, world: int, steps: int, total_ms: f
     return units_per_rank_step * world * steps / (total_ms / 1e3)
 
 
-def oracle_positions_per_s(inp: synth.Inputs, n_req: int, threads: int) -> tuple[float, float]:
+def oracle_positions_per_s(inp: synth.Inputs, n_req: int, threads: int,
+                           keep: list | None = None) -> tuple[float, float]:
+    """Time the oracle on the first n_req requests (the cpu_baseline leg);
+    its result is appended to `keep` when given."""
     import oracle
     sl = slice(0, n_req)
     t0 = time.perf_counter()
-    oracle.verify(inp.Lt[sl], inp.Ld[sl], inp.x[sl], inp.u_acc[sl], inp.u_res[sl],
-                  inp.temp[sl], inp.dtype, nthreads=threads)
+    ref = oracle.verify(inp.Lt[sl], inp.Ld[sl], inp.x[sl], inp.u_acc[sl], inp.u_res[sl],
+                        inp.temp[sl], inp.dtype, nthreads=threads)
     dt = time.perf_counter() - t0
+    if keep is not None:
+        keep.append(ref)
     return n_req * inp.gamma / dt, dt
+
+
+def parity_counts(inp: synth.Inputs, tokens: np.ndarray, n: np.ndarray, ref: dict,
+                  greedy: bool) -> dict:
+    """The GPU's outputs for the first requests of an input set against the
+    oracle's (computed in the cpu_baseline leg): flagged near-ties (accept
+    tests within 1e-6 of u, draws within 1e-6 of a CDF edge, vanished
+    residuals), requests that differ, and those that differ without a flag."""
+    import oracle
+    B = tokens.shape[0]
+    flags = ref["flags"][:B]
+    same = np.all(tokens == ref["tokens"][:B], axis=1) & (n == ref["n"][:B])
+    inv = (flags & oracle.INVALID_ANY) != 0
+    near = (flags & oracle.NEAR_ANY) != 0
+    near_pos = 0 if greedy else int(((flags & oracle.NEAR_ACCEPT) != 0).sum()
+                                    + ((flags & oracle.NEAR_SAMPLE) != 0).sum()
+                                    + ((flags & oracle.DEGENERATE) != 0).sum())
+    return {"requests": int(B), "positions": int(B * inp.gamma), "near_ties": near_pos,
+            "near_tie_requests": int(near.sum()),
+            "near_tie_rate": near_pos / max(1, B * inp.gamma),
+            "mismatches": int((~inv & ~same).sum()),
+            "unflagged_mismatches": int((~inv & ~same & ~near).sum())}
 
 
 def run_reference(args) -> None:
@@ -440,6 +467,93 @@ def measure_tree_side(binding, torch, dev, stream, steps, warmup, peak, sets=3) 
             "status": int(st.item())}
 
 
+def dev_tensors(torch, dev, inp: synth.Inputs) -> dict:
+    t = {k: torch.from_numpy(np.ascontiguousarray(getattr(inp, k))).to(dev)
+         for k in ("Lt", "Ld", "x", "u_acc", "u_res", "temp")}
+    if inp.dtype == synth.BF16:
+        t["Lt"], t["Ld"] = t["Lt"].view(torch.bfloat16), t["Ld"].view(torch.bfloat16)
+    return t
+
+
+def call_stats(ms: np.ndarray) -> dict:
+    return {"median": float(np.median(ms)), "p10": float(np.percentile(ms, 10)),
+            "p90": float(np.percentile(ms, 90)), "calls": int(ms.size)}
+
+
+def measure_workload(binding, torch, dev, stream, cid: int, steps: int, warmup: int, peak: float,
+                     sets: int = 3, parity_requests: int = 256) -> tuple[dict, dict]:
+    """Another workload at its own size, measured in the same run as the
+    headline: `steps` calls back to back between two events (call_ms), the
+    reduce kernel alone with an event on each side (reduce_ms), and per-call
+    times of max(steps, 50) calls each between its own two events; `sets`
+    input sets rotate.  Also returns the outputs for the first requests of
+    input set 0, for the parity count of the cpu_baseline leg."""
+    cfg = synth.CONFIGS[cid]
+    B, g, V = cfg["B"], cfg["gamma"], cfg["V"]
+    greedy = cfg["kind"] == "greedy"
+    host = [synth.make_inputs(cid, set_index=s) for s in range(sets)]
+    lb = host[0].Lt.nbytes if greedy else host[0].logit_bytes
+    ds = [dev_tensors(torch, dev, h) for h in host]
+    ws = binding.make_workspace(B, g, V, dev)
+    tok = torch.empty(B, g + 1, dtype=torch.int32, device=dev)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(t):
+        if greedy:
+            binding.spec_verify_greedy(t["Lt"], t["x"], tok, n, ws, st, stream)
+        else:
+            binding.spec_verify(t["Lt"], t["Ld"], t["x"], t["u_acc"], t["u_res"], t["temp"], tok,
+                                n, ws, st, stream)
+
+    for i in range(max(3, warmup)):
+        step(ds[i % sets])
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        step(ds[i % sets])
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    call_ms = a.elapsed_time(b) / steps
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for es in kev:  # torch creates an event on its first record
+        for e in es:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    for i, es in enumerate(kev):
+        binding.sv_set_stage_events(es)
+        step(ds[i % sets])
+    binding.sv_set_stage_events([])
+    torch.cuda.synchronize(dev)
+    reduce_ms = float(np.mean([es[0].elapsed_time(es[1]) for es in kev]))
+    nl = max(steps, 50)
+    lev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nl)]
+    for i, (e0, e1) in enumerate(lev):
+        e0.record(stream)
+        step(ds[i % sets])
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    lat = np.array([e0.elapsed_time(e1) for e0, e1 in lev])
+    status = int(st.item())
+    step(ds[0])
+    torch.cuda.synchronize(dev)
+    k = min(B, parity_requests)
+    out = dict(inp=host[0], tokens=tok[:k].cpu().numpy(), n=n[:k].cpu().numpy(), greedy=greedy)
+    res = {"workload": cfg["name"], "B": B, "gamma": g, "V": V, "greedy": greedy,
+           "dtype": cfg["dtype"], "logit_bytes": int(lb), "call_ms": call_ms,
+           "positions_per_s": B * g / (call_ms / 1e3), "call_gbs": lb / (call_ms / 1e3) / 1e9,
+           "call_frac_of_peak": lb / (call_ms / 1e3) / 1e9 / peak, "reduce_ms": reduce_ms,
+           "reduce_frac_of_peak": lb / (reduce_ms / 1e3) / 1e9 / peak,
+           "per_call_ms": call_stats(lat), "status": status,
+           "timing": f"{steps} calls back to back between two events; reduce with an event "
+                     f"on each side; {nl} calls each between its own events; "
+                     f"{sets} input sets rotating"}
+    del ds, ws
+    return res, out
+
+
 def run_tree_only(args) -> None:
     """Token-tree verification alone (for profiling captures): one JSON dict."""
     import torch
@@ -480,14 +594,7 @@ def run_ours(args) -> None:
                  for s in range(args.sets)]
     logit_bytes = host_sets[0].Lt.nbytes if greedy else host_sets[0].logit_bytes
 
-    def dev_tensors(inp):
-        t = {k: torch.from_numpy(np.ascontiguousarray(getattr(inp, k))).to(dev)
-             for k in ("Lt", "Ld", "x", "u_acc", "u_res", "temp")}
-        if inp.dtype == synth.BF16:
-            t["Lt"], t["Ld"] = t["Lt"].view(torch.bfloat16), t["Ld"].view(torch.bfloat16)
-        return t
-
-    sets = [dev_tensors(h) for h in host_sets]
+    sets = [dev_tensors(torch, dev, h) for h in host_sets]
     out_tok = torch.empty(B, g + 1, dtype=torch.int32, device=dev)
     out_n = torch.empty(B, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -509,9 +616,19 @@ def run_ours(args) -> None:
     if pg:
         pg.barrier()
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
+
+    def soak(seconds):  # back-to-back calls of the same workload (clocks under load)
+        t_end = time.perf_counter() + seconds
+        i = 0
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                step(sets[i % len(sets)])
+                i += 1
+            torch.cuda.synchronize(dev)
+
     if not args.no_clocks:
         clocks.start()
-        time.sleep(0.3)
+        soak(0.3)
     # two events around the K back-to-back steps (an event between two calls
     # would keep the next call's first kernel from being placed early)
     ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -567,7 +684,7 @@ def run_ours(args) -> None:
     # single-call latency distribution: K more calls, each bracketed by its
     # own events (which keep calls from overlapping, unlike the timed loop)
     lev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+           for _ in range(max(args.steps, 50))]
     for i, (a_, b_) in enumerate(lev):
         a_.record(stream)
         step(sets[i % len(sets)])
@@ -576,7 +693,13 @@ def run_ours(args) -> None:
     lat = np.array([a_.elapsed_time(b_) for a_, b_ in lev])
     latency_ms = {"p10": float(np.percentile(lat, 10)), "p50": float(np.percentile(lat, 50)),
                   "p90": float(np.percentile(lat, 90)), "calls": int(lat.size)}
+    if not args.no_clocks:
+        soak(0.1)
     clk = clocks.stop() if not args.no_clocks else None
+    if clk is not None:
+        clk["window"] = ("0.3 s of back-to-back calls of the same workload before the timed "
+                         "steps, the timed steps, the stage and per-call timings, 0.1 s of "
+                         "calls after; samples every 20 ms")
     total_ms = ev_a.elapsed_time(ev_b)
     peak, peak_kind = read_peaks()
     multi_stream = None if args.no_multi_stream else measure_streams(
@@ -663,19 +786,64 @@ def run_ours(args) -> None:
                "path": "pinned host inputs copied in chunks of requests on a copy stream, "
                        "each chunk verified as it lands, results copied back"}
 
-    cpu = None
+    # the other workloads at their own sizes, after the headline (one GPU)
+    workloads, wl_out = None, {}
+    if rank == 0 and ws_n == 1 and not args.no_workloads and not args.batch:
+        workloads = {}
+        for c2 in sorted(synth.CONFIGS):
+            if c2 == cid:
+                continue
+            res, out = measure_workload(binding, torch, dev, stream, c2, args.steps, args.warmup,
+                                        peak)
+            workloads[f"c{c2}"] = res
+            wl_out[f"c{c2}"] = out
+            torch.cuda.empty_cache()
+
+    # the headline's outputs for the first requests of input set 0 (parity count)
+    n_req = min(B, args.cpu_requests)
+    step(sets[0])
+    torch.cuda.synchronize(dev)
+    head_tok, head_n = out_tok[:n_req].cpu().numpy(), out_n[:n_req].cpu().numpy()
+
+    cpu, parity = None, None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        import oracle
         cores = os.cpu_count() or 1
-        n_req = min(B, args.cpu_requests)
         # repeat the bounded sample until about cpu_seconds of work were timed
-        passes, dt = 0, 0.0
+        passes, dt, keep = 0, 0.0, []
         while passes == 0 or dt < args.cpu_seconds:
-            dt += oracle_positions_per_s(host_sets[0], n_req, cores)[1]
+            dt += oracle_positions_per_s(host_sets[0], n_req, cores, keep if passes == 0 else None)[1]
             passes += 1
         v = passes * n_req * g / dt
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"first {n_req} of {B} requests of {cfg['name']} (set 0), fp64, "
                          f"{cores} threads, {passes} passes, {dt:.1f} s wall"}
+        # the GPU's outputs against the oracle's on the same requests: flagged
+        # near-ties and differing requests, headline and the other workloads
+        h0 = host_sets[0]
+        if greedy:
+            keep = [oracle.greedy(h0.Lt[:n_req], h0.x[:n_req], h0.dtype)]
+        parity = {cfg["name"]: parity_counts(h0, head_tok, head_n, keep[0], greedy)}
+        for key, o in wl_out.items():
+            inp, k = o["inp"], o["tokens"].shape[0]
+            if o["greedy"]:
+                ref = oracle.greedy(inp.Lt[:k], inp.x[:k], inp.dtype)
+            else:
+                ref = oracle.verify(inp.Lt[:k], inp.Ld[:k], inp.x[:k], inp.u_acc[:k],
+                                    inp.u_res[:k], inp.temp[:k], inp.dtype, nthreads=cores)
+            parity[synth.CONFIGS[int(key[1:])]["name"]] = parity_counts(inp, o["tokens"], o["n"],
+                                                                          ref, o["greedy"])
+        tot_pos = sum(p_["positions"] for p_ in parity.values())
+        parity["all"] = {"positions": tot_pos,
+                         "near_ties": sum(p_["near_ties"] for p_ in parity.values()),
+                         "mismatches": sum(p_["mismatches"] for p_ in parity.values()),
+                         "unflagged_mismatches": sum(p_["unflagged_mismatches"]
+                                                     for p_ in parity.values())}
+        parity["rule"] = ("GPU outputs vs the fp64 oracle on the first requests of input set 0 "
+                          "of each workload (the cpu_baseline leg's own oracle runs); near_ties "
+                          "counts accept tests within 1e-6 of u, draws within 1e-6 of a CDF "
+                          "edge and vanished residuals; a mismatch is a request whose tokens "
+                          "or count differ")
 
     if rank != 0:
         return
@@ -699,6 +867,8 @@ def run_ours(args) -> None:
                                "right after the timed loop (same inputs)"},
         "stages_ms_extra_calls": stage_ms, "call_ms": launch_ms,
         "single_call_latency_ms": latency_ms,
+        "per_call_ms": dict(call_stats(lat), mean_of_timed_loop=launch_ms),
+        "workloads": workloads, "parity": parity,
         "call_equivalent_gbs": logit_bytes / (launch_ms / 1e3) / 1e9,
         "concurrent_calls": multi_stream,
         "draft_side": draft_side, "kv_side": kv_side, "tree_side": tree_side,
@@ -732,6 +902,8 @@ def main():
                     help="skip timing the KV commit, valid slots and block-table window")
     ap.add_argument("--no-multi-stream", action="store_true",
                     help="skip timing calls that alternate over several streams")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip measuring the other workloads after the headline")
     ap.add_argument("--no-tree-side", action="store_true",
                     help="skip timing token-tree verification")
     ap.add_argument("--tree-only", action="store_true",
