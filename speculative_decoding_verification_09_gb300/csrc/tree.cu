@@ -258,6 +258,11 @@ struct Part {  // one warp's share of a pass
   float pad;
 };
 
+// Entries of the segment arrays: the combines give lane l segments 4 l ..
+// 4 l + 3 of the at most TW * TMAXC segments, and write all 4 * 32.
+constexpr int SEG_SLOTS = 4 * 32;
+static_assert(TW * TMAXC <= SEG_SLOTS, "every segment has an entry");
+
 struct TreeSmem {
   int32_t parent[SV_TREE_MAX_N];
   int32_t token[SV_TREE_MAX_N];
@@ -268,8 +273,10 @@ struct TreeSmem {
   float ua[SV_TREE_MAX_N];    // accept uniform of each child of the current node
   float ur;                   // residual uniform of the current node
   Part part[2][2][TW];    // [buffer][target, draft][warp], alternating per pass
-  FF seg_incl[TW * TMAXC];  // running mass after each segment (index order)
-  FF seg_tot[TW * TMAXC];
+  // running mass after each segment (index order), and each segment's mass;
+  // the combines write 4 entries per lane of a warp, whatever the segment count
+  FF seg_incl[SEG_SLOTS];
+  FF seg_tot[SEG_SLOTS];
   FF piece[TW];
   float mt, md;
   FF St, Sd, Z;
