@@ -868,17 +868,18 @@ __device__ float4 reduce_share_argmax(const uint4 (&vec)[G::MAXV], const unsigne
 // relative precision where the rows nearly agree (no cancellation).  delta is
 // clamped to <= 0 (weight 0, also for NaN); 1 - 2^delta is 1 - ex2(delta)
 // where that loses little (delta < -1/2: ex2's relative error 2^-22 grows by
-// at most 2^delta / (1 - 2^delta) < 2.5), else its Taylor series in delta,
-// sum_{n=1..6} -(ln 2)^n / n! * delta^n (truncation below 4e-7 relative).
+// at most 2^delta / (1 - 2^delta) < 2.5), else delta * p(delta) with p the
+// degree-4 minimax fit (Remez exchange, relative error) of (1 - 2^delta) /
+// delta on [-1/2, 0]: 1.3e-8 relative in exact arithmetic, 1.3e-7 as
+// evaluated here in fp32 (fit_one_minus_exp2.py recomputes both).
 // The exponent (l_t - m_t) * kf is formed as one fma with -m_t * kf rounded
 // once per row: a common factor of all the row's weights.  weight() and
 // vec_weights() perform the same fp32 operations per element.
-constexpr float OMC1 = -0.69314718055994531f, OMC2 = -0.24022650695910071f,
-                OMC3 = -0.055504108664821580f, OMC4 = -0.0096181291076284772f,
-                OMC5 = -0.0013333558146428443f, OMC6 = -1.5403530393381609e-4f;
+constexpr float OMC1 = -0.69314717173667928f, OMC2 = -0.24022564279246794f,
+                OMC3 = -0.055490406445877882f, OMC4 = -0.0095412810839257713f,
+                OMC5 = -0.0011544522739422426f;
 __device__ __forceinline__ float one_minus_exp2(float delta) {
-  float p = OMC6;
-  p = fmaf(p, delta, OMC5);
+  float p = OMC5;
   p = fmaf(p, delta, OMC4);
   p = fmaf(p, delta, OMC3);
   p = fmaf(p, delta, OMC2);
@@ -904,30 +905,29 @@ __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigne
   return r;
 }
 
-// Weights of one 16-byte vector of target values `t` and draft values `dv`,
-// summed; the same operations as weight() on packed fp32 pairs.
-template <int DT>
-__device__ __forceinline__ float vec_weights(const Record& r, const uint4& t, const uint4& dv,
-                                             bool two) {
+// Weights of one 16-byte vector of target values `t` and draft values `dv`
+// (TWO: after a rejection), added to the packed pair sum `acc`; the same
+// operations as weight() on packed fp32 pairs.
+template <int DT, bool TWO>
+__device__ __forceinline__ void vec_weights_acc(const Record& r, const uint4& t, const uint4& dv,
+                                                unsigned long long& acc) {
   using E = Elem<DT>;
   const float c1 = -(r.mt * r.kf);
   const unsigned long long cc = pk2(c1, c1), kk = pk2(r.kf, r.kf);
-  unsigned long long acc = pk2(0.f, 0.f);
 #pragma unroll
   for (int q = 0; q < E::PAIRS; ++q) {
     const unsigned long long lt = E::pair(t, q);
     float a, b;
     upk2(fma2(lt, kk, cc), a, b);
     const unsigned long long et = pk2(ex2(a), ex2(b));
-    if (two) {
+    if (TWO) {
       const unsigned long long ch = pk2(r.c0_hi, r.c0_hi), cl = pk2(r.c0_lo, r.c0_lo);
       float d0, d1;
       upk2(add2(fma2(sub2(E::pair(dv, q), lt), kk, ch), cl), d0, d1);
       d0 = fminf(d0, 0.f);
       d1 = fminf(d1, 0.f);
       const unsigned long long dd = pk2(d0, d1);
-      unsigned long long p = pk2(OMC6, OMC6);
-      p = fma2(p, dd, pk2(OMC5, OMC5));
+      unsigned long long p = pk2(OMC5, OMC5);
       p = fma2(p, dd, pk2(OMC4, OMC4));
       p = fma2(p, dd, pk2(OMC3, OMC3));
       p = fma2(p, dd, pk2(OMC2, OMC2));
@@ -941,6 +941,16 @@ __device__ __forceinline__ float vec_weights(const Record& r, const uint4& t, co
       acc = add2(acc, et);
     }
   }
+}
+// The same, summed on their own.
+template <int DT>
+__device__ __forceinline__ float vec_weights(const Record& r, const uint4& t, const uint4& dv,
+                                             bool two) {
+  unsigned long long acc = pk2(0.f, 0.f);
+  if (two)
+    vec_weights_acc<DT, true>(r, t, dv, acc);
+  else
+    vec_weights_acc<DT, false>(r, t, dv, acc);
   float a, b;
   upk2(acc, a, b);
   return a + b;
@@ -1593,16 +1603,40 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
 
 // ------------------------------------------------------------ residual
 
+// Weights of vectors [0, nv) of a target span `tv` (and draft span `dv` when
+// TWO) read from global memory, PV per lane in flight, summed in packed pairs.
+template <int DT, int PV, bool TWO>
+__device__ __forceinline__ float global_vectors_mass(const Record& r, const uint4* tv,
+                                                  const uint4* dv, int nv, int lane) {
+  using E = Elem<DT>;
+  const uint4 neg = make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD);
+  unsigned long long acc = pk2(0.f, 0.f);
+  for (int v0 = 0; v0 < nv; v0 += 32 * PV) {
+    uint4 vt[PV], vd[TWO ? PV : 1];
+#pragma unroll
+    for (int u = 0; u < PV; ++u) {
+      const int j = v0 + lane + 32 * u;
+      vt[u] = j < nv ? __ldg(tv + j) : neg;
+      if (TWO) vd[u] = j < nv ? __ldg(dv + j) : neg;
+    }
+#pragma unroll
+    for (int u = 0; u < PV; ++u) vec_weights_acc<DT, TWO>(r, vt[u], TWO ? vd[u] : vt[u], acc);
+  }
+  float a, b;
+  upk2(acc, a, b);
+  return a + b;
+}
+
 // Mass of elements [lo, hi) of the row token k is drawn from: target row
 // `trow` and (after a rejection) draft row `drow`; one warp, fp32 weights,
 // lane sums added as float pairs.  Aligned spans are read as 16-byte vectors,
-// PV per lane in flight.
-template <int DT>
+// PV per lane in flight.  TARGET_ONLY: the caller passes no draft row.
+template <int DT, bool TARGET_ONLY = false>
 __device__ void span_mass(const Record& r, const unsigned char* trow, const unsigned char* drow,
                           int lo, int hi, float& mh, float& ml) {
   using E = Elem<DT>;
   const int lane = threadIdx.x & 31;
-  const bool two = (r.mode == MODE_REJECT);
+  const bool two = !TARGET_ONLY && (r.mode == MODE_REJECT);
   float acc = 0.f;
   int e_tail = lo;
   const unsigned char* t0 = trow + size_t(lo) * E::ES;
@@ -1612,19 +1646,8 @@ __device__ void span_mass(const Record& r, const unsigned char* trow, const unsi
     const int nv = (hi - lo) / E::VEC;
     const uint4* tv = reinterpret_cast<const uint4*>(t0);
     const uint4* dv = reinterpret_cast<const uint4*>(d0);
-    for (int v0 = 0; v0 < nv; v0 += 32 * PV) {
-      uint4 vt[PV], vd[PV];
-#pragma unroll
-      for (int u = 0; u < PV; ++u) {
-        const int j = v0 + lane + 32 * u;
-        const uint4 neg = make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD,
-                                     E::NEG_INF_WORD);
-        vt[u] = j < nv ? __ldg(tv + j) : neg;
-        vd[u] = (two && j < nv) ? __ldg(dv + j) : vt[u];
-      }
-#pragma unroll
-      for (int u = 0; u < PV; ++u) acc += vec_weights<DT>(r, vt[u], vd[u], two);
-    }
+    acc = two ? global_vectors_mass<DT, PV, true>(r, tv, dv, nv, lane)
+              : global_vectors_mass<DT, PV, false>(r, tv, dv, nv, lane);
     e_tail = lo + nv * E::VEC;
   }
   for (int e = e_tail + lane; e < hi; e += 32)
@@ -1699,6 +1722,50 @@ __device__ void producer_res(const Params& P, SmemCtl<GeoResidual>& C, unsigned 
   end_markers(P, C, seq);
 }
 
+// Weights of this warp's whole vectors [j0, vhi) of a slot (target body at
+// tv, draft body at dv when TWO), summed in packed pairs: PV vectors per lane
+// are copied into registers and the slot handed back (`release`) before the
+// arithmetic.  The first PV - 1 rounds are read without a bounds test when
+// every lane has a vector in each of them (all but the rows' last chunks);
+// vectors past vhi read as -inf (weight 0).
+template <int DT, int PV, bool TWO, typename Release>
+__device__ __forceinline__ float slot_vectors_mass(const Record& r, const uint4* tv,
+                                                   const uint4* dv, int j0, int vhi, int lane,
+                                                   Release release) {
+  using E = Elem<DT>;
+  const uint4 neg = make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD);
+  uint4 vt[PV], vd[TWO ? PV : 1];
+  if (vhi - j0 >= 32 * (PV - 1)) {
+#pragma unroll
+    for (int u = 0; u < PV - 1; ++u) {
+      const int j = j0 + lane + 32 * u;
+      vt[u] = tv[j];
+      if (TWO) vd[u] = dv[j];
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < PV - 1; ++u) {
+      const int j = j0 + lane + 32 * u;
+      vt[u] = j < vhi ? tv[j] : neg;
+      if (TWO) vd[u] = j < vhi ? dv[j] : neg;
+    }
+  }
+  {
+    const int j = j0 + lane + 32 * (PV - 1);
+    vt[PV - 1] = j < vhi ? tv[j] : neg;
+    if (TWO) vd[PV - 1] = j < vhi ? dv[j] : neg;
+  }
+  unsigned long long acc = pk2(0.f, 0.f);
+  for (int j = j0 + lane + 32 * PV; j < vhi; j += 32)  // only if sub exceeds 32*PV vectors
+    vec_weights_acc<DT, TWO>(r, tv[j], TWO ? dv[j] : tv[j], acc);
+  release();
+#pragma unroll
+  for (int u = 0; u < PV; ++u) vec_weights_acc<DT, TWO>(r, vt[u], TWO ? vd[u] : vt[u], acc);
+  float a, b;
+  upk2(acc, a, b);
+  return a + b;
+}
+
 // Mass of this warp's contiguous sub-range [cw*sub, (cw+1)*sub) of a
 // phase-2 chunk held in a slot (target body at +0, draft body at +HALF),
 // returned as a float pair (hi, lo) valid in every lane.  ALIGNED: every row
@@ -1726,19 +1793,8 @@ __device__ float2 warp_slot_mass(const Params& P, const Desc& d, const Record& r
       const uint4* tv = reinterpret_cast<const uint4*>(slot);
       const uint4* dv = reinterpret_cast<const uint4*>(slot + HALF);
       const int j0 = lo / E::VEC, vhi = min(hi, d.nb_t) / E::VEC;
-      uint4 vt[PV], vd[PV];
-#pragma unroll
-      for (int u = 0; u < PV; ++u) {
-        const int j = j0 + lane + 32 * u;
-        vt[u] = j < vhi ? tv[j] : make_uint4(E::NEG_INF_WORD, E::NEG_INF_WORD, E::NEG_INF_WORD,
-                                             E::NEG_INF_WORD);
-        vd[u] = (two && j < vhi) ? dv[j] : vt[u];
-      }
-      for (int j = j0 + lane + 32 * PV; j < vhi; j += 32)  // only if sub exceeds 32*PV vectors
-        acc += vec_weights<DT>(r, tv[j], two ? dv[j] : tv[j], two);
-      release();
-#pragma unroll
-      for (int u = 0; u < PV; ++u) acc += vec_weights<DT>(r, vt[u], vd[u], two);
+      acc = two ? slot_vectors_mass<DT, PV, true>(r, tv, dv, j0, vhi, lane, release)
+                : slot_vectors_mass<DT, PV, false>(r, tv, dv, j0, vhi, lane, release);
       for (int e = max(lo, d.nb_t) + lane; e < hi; e += 32)
         acc += weight(r, E::load(trow, e), two ? E::load(drow, e) : 0.f);
     } else if constexpr (!ALIGNED) {
@@ -1961,7 +2017,7 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
     for (int j = 0; j < DRAW_RUN; ++j) mq[j] = ff(0.f);
     for (int q = qa; q < qb; ++q) {
       float h = 0.f, l = 0.f;
-      if (sub_lo(q) < sub_hi(q)) span_mass<DT>(r, trow, nullptr, sub_lo(q), sub_hi(q), h, l);
+      if (sub_lo(q) < sub_hi(q)) span_mass<DT, true>(r, trow, nullptr, sub_lo(q), sub_hi(q), h, l);
       const int j = (q - qa) >> 5;
       if (lane == ((q - qa) & 31) && j < DRAW_RUN) mq[j] = ff(h, l);
       if (lane == 0) tot = tot + ff(h, l);
@@ -2014,7 +2070,7 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
           const int qq = qa + L + 32 * j;
           float hh = 0.f, hl = 0.f;
           if (qq < qb && sub_lo(qq) < sub_hi(qq))
-            span_mass<DT>(r, trow, nullptr, sub_lo(qq), sub_hi(qq), hh, hl);
+            span_mass<DT, true>(r, trow, nullptr, sub_lo(qq), sub_hi(qq), hh, hl);
           if (lane == L) z = ff(hh, hl);
         }
       }
