@@ -284,6 +284,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
       : "memory");
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// The 16-byte-aligned interior of [p, p + bytes) into L2 (nothing outside it).
+__device__ __forceinline__ void prefetch_span_l2(const unsigned char* p, size_t bytes) {
+  const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 15u) & ~uintptr_t(15);
+  const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + bytes) & ~uintptr_t(15);
+  if (e > a) prefetch_l2(reinterpret_cast<const void*>(a), unsigned(e - a));
+}
+
 // Programmatic dependent launch: the next kernel of the call may be launched
 // (and run what does not read this kernel's outputs) before this one ends;
 // it waits for this kernel's completion, with its memory visible, before
@@ -1219,6 +1230,26 @@ __device__ void consumer(const Params& P, SmemCtl<GeoReduce>& C, const unsigned 
   }
 }
 
+// L2 prefetch of the chunks this CTA streams first (its ring's worth): the
+// row spans the producer will copy, from the call's parameters alone.
+template <int DT, bool GREEDY, bool PAIRS>
+__device__ void prefetch_first_chunks(const Params& P) {
+  using E = Elem<DT>;
+  const Split sp = reduce_split(P, blockIdx.x, gridDim.x);
+  const long long tend = min(sp.t1, sp.t0 + (long long)GeoReduce::NS * (PAIRS ? 2 : 1));
+  for (long long t = sp.t0; t < tend; ++t) {
+    const long long row = t / P.nch1;
+    const int c = int(t - row * P.nch1);
+    const int b = int(row / P.R), i = int(row - (long long)b * P.R);
+    if (b >= P.B) break;
+    const int e0 = c * P.ch1;
+    const size_t bytes = size_t(min(P.ch1, P.V - e0)) * E::ES;
+    prefetch_span_l2(P.Lt + ((size_t(b) * P.R + i) * size_t(P.V) + e0) * E::ES, bytes);
+    if (!GREEDY && i < P.gs)
+      prefetch_span_l2(P.Ld + ((size_t(b) * P.gamma + i) * size_t(P.V) + e0) * E::ES, bytes);
+  }
+}
+
 // GREEDY: chunk argmax instead of (max, sum); PAIRS: no draft rows are
 // streamed and a slot carries two target chunks (greedy verification, given
 // draft normalisers, draft sampling); CONTIG: the warps' shares are
@@ -1241,7 +1272,11 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
   }
   // launched programmatically after the previous kernel in the stream (the
   // last kernel of an earlier call, or whatever wrote the logits): nothing
-  // it wrote is read before it has completed
+  // it wrote is read before it has completed.  The first chunks of this
+  // CTA's range are only asked into L2 before that (a prefetch brings no
+  // data into the SM, and L2 is where every write lands), so the first
+  // copies after the wait need not go out to HBM.
+  if (threadIdx.x == 0) prefetch_first_chunks<DT, GREEDY, PAIRS>(P);
   wait_previous_kernel();
   if (threadIdx.x == 0) {
     // the workspace is in its ready state between calls; mark this call.
@@ -2201,10 +2236,6 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
 constexpr int FIN_WARPS = 16;
 constexpr int FIN_MAXC = 8;  // CTAs per cluster (the portable limit)
 
-// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
-__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
