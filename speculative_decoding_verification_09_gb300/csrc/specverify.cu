@@ -90,6 +90,7 @@ constexpr unsigned SUSPEND_HINT_NS = 1000000u;  // a waiting warp sleeps until t
 constexpr int SMS_CAP = 256;           // the chunk heuristic assumes at most this many SMs
 constexpr int MAXR = SV_MAX_GAMMA + 1;
 constexpr int DECIDE_WARPS = 16;       // decide: warps per request
+constexpr int DECIDE_WARPS_SMALL = 4;  // ... when R <= 4: a warp for every row, more CTAs per SM
 constexpr int DRAW_WARPS = 4;          // draw: warps per request
 constexpr int SAMPLE_WARPS = 4;        // draft sampling: warps per draft row
 constexpr float LOG2E_F = 1.4426950408889634f;
@@ -282,17 +283,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
-}
-
-// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
-__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-// The 16-byte-aligned interior of [p, p + bytes) into L2 (nothing outside it).
-__device__ __forceinline__ void prefetch_span_l2(const unsigned char* p, size_t bytes) {
-  const uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 15u) & ~uintptr_t(15);
-  const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + bytes) & ~uintptr_t(15);
-  if (e > a) prefetch_l2(reinterpret_cast<const void*>(a), unsigned(e - a));
 }
 
 // Programmatic dependent launch: the next kernel of the call may be launched
@@ -1230,26 +1220,6 @@ __device__ void consumer(const Params& P, SmemCtl<GeoReduce>& C, const unsigned 
   }
 }
 
-// L2 prefetch of the chunks this CTA streams first (its ring's worth): the
-// row spans the producer will copy, from the call's parameters alone.
-template <int DT, bool GREEDY, bool PAIRS>
-__device__ void prefetch_first_chunks(const Params& P) {
-  using E = Elem<DT>;
-  const Split sp = reduce_split(P, blockIdx.x, gridDim.x);
-  const long long tend = min(sp.t1, sp.t0 + (long long)GeoReduce::NS * (PAIRS ? 2 : 1));
-  for (long long t = sp.t0; t < tend; ++t) {
-    const long long row = t / P.nch1;
-    const int c = int(t - row * P.nch1);
-    const int b = int(row / P.R), i = int(row - (long long)b * P.R);
-    if (b >= P.B) break;
-    const int e0 = c * P.ch1;
-    const size_t bytes = size_t(min(P.ch1, P.V - e0)) * E::ES;
-    prefetch_span_l2(P.Lt + ((size_t(b) * P.R + i) * size_t(P.V) + e0) * E::ES, bytes);
-    if (!GREEDY && i < P.gs)
-      prefetch_span_l2(P.Ld + ((size_t(b) * P.gamma + i) * size_t(P.V) + e0) * E::ES, bytes);
-  }
-}
-
 // GREEDY: chunk argmax instead of (max, sum); PAIRS: no draft rows are
 // streamed and a slot carries two target chunks (greedy verification, given
 // draft normalisers, draft sampling); CONTIG: the warps' shares are
@@ -1272,11 +1242,7 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
   }
   // launched programmatically after the previous kernel in the stream (the
   // last kernel of an earlier call, or whatever wrote the logits): nothing
-  // it wrote is read before it has completed.  The first chunks of this
-  // CTA's range are only asked into L2 before that (a prefetch brings no
-  // data into the SM, and L2 is where every write lands), so the first
-  // copies after the wait need not go out to HBM.
-  if (threadIdx.x == 0) prefetch_first_chunks<DT, GREEDY, PAIRS>(P);
+  // it wrote is read before it has completed
   wait_previous_kernel();
   if (threadIdx.x == 0) {
     // the workspace is in its ready state between calls; mark this call.
@@ -1574,12 +1540,12 @@ __device__ void combine_rows(const Params& P, int b, float kf, const float2* dst
   }
 }
 
-// One CTA per request: DECIDE_WARPS warps combine the rows (row i by warp
-// i % DECIDE_WARPS), then warp 0 decides.  The draft tokens, their logits and
+// One CTA per request: NW warps combine the rows (row i by warp i % NW), then
+// warp 0 decides.  The draft tokens, their logits and
 // the uniforms are loaded by warp 0 before its rows; given draft normalisers
 // (dstats) replace the draft rows' combine.
-template <int DT, bool GREEDY>
-__global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, bool last) {
+template <int DT, bool GREEDY, int NW>
+__global__ void __launch_bounds__(32 * NW) sv_decide(const Params P, bool last) {
   __shared__ RowStat rows[MAXR];
   __shared__ Cand cand[MAXR];
   __shared__ float2 dst_sh[MAXR];
@@ -1600,7 +1566,7 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
   wait_previous_kernel();
   if (cached) __syncthreads();
   if (GREEDY) {
-    for (int i = warp; i < R; i += DECIDE_WARPS) {
+    for (int i = warp; i < R; i += NW) {
       const Partial* pp = P.part + (size_t(b) * R + i) * size_t(P.np1);
       float best;
       int bi, nan;
@@ -1614,7 +1580,7 @@ __global__ void __launch_bounds__(32 * DECIDE_WARPS) sv_decide(const Params P, b
       }
     }
   } else {
-    combine_rows<DECIDE_WARPS>(P, b, kf, dst_sh, rows);
+    combine_rows<NW>(P, b, kf, dst_sh, rows);
   }
   __syncthreads();
   if (GREEDY) {
@@ -2236,6 +2202,10 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
 constexpr int FIN_WARPS = 16;
 constexpr int FIN_MAXC = 8;  // CTAs per cluster (the portable limit)
 
+// Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -2891,8 +2861,8 @@ int launch(const Call& a) {
     const int per = min(FIN_MAXC, sms / B);
     if (g_tune.tail == 2 || (g_tune.tail == 0 && per >= 2)) fc = max(1, per);
   }
-  auto run = [&](auto reduce_k, auto decide_k, auto residual_k, auto draw_k, auto sample_k,
-                 auto finish_k) {
+  auto run = [&](auto reduce_k, auto decide_k, auto decide_small_k, auto residual_k, auto draw_k,
+                 auto sample_k, auto finish_k) {
     // programmatic launch: the reduce's CTAs may be placed while the previous
     // kernel in the stream finishes; it waits for that kernel on the device
     e = launch_after(reduce_k, grid, NTHR, smem_bytes<GeoReduce>(), st, P);
@@ -2910,8 +2880,12 @@ int launch(const Call& a) {
       mark(2);
       return;
     }
+    // one CTA per request; with at most four rows, four warps (a row each):
+    // smaller CTAs, more of them resident at large batches
     if (e == cudaSuccess)
-      e = launch_after(decide_k, unsigned(B), 32 * DECIDE_WARPS, 0, st, P, greedy);
+      e = R <= DECIDE_WARPS_SMALL
+              ? launch_after(decide_small_k, unsigned(B), 32 * DECIDE_WARPS_SMALL, 0, st, P, greedy)
+              : launch_after(decide_k, unsigned(B), 32 * DECIDE_WARPS, 0, st, P, greedy);
     mark(2);
     if (greedy) return;
     if (e == cudaSuccess) e = launch_after(residual_k, gres, NTHR, smem_bytes<GeoResidual>(), st, P);
@@ -2927,20 +2901,23 @@ int launch(const Call& a) {
                             (size_t(V) * ES) % 16 == 0;
   auto dispatch = [&](auto dt) {
     constexpr int D = decltype(dt)::value;
-    auto go = [&](auto reduce_k, auto decide_k) {
+    auto go = [&](auto reduce_k, auto greedy_c) {
+      constexpr bool GR = decltype(greedy_c)::value;
+      auto dk = sv_decide<D, GR, DECIDE_WARPS>;
+      auto dks = sv_decide<D, GR, DECIDE_WARPS_SMALL>;
       if (aligned_rows)
-        run(reduce_k, decide_k, sv_residual<D, true>, sv_draw<D>, sv_sample<D>, sv_finish<D>);
+        run(reduce_k, dk, dks, sv_residual<D, true>, sv_draw<D>, sv_sample<D>, sv_finish<D>);
       else
-        run(reduce_k, decide_k, sv_residual<D, false>, sv_draw<D>, sv_sample<D>, sv_finish<D>);
+        run(reduce_k, dk, dks, sv_residual<D, false>, sv_draw<D>, sv_sample<D>, sv_finish<D>);
     };
     if (greedy)
-      go(sv_reduce<D, true, true, false>, sv_decide<D, true>);
+      go(sv_reduce<D, true, true, false>, std::true_type());
     else if (draft)
-      go(sv_reduce<D, false, true, true>, sv_decide<D, false>);
+      go(sv_reduce<D, false, true, true>, std::false_type());
     else if (a.kind == CALL_CACHED)
-      go(sv_reduce<D, false, true, false>, sv_decide<D, false>);
+      go(sv_reduce<D, false, true, false>, std::false_type());
     else
-      go(sv_reduce<D, false, false, false>, sv_decide<D, false>);
+      go(sv_reduce<D, false, false, false>, std::false_type());
   };
   if (a.dtype == SV_F32)
     dispatch(std::integral_constant<int, SV_F32>());
