@@ -77,10 +77,20 @@ int sv_tree_verify(int dtype, const void* target_logits, const void* draft_logit
 
 /*
  * CTAs per request for sv_tree_verify (tuning and test aid): 0 (the
- * default) picks min(8, max(1, SMs / B)); 1..8 forces that size.
+ * default) picks min(8, max(1, k * SMs / B)) with k = 2 for CTAs of 8 warps
+ * and 1 for CTAs of 16 (sv_tree_set_warps); 1..8 forces that size.
  * Returns SV_OK or SV_ERR_INVALID_ARG.
  */
 int sv_tree_set_cluster(int ctas);
+
+/*
+ * Warps per CTA for sv_tree_verify (tuning and test aid): 0 (the default)
+ * takes 8 (two CTAs per SM) when 5 * B <= 4 * SMs and 16 (one CTA per SM)
+ * otherwise; 8 or 16 forces that width.  The results are those of the
+ * oracle either way (the rows' segment split, and so the rounding of the
+ * masses, differs).  Returns SV_OK or SV_ERR_INVALID_ARG.
+ */
+int sv_tree_set_warps(int warps);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,8 @@ EXPORTED = ("sv_workspace_bytes", "sv_workspace_init", "spec_verify", "spec_veri
             "sv_set_stage_events", "sv_set_tail", "sv_test_withhold_slot", "sv_error_string",
             "sv_version",
             "sv_kv_commit", "sv_kv_valid_slots", "sv_window_cols", "sv_window_block_table",
-            "sv_window_seq_lens_host", "sv_tree_verify", "sv_tree_set_cluster")
+            "sv_window_seq_lens_host", "sv_tree_verify", "sv_tree_set_cluster",
+            "sv_tree_set_warps")
 SV_TREE_MAX_N = 256
 SV_NOALLOC_MAX_WORKSPACE = 16 << 20
 
@@ -64,6 +65,7 @@ def lib() -> ctypes.CDLL:
         L.sv_window_seq_lens_host.argtypes = [P, I, I, I, I, P]
         L.sv_tree_verify.argtypes = [I, P, P, P, P, P, P, P, I, I, I, P, P, P, P, P]
         L.sv_tree_set_cluster.argtypes = [I]
+        L.sv_tree_set_warps.argtypes = [I]
         L.sv_set_tuning.argtypes = [I]
         L.sv_set_tail.argtypes = [I]
         L.sv_set_stage_events.argtypes = [P, I]
@@ -77,7 +79,7 @@ def lib() -> ctypes.CDLL:
                      "sv_test_withhold_slot",
                      "sv_kv_commit", "sv_kv_valid_slots", "sv_window_cols",
                      "sv_window_block_table", "sv_window_seq_lens_host", "sv_tree_verify",
-                     "sv_tree_set_cluster"):
+                     "sv_tree_set_cluster", "sv_tree_set_warps"):
             getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -381,3 +383,8 @@ def sv_tree_verify(target_logits, draft_logits, parent, tokens, u_accept, u_resi
 def sv_tree_set_cluster(ctas: int = 0) -> None:
     """CTAs per request for sv_tree_verify: 0 = automatic, 1..8 forced."""
     _check(lib().sv_tree_set_cluster(int(ctas)))
+
+
+def sv_tree_set_warps(warps: int = 0) -> None:
+    """Warps per CTA for sv_tree_verify: 0 = automatic, 8 or 16 forced."""
+    _check(lib().sv_tree_set_warps(int(warps)))

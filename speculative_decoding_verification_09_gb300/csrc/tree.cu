@@ -36,15 +36,17 @@ namespace cg = cooperative_groups;
 
 namespace {
 
-constexpr int TW = 16;            // warps per CTA
-constexpr int TTHR = 32 * TW;
+// Warps per CTA: 16 (one CTA per SM), or 8 (two per SM) where the batch
+// leaves room for two CTAs per SM (the kernel is a template on the width).
+constexpr int TW_MAX = 16, TW_MIN = 8;
 constexpr int TMAXC = 8;          // CTAs per cluster (the portable limit)
-static_assert(SV_TREE_MAX_N <= 32 * TW, "one child per thread at every node");
+static_assert(SV_TREE_MAX_N <= 32 * TW_MIN, "one child per thread at every node");
 constexpr int TU = 4;             // 16-byte vectors per lane and row in a batch
 constexpr int NS = 3;             // ring slots per warp
 constexpr int CHV = 32 * TU;      // 16-byte vectors of one row in a slot
 constexpr int CHB = CHV * 16;     // bytes of one row in a slot
-constexpr size_t RING_BYTES = size_t(TW) * NS * 2 * CHB;  // 192 KB of dynamic shared memory
+// dynamic shared memory of a CTA of tw warps: 192 KB per SM at either width
+constexpr size_t ring_bytes(int tw) { return size_t(tw) * NS * 2 * CHB; }
 constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;  // one second
 constexpr int RB = 8;             // elements per lane loaded together in the final rescan
 constexpr double LOG2E_D = 1.4426950408889634;
@@ -259,9 +261,9 @@ struct Part {  // one warp's share of a pass
 };
 
 // Entries of the segment arrays: the combines give lane l segments 4 l ..
-// 4 l + 3 of the at most TW * TMAXC segments, and write all 4 * 32.
+// 4 l + 3 of the at most TW_MAX * TMAXC segments, and write all 4 * 32.
 constexpr int SEG_SLOTS = 4 * 32;
-static_assert(TW * TMAXC <= SEG_SLOTS, "every segment has an entry");
+static_assert(TW_MAX * TMAXC <= SEG_SLOTS, "every segment has an entry");
 
 struct TreeSmem {
   int32_t parent[SV_TREE_MAX_N];
@@ -272,18 +274,18 @@ struct TreeSmem {
   float xl_d[SV_TREE_MAX_N];
   float ua[SV_TREE_MAX_N];    // accept uniform of each child of the current node
   float ur;                   // residual uniform of the current node
-  Part part[2][2][TW];    // [buffer][target, draft][warp], alternating per pass
+  Part part[2][2][TW_MAX];  // [buffer][target, draft][warp], alternating per pass
   // running mass after each segment (index order), and each segment's mass;
   // the combines write 4 entries per lane of a warp, whatever the segment count
   FF seg_incl[SEG_SLOTS];
   FF seg_tot[SEG_SLOTS];
-  FF piece[TW];
+  FF piece[TW_MAX];
   float mt, md;
   FF St, Sd, Z;
   float K;
   int accept, seg_pick, degenerate;
   int abort;                      // a ring wait gave up (the call's results are void)
-  unsigned long long bar[TW][NS];  // per-warp ring slots: bytes arrived
+  unsigned long long bar[TW_MAX][NS];  // per-warp ring slots: bytes arrived
 };
 
 // Element range of segment g of a row split into nseg contiguous segments.
@@ -544,9 +546,10 @@ __device__ FF mass_lane(const TreeParams& P, TreeSmem& sm, Ring& R, const unsign
   return s;
 }
 
-// Combine of a mass pass (warp 0): the partials of all 16 c segments, read
+// Combine of a mass pass (warp 0): the partials of all TW c segments, read
 // from every CTA of the cluster in index order (lane l holds segments
 // 4 l .. 4 l + 3), into the segment totals, their running sums and the total.
+template <int TW>
 __device__ void combine_mass(cg::cluster_group& cluster, TreeSmem& sm, int buf, int nseg,
                              int lane) {
   FF t[4], run{0.f, 0.f};
@@ -577,9 +580,10 @@ __device__ void combine_mass(cg::cluster_group& cluster, TreeSmem& sm, int buf, 
 // The walk of one request by one cluster.  Every CTA of the cluster runs the
 // same control flow: decisions are taken from values that each CTA combines
 // from the same partials in the same order.
-template <int DT>
-__global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
+template <int DT, int TW>
+__global__ void __launch_bounds__(32 * TW, TW_MAX / TW) sv_tree_walk(const TreeParams P) {
   using E = TE<DT>;
+  constexpr int TTHR = 32 * TW;
   __shared__ TreeSmem sm;
   extern __shared__ __align__(128) unsigned char ring_mem[];
   cg::cluster_group cluster = cg::this_cluster();
@@ -779,7 +783,7 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
         if (lane == 0) sm.part[buf][0][warp] = Part{0.f, s.h, s.l, 0.f};
       }
       cluster.sync();
-      if (warp == 0) combine_mass(cluster, sm, buf, nseg, lane);
+      if (warp == 0) combine_mass<TW>(cluster, sm, buf, nseg, lane);
       buf ^= 1;
       __syncthreads();
       if (tid == 0) {
@@ -814,7 +818,7 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
       const FF s = warp_sum(mass_lane<DT>(P, sm, R, rt, rd, a, e, mt, md, kf, 0.f, lane));
       if (lane == 0) sm.part[buf][0][warp] = Part{0.f, s.h, s.l, 0.f};
       cluster.sync();
-      if (warp == 0) combine_mass(cluster, sm, buf, nseg, lane);
+      if (warp == 0) combine_mass<TW>(cluster, sm, buf, nseg, lane);
       buf ^= 1;
       __syncthreads();
     }
@@ -880,7 +884,7 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
   }
   if (q != gpick / TW) return;
 
-  // rescan the picked segment: 16 pieces, one per warp, then one warp scans
+  // rescan the picked segment: TW pieces, one per warp, then one warp scans
   // the piece holding the remaining tau element by element
   const unsigned char* rt = P.Lt + ((long long)b * N + n) * row_bytes;
   const unsigned char* rd = Kseg != 0.f ? P.Ld + ((long long)b * N + n) * row_bytes : nullptr;
@@ -962,8 +966,18 @@ __global__ void __launch_bounds__(TTHR, 1) sv_tree_walk(const TreeParams P) {
 }
 
 int g_cluster = 0;
+int g_warps = 0;
 std::mutex g_tree_mu;
 int g_sms[64] = {};
+
+template <int TW>
+bool set_ring_smem() {
+  return cudaFuncSetAttribute(sv_tree_walk<SV_F32, TW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(ring_bytes(TW))) == cudaSuccess &&
+         cudaFuncSetAttribute(sv_tree_walk<SV_BF16, TW>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(ring_bytes(TW))) == cudaSuccess;
+}
 
 int sms_of_device(int& sms) {
   int dev = 0;
@@ -972,10 +986,7 @@ int sms_of_device(int& sms) {
   if (!g_sms[dev]) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(sv_tree_walk<SV_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(RING_BYTES)) != cudaSuccess ||
-        cudaFuncSetAttribute(sv_tree_walk<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(RING_BYTES)) != cudaSuccess)
+        !set_ring_smem<TW_MAX>() || !set_ring_smem<TW_MIN>())
       return SV_ERR_CUDA;
     g_sms[dev] = n;
   }
@@ -988,6 +999,12 @@ int sms_of_device(int& sms) {
 extern "C" int sv_tree_set_cluster(int ctas) {
   if (ctas < 0 || ctas > TMAXC) return SV_ERR_INVALID_ARG;
   g_cluster = ctas;
+  return SV_OK;
+}
+
+extern "C" int sv_tree_set_warps(int warps) {
+  if (warps != 0 && warps != TW_MIN && warps != TW_MAX) return SV_ERR_INVALID_ARG;
+  g_warps = warps;
   return SV_OK;
 }
 
@@ -1010,9 +1027,14 @@ extern "C" int sv_tree_verify(int dtype, const void* target_logits, const void* 
     return SV_ERR_INVALID_ARG;
   int sms = 0;
   if (int rc = sms_of_device(sms)) return rc;
+  // CTA width: two CTAs of 8 warps per SM up to a batch of 0.8 requests per
+  // SM (a second CTA runs while one waits at a barrier, and small batches
+  // get their rows in more segments), one of 16 above (measured crossover
+  // between 112 and 128 requests on 152 SMs)
+  const int tw = g_warps ? g_warps : (5 * (long long)B <= 4LL * sms ? TW_MIN : TW_MAX);
   int c = g_cluster;
   if (c == 0) {
-    c = sms / B;
+    c = int((long long)sms * (TW_MAX / tw) / B);
     c = c < 1 ? 1 : (c > TMAXC ? TMAXC : c);
   }
   if ((long long)B * c > 0x7fffffffLL) return SV_ERR_INVALID_ARG;
@@ -1035,8 +1057,8 @@ extern "C" int sv_tree_verify(int dtype, const void* target_logits, const void* 
                    reinterpret_cast<uintptr_t>(draft_logits)) & 15) == 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(B) * unsigned(c));
-  cfg.blockDim = dim3(TTHR);
-  cfg.dynamicSmemBytes = RING_BYTES;
+  cfg.blockDim = dim3(unsigned(32 * tw));
+  cfg.dynamicSmemBytes = ring_bytes(tw);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1045,7 +1067,12 @@ extern "C" int sv_tree_verify(int dtype, const void* target_logits, const void* 
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  const cudaError_t err = dtype == SV_F32 ? cudaLaunchKernelEx(&cfg, sv_tree_walk<SV_F32>, P)
-                                          : cudaLaunchKernelEx(&cfg, sv_tree_walk<SV_BF16>, P);
+  cudaError_t err;
+  if (tw == TW_MIN)
+    err = dtype == SV_F32 ? cudaLaunchKernelEx(&cfg, sv_tree_walk<SV_F32, TW_MIN>, P)
+                          : cudaLaunchKernelEx(&cfg, sv_tree_walk<SV_BF16, TW_MIN>, P);
+  else
+    err = dtype == SV_F32 ? cudaLaunchKernelEx(&cfg, sv_tree_walk<SV_F32, TW_MAX>, P)
+                          : cudaLaunchKernelEx(&cfg, sv_tree_walk<SV_BF16, TW_MAX>, P);
   return err == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

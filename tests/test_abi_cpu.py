@@ -197,6 +197,10 @@ def test_tree_validation(L):
     assert L.sv_tree_set_cluster(9) == binding.SV_ERR_INVALID_ARG
     assert L.sv_tree_set_cluster(-1) == binding.SV_ERR_INVALID_ARG
     assert L.sv_tree_set_cluster(0) == binding.SV_OK
+    for w in (1, 12, 32, -8):
+        assert L.sv_tree_set_warps(w) == binding.SV_ERR_INVALID_ARG
+    for w in (8, 16, 0):
+        assert L.sv_tree_set_warps(w) == binding.SV_OK
 
 
 def test_window_host_mirror_matches_oracle():

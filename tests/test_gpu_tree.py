@@ -29,6 +29,7 @@ def _gpu():
     binding.lib()
     yield
     binding.sv_tree_set_cluster(0)
+    binding.sv_tree_set_warps(0)
 
 
 def _t(a):
@@ -114,17 +115,36 @@ def test_tree_sweep(V, shape, dtype):
     compare_tree(ti, run_tree(ti), oracle_tree(ti))
 
 
+@pytest.mark.parametrize("warps", [8, 16])
 @pytest.mark.parametrize("ctas", [1, 2, 3, 5, 8])
-def test_tree_cluster_sizes(ctas):
-    """Every cluster size gives the oracle's walk (the segment split differs,
-    so only rounding may move; flagged requests excepted)."""
+def test_tree_cluster_sizes(ctas, warps):
+    """Every cluster size and CTA width gives the oracle's walk (the segment
+    split differs, so only rounding may move; flagged requests excepted)."""
     cfg = synth.custom_config(12, 0, 30011, "bf16", "mix", temp=1.0)
     ti = synth.make_tree_inputs(cfg, SHAPES["b3211"], seed=71)
     binding.sv_tree_set_cluster(ctas)
+    binding.sv_tree_set_warps(warps)
     try:
         compare_tree(ti, run_tree(ti), oracle_tree(ti))
     finally:
         binding.sv_tree_set_cluster(0)
+        binding.sv_tree_set_warps(0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", sorted(SHAPES))
+@pytest.mark.parametrize("V", [1, 33, 4099, 20011])
+def test_tree_sweep_sixteen_warps(V, shape, dtype):
+    """The sweep's cases with CTAs of 16 warps (the automatic choice takes 8
+    at these batch sizes)."""
+    cfg = synth.custom_config(6, 0, V, dtype, "normal", temp=("uniform", 0.6, 1.4))
+    ti = synth.make_tree_inputs(cfg, SHAPES[shape], seed=700 + V)
+    binding.sv_tree_set_warps(16)
+    try:
+        compare_tree(ti, run_tree(ti), oracle_tree(ti))
+    finally:
+        binding.sv_tree_set_warps(0)
+
 
 
 def test_tree_star_many_rejections():
