@@ -2527,9 +2527,18 @@ __global__ void __launch_bounds__(32 * SAMPLE_WARPS) sv_sample(const Params P) {
   wait_previous_kernel();
   const Partial* pp = P.part + size_t(r) * P.np1;
   const int np = P.np1;
+  // at most one partial per thread (the usual case): each thread loads its
+  // partial once, and the scan that gives S below is also the scan of the
+  // partials in index order that step 3 needs
+  const bool one_round = np <= NT;
+  float4 pv = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+  if (one_round && tid < np) pv = __ldg(reinterpret_cast<const float4*>(pp + tid));
   // 1. the row maximum over the partials' maxima (NaN shows in the sums)
   float m = -INFINITY;
-  for (int q = tid; q < np; q += NT) m = fmaxf(m, __ldg(&pp[q].a));
+  if (one_round)
+    m = fmaxf(m, pv.x);
+  else
+    for (int q = tid; q < np; q += NT) m = fmaxf(m, __ldg(&pp[q].a));
   m = warp_max(m);
   if (lane == 0) wmax[warp] = m;
   __syncthreads();
@@ -2537,9 +2546,13 @@ __global__ void __launch_bounds__(32 * SAMPLE_WARPS) sv_sample(const Params P) {
   for (int w = 1; w < NW; ++w) m = fmaxf(m, wmax[w]);
   // 2. the normaliser S, the sum of the partials' masses
   FF part = ff(0.f);
-  for (int q = tid; q < np; q += NT) ff_add(part.h, part.l, partial_mass(pp, q, m, kf));
+  if (one_round) {
+    if (tid < np) ff_add(part.h, part.l, (m == -INFINITY) ? pv.y : pv.y * ex2((pv.x - m) * kf));
+  } else {
+    for (int q = tid; q < np; q += NT) ff_add(part.h, part.l, partial_mass(pp, q, m, kf));
+  }
   FF S;
-  block_scan_ff<NW>(part, wsum, S);
+  const FF incl_part = block_scan_ff<NW>(part, wsum, S);
   const double Sd = ff_val(S.h, S.l);
   const bool ok = t_ok && row_ok(m, Sd);  // the same in every thread
   if (!ok) {
@@ -2552,10 +2565,21 @@ __global__ void __launch_bounds__(32 * SAMPLE_WARPS) sv_sample(const Params P) {
     }
     return;
   }
-  // 3. the crossing partial, in rounds of NT partials
+  // 3. the crossing partial, in rounds of NT partials (with one round, from
+  // the scan of step 2: thread q holds partial q alone)
   const FF tau = ff_mul(u, S);
   FF base = ff(0.f);
-  for (int q0 = 0; q0 < np; q0 += NT) {
+  if (one_round) {
+    const int q = tid;
+    const FF z = part;
+    const bool pos = q < np && ff_pos(z);
+    if (pos && ff_gt(base + incl_part, tau)) atomicMin(&sh_hit, q);
+    if (pos) atomicMax(&sh_last, q);
+    __syncthreads();
+    if (q == sh_hit) sh_rest = tau - (base + (incl_part - z));
+    if (q == sh_last) sh_rest_last = z;
+  }
+  for (int q0 = 0; !one_round && q0 < np; q0 += NT) {
     const int q = q0 + tid;
     const FF z = ff(q < np ? partial_mass(pp, q, m, kf) : 0.f);
     FF rtot;

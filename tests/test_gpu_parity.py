@@ -109,13 +109,15 @@ def test_workload2_greedy_full_size():
 
 # ------------------------------------------------------------------ greedy
 
+@pytest.mark.parametrize("gamma", [2, 4])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("V", [1, 7, 513, 20011, 70000])
-def test_greedy_planted_ties(V, dtype):
+def test_greedy_planted_ties(V, dtype, gamma):
     """Ties inside a vector, across vectors and across phase-1 chunks; the
     lowest index must win; draft tokens equal to the argmax for a random
-    prefix, then a mismatch."""
-    cfg = synth.custom_config(24, 4, V, dtype, "greedy")
+    prefix, then a mismatch.  gamma = 2 takes the decision kernel's
+    four-warp form (R <= 4), gamma = 4 its sixteen-warp form."""
+    cfg = synth.custom_config(24, gamma, V, dtype, "greedy")
     inp = synth.make_inputs(cfg, seed=V)
     wide = synth.widen(inp.Lt, inp.dtype)
     rng = np.random.default_rng(V)
