@@ -916,8 +916,9 @@ def main():
                     help="approximate seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-requests", type=int, default=32)
     ap.add_argument("--chunk", type=int, default=0, help="phase-1 chunk elements (0 = auto)")
-    ap.add_argument("--tail", type=int, default=0, choices=[0, 1, 2],
-                    help="kernels after the reduce: 0 automatic, 1 decide/residual/draw, 2 fused")
+    ap.add_argument("--tail", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="kernels of a sampling call: 0 automatic, 1 reduce + decide/residual/"
+                         "draw, 2 reduce + fused tail, 3 one kernel")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

@@ -144,8 +144,9 @@ def sv_test_withhold_slot(enable: bool) -> None:
 
 
 def sv_set_tail(mode: int = 0) -> None:
-    """Kernels after the reduce in sampling calls: 0 automatic, 1 the
-    decide / residual / draw kernels, 2 the fused tail."""
+    """Kernels of sampling calls: 0 automatic, 1 the reduce and the decide /
+    residual / draw kernels, 2 the reduce and the fused tail, 3 one kernel
+    (a cluster per request streams its rows, then decides and draws)."""
     _check(lib().sv_set_tail(mode))
 
 

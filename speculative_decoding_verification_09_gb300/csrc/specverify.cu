@@ -104,7 +104,8 @@ struct Ctrl {                 // 64 bytes at the start of the workspace
   // claims counts the reduce's claims of pool units (reset by the call's last kernel)
   unsigned long long state, claims;
   unsigned long long pad[6];  // pad[0]: the residual kernel's chunk-claim counter;
-                              // pad[1]: pool units the reduce's CTAs took (0 between calls)
+                              // pad[1]: pool units the reduce's CTAs took (0 between calls);
+                              // pad[2]: CTAs of the one-kernel path done (0 between calls)
 };
 struct Partial {              // per (request, position, chunk, consumer warp)
   float a, b, c, d;           // sampling: m_t, s_t, m_d, s_d; greedy: value, index, nan, 0
@@ -1033,11 +1034,11 @@ __device__ long long reduce_pool_units(const Params& P, long long nb) {
 // two consecutive target chunks of one range instead (a pair), so every
 // slot still carries up to two half-slots of logits.
 template <int DT, bool GREEDY, bool PAIRS>
-__device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* slots) {
+__device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* slots,
+                         const Split sp) {
   using E = Elem<DT>;
   using G = GeoReduce;
   constexpr int NS = G::NS, SLOT = G::SLOT, HALF = G::HALF;
-  const Split sp = reduce_split(P, blockIdx.x, gridDim.x);
   long long t = sp.t0, tend = sp.t1;  // the range being streamed
   unsigned long long taken = 0;       // pool units this CTA took
   auto report = [&]() {
@@ -1256,7 +1257,8 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
   }
   __syncthreads();
   if (threadIdx.x < 32) {
-    if (threadIdx.x == 0) producer<DT, GREEDY, PAIRS>(P, C, slots);
+    if (threadIdx.x == 0)
+      producer<DT, GREEDY, PAIRS>(P, C, slots, reduce_split(P, blockIdx.x, gridDim.x));
   } else {
     consumer<DT, GREEDY, PAIRS, CONTIG>(P, C, slots);
   }
@@ -1267,13 +1269,20 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
 // Combine of row i of request b (one warp): the maximum m of the partials'
 // maxima and S = sum s_c * 2^((m_c - m) * kf), accumulated as float pairs.
 // Target in fields (a, b), draft in (c, d).  Result valid in every lane.
+// NC: the partials were written by an earlier kernel (read-only cache path);
+// otherwise by this kernel's cluster, read with plain loads.
+template <bool NC = true>
+__device__ __forceinline__ float4 load_partial(const Partial* p) {
+  return NC ? __ldg(reinterpret_cast<const float4*>(p)) : *reinterpret_cast<const float4*>(p);
+}
+template <bool NC = true>
 __device__ void row_combine(const Partial* pp, int np, float kf, bool draft, float& mt,
                             FF& St, float& md, FF& Sd) {
   const int lane = threadIdx.x & 31;
   mt = -INFINITY;
   md = -INFINITY;
   for (int c = lane; c < np; c += 32) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(pp + c));
+    const float4 v = load_partial<NC>(pp + c);
     mt = fmaxf(mt, v.x);
     md = fmaxf(md, v.z);
   }
@@ -1281,7 +1290,7 @@ __device__ void row_combine(const Partial* pp, int np, float kf, bool draft, flo
   md = warp_max(md);
   float th = 0.f, tl = 0.f, dh = 0.f, dl = 0.f;
   for (int c = lane; c < np; c += 32) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(pp + c));
+    const float4 v = load_partial<NC>(pp + c);
     ff_add(th, tl, (mt == -INFINITY) ? v.y : v.y * ex2((v.x - mt) * kf));
     if (draft) ff_add(dh, dl, (md == -INFINITY) ? v.w : v.w * ex2((v.z - md) * kf));
   }
@@ -1514,7 +1523,7 @@ __device__ __forceinline__ void load_decision_inputs(const Params& P, int b, flo
 // Every row's statistics of request b for the sampling decision, the warps of
 // the CTA taking rows in turn: the partials combined (row_combine), or the
 // draft row's normaliser as given (dst_sh, cached verification).
-template <int NWARPS>
+template <int NWARPS, bool NC = true>
 __device__ void combine_rows(const Params& P, int b, float kf, const float2* dst_sh,
                              RowStat* rows) {
   const int warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -1524,7 +1533,7 @@ __device__ void combine_rows(const Params& P, int b, float kf, const float2* dst
     const Partial* pp = P.part + (size_t(b) * R + i) * size_t(P.np1);
     float mt, md;
     FF St, Sd;
-    row_combine(pp, P.np1, kf, i < P.gs, mt, St, md, Sd);
+    row_combine<NC>(pp, P.np1, kf, i < P.gs, mt, St, md, Sd);
     if (cached && i < g) {  // the draft row's normaliser, as given
       md = dst_sh[i].x;
       Sd = ff(dst_sh[i].y);
@@ -2201,6 +2210,9 @@ __global__ void __launch_bounds__(32 * DRAW_WARPS) sv_draw(const Params P) {
 // SV_ST_DEGENERATE).
 constexpr int FIN_WARPS = 16;
 constexpr int FIN_MAXC = 8;  // CTAs per cluster (the portable limit)
+// automatic choice for batches of at least two SMs per request: the whole call
+// in one kernel (sv_onecall) rather than the reduce and the fused tail
+constexpr bool ONECALL_AUTO = false;
 
 // Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
 __device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
@@ -2214,12 +2226,16 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int DT>
-__global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
+// Steps 1-4 for request b of this CTA's cluster, the request's partials in
+// P.part (NC: written by an earlier kernel; else by this cluster, visible
+// after a cluster barrier).  The decision inputs and the given draft
+// normalisers (dst_sh) were loaded by the caller.
+template <int DT, bool NC>
+__device__ void finish_request(const Params& P, const float2* dst_sh, float lt, float ld, float u,
+                               bool tok_ok, int xi) {
   using E = Elem<DT>;
   __shared__ RowStat rows[MAXR];
   __shared__ Cand cand[MAXR];
-  __shared__ float2 dst_sh[MAXR];
   __shared__ int2 mode_k;
   __shared__ Record rec;
   __shared__ FF seg_mass[2][FIN_WARPS];  // [pass][warp]: read by every CTA of the cluster
@@ -2233,26 +2249,10 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
   const int warp = int(threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int g = P.gamma, R = P.R, V = P.V;
   const int nseg = FIN_WARPS * c;
-  // the call's inputs, before the wait
-  float lt, ld, u;
-  bool tok_ok;
-  int xi;
-  load_decision_inputs<DT>(P, b, lt, ld, u, tok_ok, xi);
   const float kf = LOG2E_F / __ldg(P.temp + b);
-  const bool cached = P.dstats != nullptr;
-  if (cached && int(threadIdx.x) < g)
-    dst_sh[threadIdx.x] = __ldg(reinterpret_cast<const float2*>(P.dstats) + size_t(b) * g +
-                                threadIdx.x);
-  // the next call's reduce may be placed as SMs free up: it waits for this
-  // grid's completion before it reads anything
-  allow_next_kernel();
-  wait_previous_kernel();  // the partials
-  // the reduce has completed: the control block is ready for the next call
-  if (blockIdx.x == 0 && threadIdx.x == 0) ready_for_next_call(P);
-  __syncthreads();
 
   // 1. rows and decision
-  combine_rows<FIN_WARPS>(P, b, kf, dst_sh, rows);
+  combine_rows<FIN_WARPS, NC>(P, b, kf, dst_sh, rows);
   __syncthreads();
   if (warp == 1) record_candidates(P, b, rows, cand);
   if (warp == 0) {
@@ -2435,6 +2435,122 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
     }
   }
   cluster_wait();
+}
+
+template <int DT>
+__global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
+  __shared__ float2 dst_sh[MAXR];
+  const int b = int(blockIdx.x) / int(cooperative_groups::this_cluster().num_blocks());
+  const int g = P.gamma;
+  // the call's inputs, before the wait
+  float lt, ld, u;
+  bool tok_ok;
+  int xi;
+  load_decision_inputs<DT>(P, b, lt, ld, u, tok_ok, xi);
+  if (P.dstats != nullptr && int(threadIdx.x) < g)
+    dst_sh[threadIdx.x] = __ldg(reinterpret_cast<const float2*>(P.dstats) + size_t(b) * g +
+                                threadIdx.x);
+  // the next call's reduce may be placed as SMs free up: it waits for this
+  // grid's completion before it reads anything
+  allow_next_kernel();
+  wait_previous_kernel();  // the partials
+  // the reduce has completed: the control block is ready for the next call
+  if (blockIdx.x == 0 && threadIdx.x == 0) ready_for_next_call(P);
+  __syncthreads();
+  finish_request<DT, true>(P, dst_sh, lt, ld, u, tok_ok, xi);
+}
+
+// CTA q of c's share of request b's chunks, when the request's cluster
+// streams it: equal parts of its weight (streamed bytes), no pool.
+__device__ __forceinline__ Split request_split(const Params& P, int b, int q, int c) {
+  const long long w_req = (long long)P.nch1 * (P.R + P.gs);
+  const long long w0 = (long long)b * w_req;
+  Split sp;
+  sp.t0 = task_at_weight(P, w0 + (w_req * q + c - 1) / c);
+  sp.t1 = task_at_weight(P, w0 + (w_req * (q + 1) + c - 1) / c);
+  sp.ts = P.tasks;
+  sp.unit = 1;
+  sp.nunits = 0;
+  return sp;
+}
+
+// The whole call in one kernel, for batches that leave at least two SMs per
+// request: one cluster of c CTAs per request streams the request's rows
+// (this CTA's share of its chunks through the reduce's ring: producer lane,
+// consumer warps 1..NCW, per-warp partials into P.part), then, after a
+// cluster barrier, takes the decision, the residual mass and the draw as the
+// fused tail does.  The rows token k is drawn from were streamed by the same
+// cluster moments before, so that second pass reads them from L2.  The last
+// CTA to finish (counted in the control block's pad[2]) puts the workspace
+// back in its ready state.
+template <int DT, bool PAIRS>
+__global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_onecall(const Params P) {
+  using G = GeoReduce;
+  static_assert(FIN_WARPS >= NCW + 1, "a producer warp and the consumer warps");
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* slots = smem;
+  SmemCtl<G>& C = *reinterpret_cast<SmemCtl<G>*>(smem + size_t(G::NS) * G::SLOT);
+  __shared__ float2 dst_sh[MAXR];
+  cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+  const int c = int(cluster.num_blocks()), q = int(cluster.block_rank());
+  const int b = int(blockIdx.x) / c;
+  const int warp = int(threadIdx.x >> 5), g = P.gamma;
+  if (threadIdx.x == 0) {
+    C.abort = 0;
+    for (int s = 0; s < G::NS; ++s) {
+      mbar_init(&C.full[s], 1);
+      mbar_init(&C.empty[s], G::GW);
+    }
+  }
+  // the next call's first kernel waits for this grid's completion
+  allow_next_kernel();
+  // launched programmatically after the previous kernel in the stream
+  // (whatever wrote the logits, or an earlier call): nothing it wrote is
+  // read before it has completed, the call's inputs included
+  wait_previous_kernel();
+  // the control block's ready state (only the state word is tested here; the
+  // counters are checked by the last CTA to finish).  A workspace found busy
+  // also gets its finish count cleared: no CTA of this grid can have counted
+  // itself before block 0 starts, as each counts only after its request.
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (P.ctrl->state != 0ull) {
+      set_status(P, SV_ST_WORKSPACE);
+      P.ctrl->pad[2] = 0ull;
+    }
+    P.ctrl->state = 1ull;
+  }
+  // the decision's inputs: loaded now, used after the stream
+  float lt, ld, u;
+  bool tok_ok;
+  int xi;
+  load_decision_inputs<DT>(P, b, lt, ld, u, tok_ok, xi);
+  if (P.dstats != nullptr && int(threadIdx.x) < g)
+    dst_sh[threadIdx.x] = __ldg(reinterpret_cast<const float2*>(P.dstats) + size_t(b) * g +
+                                threadIdx.x);
+  __syncthreads();
+  if (warp == 0) {
+    if (threadIdx.x == 0) producer<DT, false, PAIRS>(P, C, slots, request_split(P, b, q, c));
+  } else if (warp <= NCW) {
+    consumer<DT, false, PAIRS, false>(P, C, slots);
+  }
+  __syncthreads();
+  cluster.sync();  // every CTA's partials of the request are written
+  finish_request<DT, false>(P, dst_sh, lt, ld, u, tok_ok, xi);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&P.ctrl->pad[2], 1ull) == (unsigned long long)gridDim.x - 1ull) {
+      __threadfence();
+      // this path takes no pool units and no chunk claims: counters left
+      // non-zero by another call's work mean the workspace was not ready
+      if (P.ctrl->claims != 0ull || P.ctrl->pad[1] != 0ull) set_status(P, SV_ST_WORKSPACE);
+      P.ctrl->claims = 0ull;
+      P.ctrl->pad[0] = 0ull;
+      P.ctrl->pad[1] = 0ull;
+      P.ctrl->pad[2] = 0ull;
+      P.ctrl->state = 0ull;
+    }
+  }
 }
 
 // ---------------------------------------------------------- draft sampling
@@ -2668,7 +2784,7 @@ __global__ void __launch_bounds__(32 * SAMPLE_WARPS) sv_sample(const Params P) {
 
 struct Tuning {
   int chunk = 0;
-  int tail = 0;                  // 0: automatic, 1: decide/residual/draw, 2: fused (sv_set_tail)
+  int tail = 0;  // 0: automatic, 1: decide/residual/draw, 2: fused tail, 3: one kernel (sv_set_tail)
   int withhold_slot = 0;         // failure-handling test (sv_test_withhold_slot)
   cudaEvent_t stage_ev[5] = {};  // profiling: events recorded around the kernels
   int stage_n = 0;
@@ -2685,6 +2801,11 @@ DevCache g_dev[64];
 template <int DT>
 bool prepare_kernel() {
   const int r = int(smem_bytes<GeoReduce>());
+  if (cudaFuncSetAttribute(sv_onecall<DT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, r) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(sv_onecall<DT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, r) !=
+          cudaSuccess)
+    return false;
   return cudaFuncSetAttribute(sv_residual<DT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(smem_bytes<GeoResidual>())) == cudaSuccess &&
          cudaFuncSetAttribute(sv_residual<DT, false>,
@@ -2737,13 +2858,13 @@ cudaError_t launch_after(void (*kern)(KArgs...), unsigned grid, unsigned block, 
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 // The same, in clusters of `cluster` CTAs along x.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_after_cluster(void (*kern)(KArgs...), unsigned grid, unsigned block,
-                                 unsigned cluster, cudaStream_t st, Args... args) {
+template <typename K>
+cudaError_t launch_after_cluster(K kern, unsigned grid, unsigned block, unsigned cluster,
+                                 cudaStream_t st, const Params& P, size_t smem) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -2754,7 +2875,7 @@ cudaError_t launch_after_cluster(void (*kern)(KArgs...), unsigned grid, unsigned
   at[1].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
+  return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 // One library call: which path, and its arguments as the C ABI gives them.
@@ -2824,14 +2945,26 @@ int launch(const Call& a) {
   const int chmax = GeoReduce::HALF / ES;     // a phase-1 chunk fits half a slot
   const int chmax2 = GeoResidual::HALF / ES;  // phase 2 likewise
 
+  // the tail after the reduce: for batches that leave at least two SMs per
+  // request, one fused kernel with a cluster of fc CTAs per request
+  int fc = 0;
+  bool one = false;  // the whole call in one kernel (sv_onecall) with clusters of fc CTAs
+  if (!greedy && !draft) {
+    const int per = min(FIN_MAXC, sms / B);
+    if (g_tune.tail == 2 || g_tune.tail == 3 || (g_tune.tail == 0 && per >= 2)) fc = max(1, per);
+    one = fc > 0 && (g_tune.tail == 3 || (g_tune.tail == 0 && ONECALL_AUTO));
+  }
+
   // phase-1 chunk: at most half a slot, at least CH1_MIN (or the whole row),
-  // and small enough that every SM gets several tasks
+  // and small enough that every SM gets several tasks (in one-kernel calls:
+  // that every CTA of a request's cluster gets two)
   int ch1;
   if (g_tune.chunk > 0) {
     ch1 = round_up(g_tune.chunk, 64);
   } else {
     const long long by_bytes = (V + chmax - 1) / chmax;
-    const long long by_tasks = (8LL * min(sms, SMS_CAP) + units - 1) / units;
+    const long long by_tasks = one ? (2LL * fc + R - 1) / R
+                                   : (8LL * min(sms, SMS_CAP) + units - 1) / units;
     const long long want = max(1LL, max(by_bytes, by_tasks));
     ch1 = round_up((V + want - 1) / want, 64);
   }
@@ -2878,15 +3011,14 @@ int launch(const Call& a) {
   };
   mark(0);
   cudaError_t e = cudaSuccess;
-  // the tail after the reduce: for batches that leave at least two SMs per
-  // request, one fused kernel with a cluster of fc CTAs per request
-  int fc = 0;
-  if (!greedy && !draft) {
-    const int per = min(FIN_MAXC, sms / B);
-    if (g_tune.tail == 2 || (g_tune.tail == 0 && per >= 2)) fc = max(1, per);
-  }
   auto run = [&](auto reduce_k, auto decide_k, auto decide_small_k, auto residual_k, auto draw_k,
-                 auto sample_k, auto finish_k) {
+                 auto sample_k, auto finish_k, auto onecall_k) {
+    if (one) {
+      e = launch_after_cluster(onecall_k, unsigned(B) * unsigned(fc), 32 * FIN_WARPS,
+                               unsigned(fc), st, P, smem_bytes<GeoReduce>());
+      mark(1);
+      return;
+    }
     // programmatic launch: the reduce's CTAs may be placed while the previous
     // kernel in the stream finishes; it waits for that kernel on the device
     e = launch_after(reduce_k, grid, NTHR, smem_bytes<GeoReduce>(), st, P);
@@ -2900,7 +3032,7 @@ int launch(const Call& a) {
     if (fc > 0) {
       if (e == cudaSuccess)
         e = launch_after_cluster(finish_k, unsigned(B) * unsigned(fc), 32 * FIN_WARPS,
-                                 unsigned(fc), st, P);
+                                 unsigned(fc), st, P, size_t(0));
       mark(2);
       return;
     }
@@ -2925,23 +3057,25 @@ int launch(const Call& a) {
                             (size_t(V) * ES) % 16 == 0;
   auto dispatch = [&](auto dt) {
     constexpr int D = decltype(dt)::value;
-    auto go = [&](auto reduce_k, auto greedy_c) {
+    auto go = [&](auto reduce_k, auto greedy_c, auto pairs_c) {
       constexpr bool GR = decltype(greedy_c)::value;
+      constexpr bool PR = decltype(pairs_c)::value;  // the one-kernel path's slots: target pairs
       auto dk = sv_decide<D, GR, DECIDE_WARPS>;
       auto dks = sv_decide<D, GR, DECIDE_WARPS_SMALL>;
+      auto ok = sv_onecall<D, PR>;
       if (aligned_rows)
-        run(reduce_k, dk, dks, sv_residual<D, true>, sv_draw<D>, sv_sample<D>, sv_finish<D>);
+        run(reduce_k, dk, dks, sv_residual<D, true>, sv_draw<D>, sv_sample<D>, sv_finish<D>, ok);
       else
-        run(reduce_k, dk, dks, sv_residual<D, false>, sv_draw<D>, sv_sample<D>, sv_finish<D>);
+        run(reduce_k, dk, dks, sv_residual<D, false>, sv_draw<D>, sv_sample<D>, sv_finish<D>, ok);
     };
     if (greedy)
-      go(sv_reduce<D, true, true, false>, std::true_type());
+      go(sv_reduce<D, true, true, false>, std::true_type(), std::true_type());
     else if (draft)
-      go(sv_reduce<D, false, true, true>, std::false_type());
+      go(sv_reduce<D, false, true, true>, std::false_type(), std::true_type());
     else if (a.kind == CALL_CACHED)
-      go(sv_reduce<D, false, true, false>, std::false_type());
+      go(sv_reduce<D, false, true, false>, std::false_type(), std::true_type());
     else
-      go(sv_reduce<D, false, false, false>, std::false_type());
+      go(sv_reduce<D, false, false, false>, std::false_type(), std::false_type());
   };
   if (a.dtype == SV_F32)
     dispatch(std::integral_constant<int, SV_F32>());
@@ -3112,7 +3246,7 @@ int sv_set_tuning(int chunk_elems) {
 }
 
 int sv_set_tail(int mode) {
-  if (mode < 0 || mode > 2) return SV_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 3) return SV_ERR_INVALID_ARG;
   g_tune.tail = mode;
   return SV_OK;
 }

@@ -102,9 +102,9 @@ def test_stage_events_validation(L):
 
 
 def test_tail_selection_validation(L):
-    assert L.sv_set_tail(3) == binding.SV_ERR_INVALID_ARG
+    assert L.sv_set_tail(4) == binding.SV_ERR_INVALID_ARG
     assert L.sv_set_tail(-1) == binding.SV_ERR_INVALID_ARG
-    for mode in (1, 2, 0):
+    for mode in (1, 2, 3, 0):
         assert L.sv_set_tail(mode) == binding.SV_OK
 
 

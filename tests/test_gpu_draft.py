@@ -17,11 +17,12 @@ from speculative_decoding_verification_09_gb300 import binding, synth
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", autouse=True, params=[1, 2], ids=["tail3", "fused"])
+@pytest.fixture(scope="module", autouse=True, params=[1, 2, 3], ids=["tail3", "fused", "onecall"])
 def _gpu(request):
-    """Every test of the module runs twice: with the decide / residual / draw
-    kernels after the reduce, and with the fused tail (one cluster per
-    request), whatever the batch size."""
+    """Every test of the module runs three times: with the decide / residual /
+    draw kernels after the reduce, with the fused tail (one cluster per
+    request), and as one kernel (the cluster also streams its request's
+    rows), whatever the batch size."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     binding.lib()
