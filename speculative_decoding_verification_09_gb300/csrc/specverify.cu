@@ -1035,14 +1035,15 @@ __device__ long long reduce_pool_units(const Params& P, long long nb) {
 // slot still carries up to two half-slots of logits.
 template <int DT, bool GREEDY, bool PAIRS>
 __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* slots,
-                         const Split sp) {
+                         const Split sp, unsigned long long* pool_ctr,
+                         unsigned long long* taken_ctr) {
   using E = Elem<DT>;
   using G = GeoReduce;
   constexpr int NS = G::NS, SLOT = G::SLOT, HALF = G::HALF;
   long long t = sp.t0, tend = sp.t1;  // the range being streamed
   unsigned long long taken = 0;       // pool units this CTA took
   auto report = [&]() {
-    if (taken) atomicAdd(&P.ctrl->pad[1], taken);
+    if (taken && taken_ctr) atomicAdd(taken_ctr, taken);
   };
   // a claim is issued while the current range still has NS tasks to go, so
   // its round trip is hidden behind the slots in flight
@@ -1050,7 +1051,7 @@ __device__ void producer(const Params& P, SmemCtl<GeoReduce>& C, unsigned char* 
   bool pending = false;
   auto claim = [&]() {
     if (sp.nunits > 0) {
-      claimed = (long long)atomicAdd(&P.ctrl->claims, 1ull);
+      claimed = (long long)atomicAdd(pool_ctr, 1ull);
       pending = true;
     }
   };
@@ -1258,7 +1259,8 @@ __global__ void __launch_bounds__(NTHR, 1) sv_reduce(const Params P) {
   __syncthreads();
   if (threadIdx.x < 32) {
     if (threadIdx.x == 0)
-      producer<DT, GREEDY, PAIRS>(P, C, slots, reduce_split(P, blockIdx.x, gridDim.x));
+      producer<DT, GREEDY, PAIRS>(P, C, slots, reduce_split(P, blockIdx.x, gridDim.x),
+                                  &P.ctrl->claims, &P.ctrl->pad[1]);
   } else {
     consumer<DT, GREEDY, PAIRS, CONTIG>(P, C, slots);
   }
@@ -2461,16 +2463,20 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_finish(const Params P) {
 }
 
 // CTA q of c's share of request b's chunks, when the request's cluster
-// streams it: equal parts of its weight (streamed bytes), no pool.
+// streams it: like the reduce's split over the whole grid, equal parts of
+// the first (POOL_DIV - 1) / POOL_DIV of the request's weight, the rest a
+// pool of units the cluster's CTAs claim once their part is nearly done.
 __device__ __forceinline__ Split request_split(const Params& P, int b, int q, int c) {
   const long long w_req = (long long)P.nch1 * (P.R + P.gs);
   const long long w0 = (long long)b * w_req;
+  const long long Ws = w_req - w_req / POOL_DIV;
   Split sp;
-  sp.t0 = task_at_weight(P, w0 + (w_req * q + c - 1) / c);
-  sp.t1 = task_at_weight(P, w0 + (w_req * (q + 1) + c - 1) / c);
-  sp.ts = P.tasks;
-  sp.unit = 1;
-  sp.nunits = 0;
+  sp.t0 = task_at_weight(P, w0 + (Ws * q + c - 1) / c);
+  sp.t1 = task_at_weight(P, w0 + (Ws * (q + 1) + c - 1) / c);
+  sp.ts = task_at_weight(P, w0 + Ws);
+  const long long pool = (long long)(b + 1) * P.R * P.nch1 - sp.ts;
+  sp.unit = max(1LL, (pool + 2LL * c - 1) / (2LL * c));  // about two units per CTA
+  sp.nunits = (pool + sp.unit - 1) / sp.unit;
   return sp;
 }
 
@@ -2495,13 +2501,18 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_onecall(const Params P) 
   const int c = int(cluster.num_blocks()), q = int(cluster.block_rank());
   const int b = int(blockIdx.x) / c;
   const int warp = int(threadIdx.x >> 5), g = P.gamma;
+  __shared__ unsigned long long pool_ctr;  // rank 0's counts the cluster's pool claims
   if (threadIdx.x == 0) {
     C.abort = 0;
     for (int s = 0; s < G::NS; ++s) {
       mbar_init(&C.full[s], 1);
       mbar_init(&C.empty[s], G::GW);
     }
+    pool_ctr = 0ull;
   }
+  // the counter is zero in every CTA before any CTA of the cluster claims
+  // (the barrier completes below, after the wait for the previous kernel)
+  cluster_arrive();
   // the next call's first kernel waits for this grid's completion
   allow_next_kernel();
   // launched programmatically after the previous kernel in the stream
@@ -2527,9 +2538,12 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_onecall(const Params P) 
   if (P.dstats != nullptr && int(threadIdx.x) < g)
     dst_sh[threadIdx.x] = __ldg(reinterpret_cast<const float2*>(P.dstats) + size_t(b) * g +
                                 threadIdx.x);
+  cluster_wait();
   __syncthreads();
   if (warp == 0) {
-    if (threadIdx.x == 0) producer<DT, false, PAIRS>(P, C, slots, request_split(P, b, q, c));
+    if (threadIdx.x == 0)
+      producer<DT, false, PAIRS>(P, C, slots, request_split(P, b, q, c),
+                                 cluster.map_shared_rank(&pool_ctr, 0), nullptr);
   } else if (warp <= NCW) {
     consumer<DT, false, PAIRS, false>(P, C, slots);
   }
