@@ -1026,8 +1026,10 @@ __device__ long long reduce_pool_units(const Params& P, long long nb) {
   return reduce_split(P, 0, nb).nunits;
 }
 
-// Producer (one lane): this CTA's static range of chunks, then the pool
-// units it claims, each in order, into the slot ring.  Chunk t is chunk
+// Producer (one lane): the static range of chunks of its split, then the
+// pool units it claims from *pool_ctr (the reduce: a counter in the control
+// block, the count of units taken added to *taken_ctr; the one-kernel path:
+// a counter in its cluster's first CTA), each in order, into the slot ring.  Chunk t is chunk
 // t % nch1 of row t / nch1 (row = b * R + i).  A slot holds a target chunk
 // and the same span of the draft row; where no draft rows are streamed
 // (greedy verification, given draft normalisers, draft sampling) it holds
