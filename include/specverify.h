@@ -226,12 +226,13 @@ int sv_set_tuning(int chunk_elems);
  * batch leaves at least two SMs per request (B * 2 <= SMs) and the
  * decide / residual / draw kernels otherwise; 1 forces the three kernels;
  * 2 forces the fused tail (one kernel, one cluster of up to 8 CTAs per
- * request); 3 runs the whole call as one kernel (one cluster per request
+ * request); 3 runs the whole call as one kernel: one cluster per request
  * streams the request's rows, then decides and draws like the fused tail,
- * its second pass reading the rows the cluster has just streamed).  All
- * compute the same decision and draw the token by the same rule.  Not
- * thread-safe, like sv_set_tuning().  Returns SV_OK, or SV_ERR_INVALID_ARG
- * for a mode outside [0, 3].
+ * its second pass reading the rows the cluster has just streamed (mode 3
+ * also runs greedy calls, spec_verify_greedy, as one kernel; the other
+ * modes leave them as they are).  All compute the same decision and draw
+ * the token by the same rule.  Not thread-safe, like sv_set_tuning().
+ * Returns SV_OK, or SV_ERR_INVALID_ARG for a mode outside [0, 3].
  */
 int sv_set_tail(int mode);
 

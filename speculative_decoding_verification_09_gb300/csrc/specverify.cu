@@ -1310,13 +1310,14 @@ __device__ void row_combine(const Partial* pp, int np, float kf, bool draft, flo
 }
 
 // Argmax of row i of request b (one warp) over its partials.
+template <bool NC = true>
 __device__ void row_argmax(const Partial* pp, int np, float& best, int& bi, int& nan) {
   const int lane = threadIdx.x & 31;
   best = -INFINITY;
   bi = INT_MAX;
   nan = 0;
   for (int c = lane; c < np; c += 32) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(pp + c));
+    const float4 v = load_partial<NC>(pp + c);
     am_merge(best, bi, nan, v.x, __float_as_int(v.y), __float_as_int(v.z));
   }
 #pragma unroll
@@ -2217,6 +2218,8 @@ constexpr int FIN_MAXC = 8;  // CTAs per cluster (the portable limit)
 // automatic choice for batches of at least two SMs per request: the whole call
 // in one kernel (sv_onecall) rather than the reduce and the fused tail
 constexpr bool ONECALL_AUTO = false;
+// the same for greedy calls (the argmax reduce and the decision in one kernel)
+constexpr bool ONECALL_GREEDY_AUTO = false;
 
 // Bulk prefetch of [p, p + bytes) into L2 (p and bytes multiples of 16).
 __device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
@@ -2491,7 +2494,7 @@ __device__ __forceinline__ Split request_split(const Params& P, int b, int q, in
 // cluster moments before, so that second pass reads them from L2.  The last
 // CTA to finish (counted in the control block's pad[2]) puts the workspace
 // back in its ready state.
-template <int DT, bool PAIRS>
+template <int DT, bool GREEDY, bool PAIRS>
 __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_onecall(const Params P) {
   using G = GeoReduce;
   static_assert(FIN_WARPS >= NCW + 1, "a producer warp and the consumer warps");
@@ -2536,22 +2539,49 @@ __global__ void __launch_bounds__(32 * FIN_WARPS, 1) sv_onecall(const Params P) 
   float lt, ld, u;
   bool tok_ok;
   int xi;
-  load_decision_inputs<DT>(P, b, lt, ld, u, tok_ok, xi);
-  if (P.dstats != nullptr && int(threadIdx.x) < g)
+  lt = ld = u = 0.f;
+  tok_ok = true;
+  xi = -1;
+  if (!GREEDY) load_decision_inputs<DT>(P, b, lt, ld, u, tok_ok, xi);
+  if (!GREEDY && P.dstats != nullptr && int(threadIdx.x) < g)
     dst_sh[threadIdx.x] = __ldg(reinterpret_cast<const float2*>(P.dstats) + size_t(b) * g +
                                 threadIdx.x);
   cluster_wait();
   __syncthreads();
   if (warp == 0) {
     if (threadIdx.x == 0)
-      producer<DT, false, PAIRS>(P, C, slots, request_split(P, b, q, c),
-                                 cluster.map_shared_rank(&pool_ctr, 0), nullptr);
+      producer<DT, GREEDY, PAIRS>(P, C, slots, request_split(P, b, q, c),
+                                  cluster.map_shared_rank(&pool_ctr, 0), nullptr);
   } else if (warp <= NCW) {
-    consumer<DT, false, PAIRS, false>(P, C, slots);
+    consumer<DT, GREEDY, PAIRS, false>(P, C, slots);
   }
   __syncthreads();
   cluster.sync();  // every CTA's partials of the request are written
-  finish_request<DT, false>(P, dst_sh, lt, ld, u, tok_ok, xi);
+  if (GREEDY) {
+    // the rows' argmaxes over the cluster's partials and the decision, by
+    // the cluster's first CTA (as the decide kernel takes them)
+    __shared__ RowStat rows[MAXR];
+    if (q == 0) {
+      const int lane = threadIdx.x & 31;
+      for (int i = warp; i < P.R; i += FIN_WARPS) {
+        const Partial* pp = P.part + (size_t(b) * P.R + i) * size_t(P.np1);
+        float best;
+        int bi, nan;
+        row_argmax<false>(pp, P.np1, best, bi, nan);
+        if (lane == 0) {
+          RowStat r;
+          r.mt = best; r.md = 0.f; r.St_h = r.St_l = r.Sd_h = r.Sd_l = 0.f;
+          r.bad = (nan || bi == INT_MAX || best == INFINITY) ? SV_ST_NONFINITE : 0;
+          r.amax = bi;
+          rows[i] = r;
+        }
+      }
+      __syncthreads();
+      if (warp == 0) decide_greedy(P, b, rows);
+    }
+  } else {
+    finish_request<DT, false>(P, dst_sh, lt, ld, u, tok_ok, xi);
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -2817,10 +2847,12 @@ DevCache g_dev[64];
 template <int DT>
 bool prepare_kernel() {
   const int r = int(smem_bytes<GeoReduce>());
-  if (cudaFuncSetAttribute(sv_onecall<DT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, r) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(sv_onecall<DT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, r) !=
-          cudaSuccess)
+  if (cudaFuncSetAttribute(sv_onecall<DT, false, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, r) != cudaSuccess ||
+      cudaFuncSetAttribute(sv_onecall<DT, false, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, r) != cudaSuccess ||
+      cudaFuncSetAttribute(sv_onecall<DT, true, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, r) != cudaSuccess)
     return false;
   return cudaFuncSetAttribute(sv_residual<DT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               int(smem_bytes<GeoResidual>())) == cudaSuccess &&
@@ -2969,6 +3001,10 @@ int launch(const Call& a) {
     const int per = min(FIN_MAXC, sms / B);
     if (g_tune.tail == 2 || g_tune.tail == 3 || (g_tune.tail == 0 && per >= 2)) fc = max(1, per);
     one = fc > 0 && (g_tune.tail == 3 || (g_tune.tail == 0 && ONECALL_AUTO));
+  } else if (greedy) {
+    const int per = min(FIN_MAXC, sms / B);
+    one = g_tune.tail == 3 || (g_tune.tail == 0 && ONECALL_GREEDY_AUTO && per >= 2);
+    if (one) fc = max(1, per);
   }
 
   // phase-1 chunk: at most half a slot, at least CH1_MIN (or the whole row),
@@ -3078,7 +3114,7 @@ int launch(const Call& a) {
       constexpr bool PR = decltype(pairs_c)::value;  // the one-kernel path's slots: target pairs
       auto dk = sv_decide<D, GR, DECIDE_WARPS>;
       auto dks = sv_decide<D, GR, DECIDE_WARPS_SMALL>;
-      auto ok = sv_onecall<D, PR>;
+      auto ok = sv_onecall<D, GR, PR>;
       if (aligned_rows)
         run(reduce_k, dk, dks, sv_residual<D, true>, sv_draw<D>, sv_sample<D>, sv_finish<D>, ok);
       else
