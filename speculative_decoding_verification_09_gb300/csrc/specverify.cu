@@ -36,7 +36,10 @@
 // memory, the token found by the CTA owning the crossing segment).
 // Greedy verification runs reduce (chunk argmax) and decide only; draft
 // sampling runs reduce (contiguous warp shares) and sample (one CTA per draft
-// row: the crossing partial's span, scanned in index order).
+// row: the crossing partial's span, scanned in index order).  On request
+// (sv_set_tail(3)) a sampling or greedy call runs as one kernel, onecall:
+// each request's cluster streams the request's rows through the reduce's
+// ring, then decides (and draws, like finish) from rows still in L2.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <limits.h>
