@@ -10,6 +10,8 @@ then one token in [0, V).  The same 1e-6 as the chain rule: the kernel sums
 each row in float pairs over fp32 vector sums, so a residual mass S_j carries
 a relative error near 1e-7, which the next ratio divides by S_j.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -33,7 +35,7 @@ def _gpu():
 
 
 def _t(a):
-    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    return torch.from_numpy(np.array(a, order="C", copy=True)).to(DEV)
 
 
 def run_tree(ti: synth.TreeInputs, ld_offset: int = 0, no_draft: bool = False) -> dict:
@@ -251,3 +253,30 @@ def test_tree_workload():
     stats = compare_tree(ti, run_tree(ti), oracle_tree(ti))
     print(f"\n{ti.name}: {stats}")
     assert stats["near"] <= ti.B // 8
+
+
+@pytest.mark.parametrize("seed", range(int(os.environ.get("SV_TREE_FUZZ_SEEDS", "24"))))
+def test_tree_fuzz(seed):
+    """Random trees, batches, vocabularies, dtypes, recipes, temperatures and
+    kernel shapes (CTA width, cluster size: automatic or forced) against the
+    oracle."""
+    rng = np.random.default_rng(4000 + seed)
+    B = int(rng.integers(1, 40))
+    N = int(rng.integers(1, 48))
+    V = int(rng.choice([int(rng.integers(1, 64)), int(rng.integers(64, 5000)),
+                        int(rng.integers(5000, 40000))]))
+    dtype = str(rng.choice(["f32", "bf16"]))
+    kind = str(rng.choice(["normal", "zipf", "mix"]))
+    temp = ("uniform", 0.3, 2.0) if rng.random() < 0.5 else float(rng.uniform(0.2, 3.0))
+    cfg = synth.custom_config(B, 0, V, dtype, kind, temp=temp)
+    parents = synth.random_parents(N, 5000 + seed, int(rng.integers(1, 6)))
+    ti = synth.make_tree_inputs(cfg, parents, seed=6000 + seed)
+    warps = int(rng.choice([0, 8, 16]))
+    ctas = int(rng.choice([0, 0, 1, 2, 3, 4, 8]))
+    binding.sv_tree_set_warps(warps)
+    binding.sv_tree_set_cluster(ctas)
+    try:
+        compare_tree(ti, run_tree(ti), oracle_tree(ti))
+    finally:
+        binding.sv_tree_set_warps(0)
+        binding.sv_tree_set_cluster(0)
