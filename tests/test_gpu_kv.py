@@ -1,6 +1,8 @@
 """GPU parity of the KV-cache steps (sv_kv_commit, sv_kv_valid_slots,
 sv_window_block_table) through the C ABI against the oracle on the same
 seeded inputs: integer and byte work, so every comparison is bit-exact."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -151,3 +153,36 @@ def test_window_random(W, blk, K):
     assert got[3] == binding.SV_ST_BAD_LENGTH
     # every length mirror is windowed alike: the host function gives the same lengths
     assert np.array_equal(binding.sv_window_seq_lens_host(seq, W, blk, K), got[0])
+
+
+@pytest.mark.parametrize("seed", range(int(os.environ.get("SV_KV_FUZZ_SEEDS", "24"))))
+def test_commit_fuzz(seed):
+    """Random shapes (batch, layer-heads, staged entries, row size, sinks,
+    window), positions near and far into the ring, accepted counts including
+    dropped requests (-1): pools, positions and valid slots bit-exact with
+    the oracle."""
+    rng = np.random.default_rng(7000 + seed)
+    B = int(rng.integers(1, 20))
+    LH = int(rng.integers(1, 6))
+    R = int(rng.integers(1, 9))
+    D = int(rng.choice([8, 16, 64, 256]))  # int16 elements: rows of 16 .. 512 bytes
+    S = int(rng.integers(0, 5))
+    W = int(rng.integers(R, R + 12))
+    C = S + W
+    kp = rng.integers(-(1 << 15), 1 << 15, size=(B, LH, C, D)).astype(np.int16)
+    vp = rng.integers(-(1 << 15), 1 << 15, size=(B, LH, C, D)).astype(np.int16)
+    kn = rng.integers(-(1 << 15), 1 << 15, size=(B, LH, R, D)).astype(np.int16)
+    vn = rng.integers(-(1 << 15), 1 << 15, size=(B, LH, R, D)).astype(np.int16)
+    pos = rng.integers(0, 4 * C + 3, size=B).astype(np.int32)
+    k = rng.integers(-1, R, size=B).astype(np.int32)
+    gk, gv, gpos, st = _commit(kp, vp, kn, vn, k, pos, S, W)
+    ref = oracle.kv_commit(kp, vp, kn, vn, k, pos, S, W)
+    assert st == 0
+    assert np.array_equal(gk, ref["k_pool"]) and np.array_equal(gv, ref["v_pool"])
+    assert np.array_equal(gpos, ref["pos"])
+    slots, ln, st2 = _valid(gpos, S, W)
+    vref = oracle.kv_valid_slots(gpos, S, W)
+    assert st2 == 0
+    assert np.array_equal(ln, vref["len"])
+    for b in range(B):
+        assert np.array_equal(slots[b, :ln[b]], vref["slots"][b, :vref["len"][b]])
